@@ -1,0 +1,361 @@
+"""Pins for the fp64 CPU oracle, against things other than itself.
+
+- closed forms of the pages' own samples (tests/golden/*.json);
+- central finite differences of L = sum(dY * O) for dQ, dK, dV;
+- torch.nn.functional.scaled_dot_product_attention in float64 with an
+  explicit boolean mask (a library routine), and autograd for its gradients;
+- invariants: softmax rows sum to one, logsumexp of the visible scores,
+  BAND wider than the sequence == sparse_mode 0, keep mask all ones ==
+  no dropout, TND sequence == BNSD with B = 1, Skv = 1 -> out = v,
+  pre = next = 0 -> out_i = v_i, empty rows, dropout bit order checked with
+  numpy.unpackbits;
+- the sampled-row / sampled-column entry points equal the full ones.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from attention_swa_forward_gb300.workloads import Geometry, draw
+from oracle import swa_oracle as orc
+from tests.helpers import to_problem
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _tnd_problem(g, **over):
+    d = dict(layout="TND", B=len(g["cu_seqlens_q"]), N=g["N"], D=g["D"], cu_seqlens_q=g["cu_seqlens_q"],
+             cu_seqlens_kv=g["cu_seqlens_kv"], scale=g["scale"], pre_tokens=g["pre_tokens"],
+             next_tokens=g["next_tokens"], sparse_mode=g["sparse_mode"], keep_prob=g["keep_prob"])
+    d.update(over)
+    return orc.Problem(**d)
+
+
+# ------------------------------------------------------------ pages' samples --
+@pytest.mark.parametrize("reading", ["value_one", "fp16_bit_pattern_one"])
+def test_pages_forward_sample_closed_form(reading):
+    g = _load("aclnn_varlen_forward_sample.json")
+    c = g["fill_readings"][reading]
+    pr = _tnd_problem(g)
+    x = np.full((g["T"], g["N"], g["D"]), c)
+    out, smax, ssum = orc.forward(pr, x, x, x)
+    assert np.allclose(out, c, rtol=1e-12, atol=0)
+    assert np.allclose(smax, g["scale"] * g["D"] * c * c, rtol=1e-12, atol=0)
+    assert np.allclose(ssum, g["T"], rtol=1e-12, atol=0)
+
+
+def test_pages_backward_sample_given_stats_closed_form():
+    g = _load("aclnn_unpadding_grad_v2_sample.json")
+    f = g["fill"]
+    pr = _tnd_problem(g)
+    shape = (g["T"], g["N"], g["D"])
+    q, k, v, dy = (np.full(shape, f[n]) for n in ("q", "k", "v", "dy"))
+    given_out = np.full(shape, f["attention_in"])
+    gm = np.full((g["T"], g["N"]), f["softmax_max"])
+    gs = np.full((g["T"], g["N"]), f["softmax_sum"])
+    dq, dk, dv = orc.backward(pr, q, k, v, dy, None, given_out, gm, gs)
+    p = math.exp(g["scale"] * g["D"] * f["q"] * f["k"] - f["softmax_max"]) / f["softmax_sum"]
+    assert np.all(dq == 0.0) and np.all(dk == 0.0)
+    assert np.allclose(dv, g["T"] * p * f["dy"], rtol=1e-12, atol=0)
+
+
+def test_pages_backward_sample_exact_mode():
+    g = _load("aclnn_unpadding_grad_v2_sample.json")
+    pr = _tnd_problem(g)
+    x = np.ones((g["T"], g["N"], g["D"]))
+    dq, dk, dv = orc.backward(pr, x, x, x, x)
+    assert np.allclose(dq, 0.0, atol=1e-12) and np.allclose(dk, 0.0, atol=1e-12)
+    assert np.allclose(dv, 1.0, rtol=1e-12)
+
+
+# ------------------------------------------------------- finite differences --
+FD_CASES = {
+    "bnsd_nomask": dict(layout="BNSD", B=1, N=2, D=4, S_q=6, S_kv=6, scale=0.7, sparse_mode=0),
+    "bnsd_band": dict(layout="BNSD", B=1, N=1, D=4, S_q=7, S_kv=7, scale=0.9, sparse_mode=4, pre_tokens=2,
+                      next_tokens=1),
+    "bnsd_band_negative_pre": dict(layout="BNSD", B=1, N=1, D=3, S_q=6, S_kv=6, scale=1.1, sparse_mode=4,
+                                   pre_tokens=-1, next_tokens=2),
+    "bnsd_rect_band": dict(layout="BNSD", B=2, N=1, D=3, S_q=5, S_kv=8, scale=0.8, sparse_mode=4, pre_tokens=1,
+                           next_tokens=3),
+    "bnsd_dropout": dict(layout="BNSD", B=1, N=2, D=4, S_q=5, S_kv=5, scale=0.6, sparse_mode=4, pre_tokens=2,
+                         next_tokens=2, keep_prob=0.7),
+    "tnd_varlen": dict(layout="TND", B=4, N=2, D=3, cu_seqlens_q=[3, 3, 8, 0], cu_seqlens_kv=[4, 6, 9, 0],
+                       scale=0.75, sparse_mode=0),
+    "tnd_band_dropout": dict(layout="TND", B=2, N=1, D=4, cu_seqlens_q=[4, 9], cu_seqlens_kv=[4, 9], scale=0.9,
+                             sparse_mode=4, pre_tokens=1, next_tokens=1, keep_prob=0.6),
+}
+
+
+def _fd_inputs(case, seed):
+    geom = Geometry(**case)
+    inp = draw(geom, seed)
+    return geom, inp
+
+
+@pytest.mark.parametrize("name", sorted(FD_CASES))
+def test_finite_differences(name):
+    case = FD_CASES[name]
+    geom, inp = _fd_inputs(case, 1000 + len(name))
+    pr = to_problem(geom)
+    q, k, v, dy = (t.double().numpy() for t in (inp.q, inp.k, inp.v, inp.dy))
+    mask = inp.drop_mask
+    dq, dk, dv = orc.backward(pr, q, k, v, dy, mask)
+
+    def loss(qq, kk, vv):
+        out, _, _ = orc.forward(pr, qq, kk, vv, mask)
+        return float(np.sum(out * dy))
+
+    h = 1e-6
+    for which, base, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(base)
+        flat = base.reshape(-1)
+        for idx in range(flat.size):
+            save = flat[idx]
+            flat[idx] = save + h
+            lp = loss(q, k, v)
+            flat[idx] = save - h
+            lm = loss(q, k, v)
+            flat[idx] = save
+            num.reshape(-1)[idx] = (lp - lm) / (2 * h)
+        err = np.linalg.norm((num - grad).ravel()) / max(np.linalg.norm(num.ravel()), 1e-30)
+        assert err <= 1e-6, (name, which, err)
+
+
+# ------------------------------------------------------- library routine ----
+def _dense_mask(pr, lq, lk):
+    i = np.arange(lq)[:, None]
+    j = np.arange(lk)[None, :]
+    if pr.sparse_mode == 4:
+        return (j >= i - pr.pre_tokens) & (j <= i + pr.next_tokens)
+    return np.ones((lq, lk), dtype=bool)
+
+
+SDPA_CASES = {
+    "nomask": dict(layout="BNSD", B=2, N=2, D=8, S_q=33, S_kv=33, scale=0.35, sparse_mode=0),
+    "band": dict(layout="BNSD", B=1, N=3, D=16, S_q=70, S_kv=70, scale=0.25, sparse_mode=4, pre_tokens=9,
+                 next_tokens=3),
+    "band_sym": dict(layout="BNSD", B=2, N=1, D=8, S_q=40, S_kv=40, scale=0.4, sparse_mode=4, pre_tokens=5,
+                     next_tokens=5),
+    "rect": dict(layout="BNSD", B=1, N=2, D=8, S_q=20, S_kv=37, scale=0.3, sparse_mode=4, pre_tokens=4,
+                 next_tokens=12),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SDPA_CASES))
+def test_against_sdpa_float64(name):
+    case = SDPA_CASES[name]
+    geom = Geometry(**case)
+    inp = draw(geom, 2000 + len(name))
+    pr = to_problem(geom)
+    out, smax, ssum = orc.forward(pr, inp.q, inp.k, inp.v)
+    dq, dk, dv = orc.backward(pr, inp.q, inp.k, inp.v, inp.dy)
+    q = inp.q.double().requires_grad_(True)
+    k = inp.k.double().requires_grad_(True)
+    v = inp.v.double().requires_grad_(True)
+    m = torch.from_numpy(_dense_mask(pr, geom.S_q, geom.S_kv))
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=m, scale=geom.scale)
+    ref.backward(inp.dy.double())
+    assert np.allclose(out, ref.detach().numpy(), rtol=1e-10, atol=1e-12)
+    assert np.allclose(dq, q.grad.numpy(), rtol=1e-9, atol=1e-11)
+    assert np.allclose(dk, k.grad.numpy(), rtol=1e-9, atol=1e-11)
+    assert np.allclose(dv, v.grad.numpy(), rtol=1e-9, atol=1e-11)
+    # statistics: softmax_max is the max visible scaled score, and
+    # softmax_max + log(softmax_sum) is the logsumexp of the visible scores
+    s = geom.scale * torch.einsum("bnid,bnjd->bnij", inp.q.double(), inp.k.double())
+    s = s.masked_fill(~m, float("-inf"))
+    assert np.allclose(smax, torch.amax(s, dim=-1).numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(smax + np.log(ssum), torch.logsumexp(s, dim=-1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------- invariants ---
+def test_probability_rows_sum_to_one():
+    # V = identity (one-hot per key) makes out_i = P_i
+    S = 48
+    geom = Geometry("BNSD", 1, 2, S, S_q=S, S_kv=S, scale=0.2, sparse_mode=4, pre_tokens=7, next_tokens=2)
+    inp = draw(geom, 7)
+    eye = torch.eye(S, dtype=torch.bfloat16).expand(1, 2, S, S).contiguous()
+    out, _, _ = orc.forward(to_problem(geom), inp.q, inp.k, eye)
+    assert np.allclose(out.sum(-1), 1.0, rtol=0, atol=1e-13)
+    # and P vanishes outside the band
+    band = _dense_mask(to_problem(geom), S, S)
+    assert np.all(out[..., ~band] == 0.0)
+
+
+def test_wide_band_equals_no_mask():
+    base = dict(layout="BNSD", B=1, N=2, D=16, S_q=50, S_kv=50, scale=0.3)
+    g0 = Geometry(**base, sparse_mode=0)
+    g4 = Geometry(**base, sparse_mode=4, pre_tokens=50, next_tokens=50)
+    inp = draw(g0, 11)
+    a = orc.forward(to_problem(g0), inp.q, inp.k, inp.v)
+    b = orc.forward(to_problem(g4), inp.q, inp.k, inp.v)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    ga = orc.backward(to_problem(g0), inp.q, inp.k, inp.v, inp.dy)
+    gb = orc.backward(to_problem(g4), inp.q, inp.k, inp.v, inp.dy)
+    for x, y in zip(ga, gb):
+        assert np.array_equal(x, y)
+
+
+def test_keep_all_is_identity():
+    g = Geometry("BNSD", 1, 2, 8, S_q=30, S_kv=30, scale=0.5, sparse_mode=4, pre_tokens=6, next_tokens=6)
+    inp = draw(g, 12)
+    ones = np.full((g.mask_bits() + 7) // 8, 0xFF, dtype=np.uint8)
+    a = orc.forward(to_problem(g), inp.q, inp.k, inp.v, None)
+    b = orc.forward(to_problem(g), inp.q, inp.k, inp.v, ones)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    ga = orc.backward(to_problem(g), inp.q, inp.k, inp.v, inp.dy, None)
+    gb = orc.backward(to_problem(g), inp.q, inp.k, inp.v, inp.dy, ones)
+    for x, y in zip(ga, gb):
+        assert np.array_equal(x, y)
+
+
+def test_dropout_mask_bit_order_and_element_order():
+    # V = identity: out = P * z / keep, with z decoded by numpy.unpackbits
+    B, N, S, keep = 2, 2, 24, 0.75
+    g = Geometry("BNSD", B, N, S, S_q=S, S_kv=S, scale=0.3, sparse_mode=4, pre_tokens=5, next_tokens=3,
+                 keep_prob=keep)
+    inp = draw(g, 13)
+    eye = torch.eye(S, dtype=torch.bfloat16).expand(B, N, S, S).contiguous()
+    p_nodrop, _, _ = orc.forward(to_problem(Geometry(**{**g.as_dict(), "keep_prob": 1.0})), inp.q, inp.k, eye)
+    p_drop, _, _ = orc.forward(to_problem(g), inp.q, inp.k, eye, inp.drop_mask)
+    z = np.unpackbits(inp.drop_mask.numpy(), bitorder="little")[: B * N * S * S].reshape(B, N, S, S)
+    assert 0 < z.mean() < 1
+    assert np.allclose(p_drop, p_nodrop * z / keep, rtol=1e-14, atol=1e-15)
+
+
+def test_tnd_sequence_equals_bnsd():
+    lens_q, lens_kv = [5, 0, 17, 9], [7, 3, 17, 4]
+    cu_q, cu_kv = list(np.cumsum(lens_q)), list(np.cumsum(lens_kv))
+    g = Geometry("TND", 4, 2, 8, cu_seqlens_q=cu_q, cu_seqlens_kv=cu_kv, scale=0.4, sparse_mode=4, pre_tokens=3,
+                 next_tokens=2, keep_prob=0.8)
+    inp = draw(g, 14)
+    pr = to_problem(g)
+    out, smax, ssum = orc.forward(pr, inp.q, inp.k, inp.v, inp.drop_mask)
+    dq, dk, dv = orc.backward(pr, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask)
+    z = np.unpackbits(inp.drop_mask.numpy(), bitorder="little")
+    qs = ks = zoff = 0
+    for lq, lk in zip(lens_q, lens_kv):
+        if lq and lk:
+            sub = Geometry("BNSD", 1, 2, 8, S_q=lq, S_kv=lk, scale=0.4, sparse_mode=4, pre_tokens=3, next_tokens=2,
+                           keep_prob=0.8)
+            nb = 2 * lq * lk
+            sub_mask = np.packbits(z[zoff:zoff + nb], bitorder="little")
+            t = lambda x, s, l: x[s:s + l].permute(1, 0, 2).unsqueeze(0).contiguous()  # [L,N,D] -> [1,N,L,D]
+            o2, m2, l2 = orc.forward(to_problem(sub), t(inp.q, qs, lq), t(inp.k, ks, lk), t(inp.v, ks, lk), sub_mask)
+            g2 = orc.backward(to_problem(sub), t(inp.q, qs, lq), t(inp.k, ks, lk), t(inp.v, ks, lk),
+                              t(inp.dy, qs, lq), sub_mask)
+            assert np.array_equal(out[qs:qs + lq], o2[0].transpose(1, 0, 2))
+            assert np.array_equal(smax[qs:qs + lq], m2[0].T)
+            assert np.array_equal(ssum[qs:qs + lq], l2[0].T)
+            assert np.allclose(dq[qs:qs + lq], g2[0][0].transpose(1, 0, 2), rtol=1e-13, atol=1e-15)
+            assert np.allclose(dk[ks:ks + lk], g2[1][0].transpose(1, 0, 2), rtol=1e-13, atol=1e-15)
+            assert np.allclose(dv[ks:ks + lk], g2[2][0].transpose(1, 0, 2), rtol=1e-13, atol=1e-15)
+            zoff += nb
+        elif lq:  # no keys: every row is empty
+            assert np.all(out[qs:qs + lq] == 0) and np.all(ssum[qs:qs + lq] == 0)
+            assert np.all(np.isneginf(smax[qs:qs + lq]))
+        qs += lq
+        ks += lk
+    assert zoff == g.mask_bits()
+
+
+def test_single_key_returns_value():
+    g = Geometry("BNSD", 2, 2, 8, S_q=9, S_kv=1, scale=0.5, sparse_mode=0)
+    inp = draw(g, 15)
+    out, _, ssum = orc.forward(to_problem(g), inp.q, inp.k, inp.v)
+    assert np.array_equal(out, np.broadcast_to(inp.v.double().numpy(), out.shape))
+    assert np.all(ssum == 1.0)
+
+
+def test_zero_width_band_returns_own_value():
+    g = Geometry("BNSD", 1, 2, 8, S_q=12, S_kv=12, scale=0.5, sparse_mode=4, pre_tokens=0, next_tokens=0)
+    inp = draw(g, 16)
+    out, smax, ssum = orc.forward(to_problem(g), inp.q, inp.k, inp.v)
+    assert np.array_equal(out, inp.v.double().numpy())
+    assert np.all(ssum == 1.0)
+    qk = g.scale * (inp.q.double() * inp.k.double()).sum(-1).numpy()
+    assert np.allclose(smax, qk, rtol=1e-14, atol=1e-15)
+
+
+def test_empty_rows_convention():
+    # window [i+1, i+2]: the last row sees nothing
+    g = Geometry("BNSD", 1, 1, 4, S_q=6, S_kv=6, scale=0.5, sparse_mode=4, pre_tokens=-1, next_tokens=2)
+    inp = draw(g, 17)
+    out, smax, ssum = orc.forward(to_problem(g), inp.q, inp.k, inp.v)
+    dq, dk, dv = orc.backward(to_problem(g), inp.q, inp.k, inp.v, inp.dy)
+    assert np.all(out[0, 0, 5] == 0) and np.isneginf(smax[0, 0, 5]) and ssum[0, 0, 5] == 0
+    assert np.all(dq[0, 0, 5] == 0)
+    assert np.all(np.isfinite(dq)) and np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
+    # key 0 is seen by nobody (j >= i + 1 >= 1)
+    assert np.all(dk[0, 0, 0] == 0) and np.all(dv[0, 0, 0] == 0)
+    # an entirely empty band
+    g2 = Geometry(**{**g.as_dict(), "pre_tokens": -3, "next_tokens": 1})
+    out2, smax2, ssum2 = orc.forward(to_problem(g2), inp.q, inp.k, inp.v)
+    assert np.all(out2 == 0) and np.all(np.isneginf(smax2)) and np.all(ssum2 == 0)
+
+
+def test_given_stats_mode_matches_exact_mode():
+    g = Geometry("BNSD", 1, 2, 8, S_q=20, S_kv=20, scale=0.4, sparse_mode=4, pre_tokens=4, next_tokens=1,
+                 keep_prob=0.85)
+    inp = draw(g, 18)
+    pr = to_problem(g)
+    out, smax, ssum = orc.forward(pr, inp.q, inp.k, inp.v, inp.drop_mask)
+    a = orc.backward(pr, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask)
+    b = orc.backward(pr, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask, out, smax, ssum)
+    for x, y in zip(a, b):
+        assert np.allclose(x, y, rtol=1e-13, atol=1e-15)
+
+
+# ---------------------------------------------- sampled entry points -------
+@pytest.mark.parametrize("layout", ["BNSD", "TND"])
+def test_sampled_entry_points_match_full(layout):
+    if layout == "BNSD":
+        g = Geometry("BNSD", 2, 2, 8, S_q=40, S_kv=40, scale=0.4, sparse_mode=4, pre_tokens=6, next_tokens=2,
+                     keep_prob=0.9)
+        nq, nk = 2 * 40 * 2, 2 * 40 * 2
+    else:
+        g = Geometry("TND", 3, 2, 8, cu_seqlens_q=[10, 30, 37], cu_seqlens_kv=[10, 30, 37], scale=0.4,
+                     sparse_mode=4, pre_tokens=5, next_tokens=5, keep_prob=0.9)
+        nq, nk = 37 * 2, 37 * 2
+    inp = draw(g, 19)
+    pr = to_problem(g)
+    out, smax, ssum = orc.forward(pr, inp.q, inp.k, inp.v, inp.drop_mask)
+    dq, dk, dv = orc.backward(pr, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask)
+    rows = np.array([0, 3, 17, nq - 1, nq // 2])
+    cols = np.array([0, 5, 21, nk - 1, nk // 3])
+    o_s, m_s, l_s = orc.forward_rows(pr, inp.q, inp.k, inp.v, inp.drop_mask, rows)
+    dq_s = orc.backward_dq_rows(pr, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask, rows)
+    dk_s, dv_s = orc.backward_dkv_cols(pr, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask, cols)
+    D = g.D
+    if layout == "BNSD":
+        flat_q = lambda a: a.reshape(-1, D)
+        flat_s = lambda a: a.reshape(-1)
+    else:  # TND rows are (t, n) -> flat id t*N + n, same as reshape
+        flat_q = lambda a: a.reshape(-1, D)
+        flat_s = lambda a: a.reshape(-1)
+    assert np.array_equal(o_s, flat_q(out)[rows])
+    assert np.array_equal(m_s, flat_s(smax)[rows])
+    assert np.array_equal(l_s, flat_s(ssum)[rows])
+    assert np.allclose(dq_s, flat_q(dq)[rows], rtol=1e-13, atol=1e-15)
+    assert np.allclose(dk_s, flat_q(dk)[cols], rtol=1e-13, atol=1e-15)
+    assert np.allclose(dv_s, flat_q(dv)[cols], rtol=1e-13, atol=1e-15)
+    lo, hi = orc.key_ranges(pr, rows)
+    for t, r in enumerate(rows):
+        # the visible range reproduces softmax_sum with zero scores
+        assert hi[t] >= lo[t]
+
+
+def test_visible_pair_count_matches_dense_mask():
+    for case in SDPA_CASES.values():
+        pr = to_problem(Geometry(**case))
+        dense = _dense_mask(pr, pr.S_q, pr.S_kv).sum() * pr.B * pr.N
+        assert orc.visible_pairs(pr) == dense
