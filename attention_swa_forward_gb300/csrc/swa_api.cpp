@@ -1,0 +1,490 @@
+// swa_api.cpp — the C ABI of libswa (include/swa.h): argument checks, the
+// band / varlen tile scheduler, TMA descriptors and kernel launches.
+//
+// Follows the two-phase workspace convention and status codes of the
+// FlashAttentionVarLenScore doc ("两段式接口", "返回值"), and the swa_forward /
+// swa_backward split limited to sparse modes 0 and 4 (pzsr.cn article §3).
+#include "swa.h"
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "swa_internal.h"
+
+using namespace swa;
+
+namespace {
+
+thread_local std::string t_last_error = "no error";
+thread_local cudaEvent_t t_ev[4] = {nullptr, nullptr, nullptr, nullptr};  // fwd start/stop, bwd start/stop
+
+swa_status_t fail(swa_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+constexpr int64_t kMaxRows = int64_t(1) << 20;  // T (TND) or S (BNSD) limit: 1M rows
+constexpr double kLog2e = 1.4426950408889634;
+
+struct Seq {
+  int64_t q_start, q_len, kv_start, kv_len, mask_base;
+};
+
+struct Plan {
+  Geometry g{};
+  int64_t B = 0;
+  std::vector<Seq> seqs;       // per batch
+  int64_t q_rows = 0;          // rows of q per head: B*S_q or T_q
+  int64_t kv_rows = 0;
+  int64_t mask_bits = 0;
+};
+
+// Sequence spans from cumulative ends; a drop (trailing zeros) marks skipped
+// batches (aclnnFlashAttentionUnpaddingScoreGradV2 article §6.4).
+swa_status_t parse_cumulative(const int64_t* cu, int64_t B, int64_t T, const char* name, std::vector<int64_t>& start,
+                              std::vector<int64_t>& len) {
+  start.assign(B, 0);
+  len.assign(B, 0);
+  int64_t prev = 0;
+  bool in_tail = false;
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t e = cu[b];
+    if (in_tail) {
+      if (e != 0) return fail(SWA_ERR_PARAM_INVALID, "%s[%lld] = %lld after the trailing zeros", name, (long long)b,
+                              (long long)e);
+      start[b] = T;
+      continue;
+    }
+    if (e < prev) {
+      if (e != 0) return fail(SWA_ERR_PARAM_INVALID, "%s is not non-decreasing at index %lld", name, (long long)b);
+      if (prev != T) return fail(SWA_ERR_PARAM_INVALID, "%s ends at %lld before its trailing zeros, T = %lld", name,
+                                 (long long)prev, (long long)T);
+      in_tail = true;
+      start[b] = T;
+      continue;
+    }
+    start[b] = prev;
+    len[b] = e - prev;
+    prev = e;
+  }
+  if (!in_tail && prev != T)
+    return fail(SWA_ERR_PARAM_INVALID, "%s ends at %lld but T = %lld", name, (long long)prev, (long long)T);
+  return SWA_OK;
+}
+
+swa_status_t make_plan(const swa_params_t* p, Plan& plan) {
+  if (!p) return fail(SWA_ERR_PARAM_NULLPTR, "params is NULL");
+  if (p->layout != SWA_LAYOUT_BNSD && p->layout != SWA_LAYOUT_TND)
+    return fail(SWA_ERR_PARAM_INVALID, "layout %d is neither BNSD (0) nor TND (1)", p->layout);
+  if (p->sparse_mode != 0 && p->sparse_mode != 4)
+    return fail(SWA_ERR_PARAM_INVALID, "sparse_mode should be 0 or 4, got %d", p->sparse_mode);
+  if (!(p->keep_prob > 0.0 && p->keep_prob <= 1.0))
+    return fail(SWA_ERR_PARAM_INVALID, "keep_prob must be in (0, 1], got %g", p->keep_prob);
+  if (p->N < 1 || p->N > 256) return fail(SWA_ERR_PARAM_INVALID, "N must be in [1, 256], got %lld", (long long)p->N);
+  if (p->B < 1) return fail(SWA_ERR_PARAM_INVALID, "B must be >= 1, got %lld", (long long)p->B);
+  if (p->D < 1 || p->D > 768) return fail(SWA_ERR_PARAM_INVALID, "D must be in [1, 768], got %lld", (long long)p->D);
+  if (p->D != 64 && p->D != 128) return fail(SWA_ERR_UNSUPPORTED, "D = %lld is not built (64 or 128)", (long long)p->D);
+  if (!std::isfinite(p->scale)) return fail(SWA_ERR_PARAM_INVALID, "scale is not finite");
+  if (p->sparse_mode == 4) {
+    // an everywhere-empty band is almost certainly a caller error
+    const long double s = (long double)p->pre_tokens + (long double)p->next_tokens;
+    if (s < 0) return fail(SWA_ERR_PARAM_INVALID, "pre_tokens + next_tokens < 0: every row would be empty");
+  }
+
+  plan = Plan();
+  plan.B = p->B;
+  Geometry& g = plan.g;
+  g.layout = p->layout;
+  g.N = static_cast<int32_t>(p->N);
+  g.D = static_cast<int32_t>(p->D);
+  g.sparse_mode = p->sparse_mode;
+  g.scale = static_cast<float>(p->scale);
+  g.scale_log2 = static_cast<float>(p->scale * kLog2e);
+  g.inv_keep = static_cast<float>(1.0 / p->keep_prob);
+
+  int64_t max_len = 0;
+  if (p->layout == SWA_LAYOUT_BNSD) {
+    if (p->S_q < 1 || p->S_q > kMaxRows || p->S_kv < 1 || p->S_kv > kMaxRows)
+      return fail(SWA_ERR_PARAM_INVALID, "S_q / S_kv must be in [1, %lld]", (long long)kMaxRows);
+    if (p->B * p->S_q > (int64_t(1) << 31) || p->B * p->S_kv > (int64_t(1) << 31))
+      return fail(SWA_ERR_PARAM_INVALID, "B * S exceeds 2^31 rows");
+    g.S_q = static_cast<int32_t>(p->S_q);
+    g.S_kv = static_cast<int32_t>(p->S_kv);
+    plan.seqs.resize(p->B);
+    for (int64_t b = 0; b < p->B; ++b)
+      plan.seqs[b] = Seq{0, p->S_q, 0, p->S_kv, b * p->N * p->S_q * p->S_kv};
+    plan.q_rows = p->B * p->S_q;
+    plan.kv_rows = p->B * p->S_kv;
+    plan.mask_bits = p->B * p->N * p->S_q * p->S_kv;
+    max_len = std::max(p->S_q, p->S_kv);
+  } else {
+    if (!p->cu_seqlens_q || !p->cu_seqlens_kv) return fail(SWA_ERR_PARAM_NULLPTR, "cu_seqlens_q / cu_seqlens_kv is NULL");
+    if (p->T_q < 1 || p->T_q > kMaxRows || p->T_kv < 1 || p->T_kv > kMaxRows)
+      return fail(SWA_ERR_PARAM_INVALID, "T_q / T_kv must be in [1, %lld]", (long long)kMaxRows);
+    std::vector<int64_t> qs, ql, ks, kl;
+    swa_status_t st = parse_cumulative(p->cu_seqlens_q, p->B, p->T_q, "cu_seqlens_q", qs, ql);
+    if (st != SWA_OK) return st;
+    st = parse_cumulative(p->cu_seqlens_kv, p->B, p->T_kv, "cu_seqlens_kv", ks, kl);
+    if (st != SWA_OK) return st;
+    plan.seqs.resize(p->B);
+    int64_t bits = 0;
+    for (int64_t b = 0; b < p->B; ++b) {
+      plan.seqs[b] = Seq{qs[b], ql[b], ks[b], kl[b], bits};
+      bits += p->N * ql[b] * kl[b];
+      max_len = std::max(max_len, std::max(ql[b], kl[b]));
+    }
+    g.S_q = 0;
+    g.S_kv = 0;
+    plan.q_rows = p->T_q;
+    plan.kv_rows = p->T_kv;
+    plan.mask_bits = bits;
+  }
+  // The window cannot reach further than the longest sequence: clamp.
+  const int64_t lim = max_len + 1;
+  g.pre = static_cast<int32_t>(std::min(std::max(p->pre_tokens, -lim), lim));
+  g.next = static_cast<int32_t>(std::min(std::max(p->next_tokens, -lim), lim));
+  return SWA_OK;
+}
+
+// ------------------------------------------------------------ scheduler --
+// Number of key tiles a query tile visits (forward) or query tiles a key tile
+// visits (backward), by the BAND inequality i - pre <= j <= i + next.
+int64_t fwd_tile_cost(const Geometry& g, const Seq& s, int64_t t) {
+  const int64_t q0 = t * kTileM, q_last = std::min(q0 + kTileM - 1, s.q_len - 1);
+  int64_t lo = 0, hi = s.kv_len - 1;
+  if (g.sparse_mode == 4) {
+    lo = std::max<int64_t>(lo, q0 - g.pre);
+    hi = std::min<int64_t>(hi, q_last + g.next);
+  }
+  return lo <= hi ? hi / kTileN - lo / kTileN + 1 : 0;
+}
+int64_t bwd_tile_cost(const Geometry& g, const Seq& s, int64_t t) {
+  const int64_t j0 = t * kTileN, j_last = std::min(j0 + kTileN - 1, s.kv_len - 1);
+  int64_t lo = 0, hi = s.q_len - 1;
+  if (g.sparse_mode == 4) {
+    lo = std::max<int64_t>(lo, j0 - g.next);
+    hi = std::min<int64_t>(hi, j_last + g.pre);
+  }
+  return lo <= hi ? hi / kTileM - lo / kTileM + 1 : 0;
+}
+
+// Work entries of one launch family, heaviest first.
+std::vector<SeqDesc> build_descs(const Plan& plan, bool forward) {
+  const Geometry& g = plan.g;
+  struct Entry {
+    SeqDesc d;
+    int64_t weight;
+  };
+  std::vector<Entry> entries;
+  auto fill = [&](const Seq& s, int32_t b, int32_t heads) {
+    const int64_t rows = forward ? s.q_len : s.kv_len;
+    if (rows <= 0) return;
+    const int64_t tiles = (rows + kTileM - 1) / kTileM;
+    int64_t wmax = 0;
+    for (int64_t t = 0; t < tiles; ++t)
+      wmax = std::max(wmax, forward ? fwd_tile_cost(g, s, t) : bwd_tile_cost(g, s, t));
+    const int64_t c0 = forward ? fwd_tile_cost(g, s, 0) : bwd_tile_cost(g, s, 0);
+    const int64_t c1 = forward ? fwd_tile_cost(g, s, tiles - 1) : bwd_tile_cost(g, s, tiles - 1);
+    SeqDesc d{};
+    d.q_start = static_cast<int32_t>(s.q_start);
+    d.q_len = static_cast<int32_t>(s.q_len);
+    d.kv_start = static_cast<int32_t>(s.kv_start);
+    d.kv_len = static_cast<int32_t>(s.kv_len);
+    d.mask_base = s.mask_base;
+    d.b = b;
+    d.tiles = static_cast<int32_t>(tiles);
+    d.heads = heads;
+    d.descending = c1 >= c0 ? 1 : 0;
+    entries.push_back(Entry{d, wmax});
+  };
+  if (g.layout == 0) {
+    fill(plan.seqs[0], -1, static_cast<int32_t>(plan.B * g.N));
+  } else {
+    for (int64_t b = 0; b < plan.B; ++b) fill(plan.seqs[b], static_cast<int32_t>(b), g.N);
+    std::stable_sort(entries.begin(), entries.end(),
+                     [](const Entry& x, const Entry& y) { return x.weight > y.weight; });
+  }
+  std::vector<SeqDesc> out;
+  out.reserve(entries.size());
+  for (auto& e : entries) out.push_back(e.d);
+  return out;
+}
+
+// Split the entries into launches of at most CAP entries and run `launch` on each table.
+template <int CAP, typename F>
+cudaError_t for_each_table(const std::vector<SeqDesc>& descs, size_t begin, size_t end, F&& launch) {
+  static thread_local std::unique_ptr<SeqTable<CAP>> tab_storage;
+  if (!tab_storage) tab_storage.reset(new SeqTable<CAP>());
+  SeqTable<CAP>& tab = *tab_storage;
+  for (size_t c = begin; c < end; c += CAP) {
+    const size_t n = std::min<size_t>(CAP, end - c);
+    std::memset(&tab, 0, sizeof tab);
+    int64_t items = 0;
+    for (size_t i = 0; i < n; ++i) {
+      tab.d[i] = descs[c + i];
+      tab.d[i].item_begin = static_cast<int32_t>(items);
+      items += static_cast<int64_t>(descs[c + i].tiles) * descs[c + i].heads;
+    }
+    tab.count = static_cast<int32_t>(n);
+    tab.n_items = static_cast<int32_t>(items);
+    cudaError_t e = launch(tab);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <typename FS, typename FL>
+cudaError_t run_tables(const std::vector<SeqDesc>& descs, FS&& small, FL&& large) {
+  if (descs.empty()) return cudaSuccess;
+  if (descs.size() <= static_cast<size_t>(kSmallTable))
+    return for_each_table<kSmallTable>(descs, 0, descs.size(), small);
+  return for_each_table<kLargeTable>(descs, 0, descs.size(), large);
+}
+
+// ------------------------------------------------------------ TMA maps --
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 128 rows x 64 columns per box, 128-byte swizzle.  BNSD: (d, s, n, b);
+// TND: (d, n, t, 1).
+swa_status_t make_map(CUtensorMap* m, const void* ptr, const Plan& plan, bool q_side, const char* name) {
+  auto fn = encode_fn();
+  if (!fn) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const Geometry& g = plan.g;
+  const cuuint64_t D = g.D, N = g.N;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4];
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  if (g.layout == 0) {
+    const cuuint64_t S = q_side ? g.S_q : g.S_kv;
+    dims[0] = D; dims[1] = S; dims[2] = N; dims[3] = static_cast<cuuint64_t>(plan.B);
+    strides[0] = D * 2; strides[1] = S * D * 2; strides[2] = N * S * D * 2;
+    box[0] = 64; box[1] = kTileM; box[2] = 1; box[3] = 1;
+  } else {
+    const cuuint64_t T = static_cast<cuuint64_t>(q_side ? plan.q_rows : plan.kv_rows);
+    dims[0] = D; dims[1] = N; dims[2] = T; dims[3] = 1;
+    strides[0] = D * 2; strides[1] = N * D * 2; strides[2] = T * N * D * 2;
+    box[0] = 64; box[1] = 1; box[2] = kTileM; box[3] = 1;
+  }
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
+  return SWA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct BwdLayout {
+  size_t lse2, dsum, dq_acc, total;
+};
+BwdLayout bwd_layout(const Plan& plan) {
+  const size_t rows = static_cast<size_t>(plan.q_rows) * plan.g.N;
+  BwdLayout l;
+  l.lse2 = kHeaderBytes;
+  l.dsum = l.lse2 + round256(rows * 4);
+  l.dq_acc = l.dsum + round256(rows * 4);
+  l.total = l.dq_acc + round256(rows * plan.g.D * 4);
+  return l;
+}
+
+swa_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(SWA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ ABI --
+extern "C" {
+
+void swa_params_default(swa_params_t* p) {
+  if (!p) return;
+  std::memset(p, 0, sizeof *p);
+  p->scale = 1.0;
+  p->keep_prob = 1.0;
+  p->pre_tokens = 2147483647;
+  p->next_tokens = 2147483647;
+  p->sparse_mode = 0;
+}
+
+swa_status_t swa_forward_workspace_size(const swa_params_t* p, size_t* bytes) {
+  if (!bytes) return fail(SWA_ERR_PARAM_NULLPTR, "bytes is NULL");
+  Plan plan;
+  swa_status_t st = make_plan(p, plan);
+  if (st != SWA_OK) return st;
+  *bytes = kHeaderBytes;
+  return SWA_OK;
+}
+
+swa_status_t swa_backward_workspace_size(const swa_params_t* p, size_t* bytes) {
+  if (!bytes) return fail(SWA_ERR_PARAM_NULLPTR, "bytes is NULL");
+  Plan plan;
+  swa_status_t st = make_plan(p, plan);
+  if (st != SWA_OK) return st;
+  *bytes = bwd_layout(plan).total;
+  return SWA_OK;
+}
+
+swa_status_t swa_forward(const swa_params_t* p, const void* q, const void* k, const void* v, const uint8_t* drop_mask,
+                         void* out, float* softmax_max, float* softmax_sum, void* workspace, size_t workspace_bytes,
+                         swa_stream_t stream) {
+  Plan plan;
+  swa_status_t st = make_plan(p, plan);
+  if (st != SWA_OK) return st;
+  if (!q || !k || !v || !out || !softmax_max || !softmax_sum)
+    return fail(SWA_ERR_PARAM_NULLPTR, "a required tensor pointer is NULL");
+  if ((p->keep_prob < 1.0) != (drop_mask != nullptr))
+    return fail(SWA_ERR_PARAM_INVALID, "drop_mask must be given iff keep_prob < 1 (keep_prob = %g)", p->keep_prob);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(softmax_max) ||
+      !aligned16(softmax_sum) || !aligned16(drop_mask))
+    return fail(SWA_ERR_PARAM_INVALID, "tensor pointers (and drop_mask) must be 16-byte aligned");
+  if (!workspace || workspace_bytes < kHeaderBytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(SWA_ERR_WORKSPACE, "workspace must be >= %zu bytes and 256-byte aligned", kHeaderBytes);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  CUtensorMap mq, mk, mv;
+  if ((st = make_map(&mq, q, plan, true, "q")) != SWA_OK) return st;
+  if ((st = make_map(&mk, k, plan, false, "k")) != SWA_OK) return st;
+  if ((st = make_map(&mv, v, plan, false, "v")) != SWA_OK) return st;
+
+  FwdArgs a{};
+  a.g = plan.g;
+  a.g.has_mask = drop_mask != nullptr;
+  a.mask = drop_mask;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.smax = softmax_max;
+  a.ssum = softmax_sum;
+  a.err = static_cast<int32_t*>(workspace);
+
+  cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
+  const std::vector<SeqDesc> descs = build_descs(plan, true);
+  if (t_ev[0]) cudaEventRecord(t_ev[0], s);
+  e = run_tables(
+      descs, [&](const SeqTable<kSmallTable>& t) { return launch_forward(a, t, mq, mk, mv, s); },
+      [&](const SeqTable<kLargeTable>& t) { return launch_forward(a, t, mq, mk, mv, s); });
+  if (t_ev[1]) cudaEventRecord(t_ev[1], s);
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return SWA_OK;
+}
+
+swa_status_t swa_backward(const swa_params_t* p, const void* q, const void* k, const void* v, const void* dy,
+                          const void* out, const float* softmax_max, const float* softmax_sum,
+                          const uint8_t* drop_mask, void* dq, void* dk, void* dv, void* workspace,
+                          size_t workspace_bytes, swa_stream_t stream) {
+  Plan plan;
+  swa_status_t st = make_plan(p, plan);
+  if (st != SWA_OK) return st;
+  if (!q || !k || !v || !dy || !out || !softmax_max || !softmax_sum || !dq || !dk || !dv)
+    return fail(SWA_ERR_PARAM_NULLPTR, "a required tensor pointer is NULL");
+  if ((p->keep_prob < 1.0) != (drop_mask != nullptr))
+    return fail(SWA_ERR_PARAM_INVALID, "drop_mask must be given iff keep_prob < 1 (keep_prob = %g)", p->keep_prob);
+  for (const void* ptr : {q, k, v, dy, out, static_cast<const void*>(drop_mask), static_cast<const void*>(softmax_max),
+                          static_cast<const void*>(softmax_sum), static_cast<const void*>(dq),
+                          static_cast<const void*>(dk), static_cast<const void*>(dv)})
+    if (!aligned16(ptr)) return fail(SWA_ERR_PARAM_INVALID, "tensor pointers must be 16-byte aligned");
+  const BwdLayout lay = bwd_layout(plan);
+  if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(SWA_ERR_WORKSPACE, "workspace must be >= %zu bytes and 256-byte aligned (got %zu)", lay.total,
+                workspace_bytes);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  CUtensorMap mq, mk, mv, mdy;
+  if ((st = make_map(&mq, q, plan, true, "q")) != SWA_OK) return st;
+  if ((st = make_map(&mk, k, plan, false, "k")) != SWA_OK) return st;
+  if ((st = make_map(&mv, v, plan, false, "v")) != SWA_OK) return st;
+  if ((st = make_map(&mdy, dy, plan, true, "dy")) != SWA_OK) return st;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* lse2 = reinterpret_cast<float*>(ws + lay.lse2);
+  float* dsum = reinterpret_cast<float*>(ws + lay.dsum);
+  float* dq_acc = reinterpret_cast<float*>(ws + lay.dq_acc);
+  const int64_t rows = plan.q_rows * plan.g.N;
+
+  PrepArgs pa{};
+  pa.g = plan.g;
+  pa.rows = rows;
+  pa.err = reinterpret_cast<int32_t*>(ws);
+  pa.dy = static_cast<const __nv_bfloat16*>(dy);
+  pa.out = static_cast<const __nv_bfloat16*>(out);
+  pa.smax = softmax_max;
+  pa.ssum = softmax_sum;
+  pa.lse2 = lse2;
+  pa.dsum = dsum;
+  pa.dq_acc = dq_acc;
+  cudaError_t e = launch_prep(pa, s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
+
+  BwdArgs a{};
+  a.g = plan.g;
+  a.g.has_mask = drop_mask != nullptr;
+  a.mask = drop_mask;
+  a.lse2 = lse2;
+  a.dsum = dsum;
+  a.dq_acc = dq_acc;
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.err = reinterpret_cast<int32_t*>(ws);
+  const std::vector<SeqDesc> descs = build_descs(plan, false);
+  if (t_ev[2]) cudaEventRecord(t_ev[2], s);
+  e = run_tables(
+      descs, [&](const SeqTable<kSmallTable>& t) { return launch_backward(a, t, mq, mk, mv, mdy, s); },
+      [&](const SeqTable<kLargeTable>& t) { return launch_backward(a, t, mq, mk, mv, mdy, s); });
+  if (t_ev[3]) cudaEventRecord(t_ev[3], s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  // Key rows that no work item covers (skipped batches, length-0 sequences)
+  // hold no data, so nothing else of dk / dv needs writing.
+  e = launch_dq_convert(dq_acc, static_cast<__nv_bfloat16*>(dq), rows * plan.g.D, plan.g.scale, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dQ convert launch");
+  return SWA_OK;
+}
+
+swa_status_t swa_workspace_status(const void* workspace, swa_stream_t stream) {
+  if (!workspace) return fail(SWA_ERR_PARAM_NULLPTR, "workspace is NULL");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int32_t word = 0;
+  e = cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the workspace header");
+  if (word != 0) return fail(SWA_ERR_TIMEOUT, "a kernel gave up a bounded wait (code %d)", word);
+  return SWA_OK;
+}
+
+void swa_set_timing_events(void* fwd_start, void* fwd_stop, void* bwd_start, void* bwd_stop) {
+  t_ev[0] = static_cast<cudaEvent_t>(fwd_start);
+  t_ev[1] = static_cast<cudaEvent_t>(fwd_stop);
+  t_ev[2] = static_cast<cudaEvent_t>(bwd_start);
+  t_ev[3] = static_cast<cudaEvent_t>(bwd_stop);
+}
+
+const char* swa_last_error(void) { return t_last_error.c_str(); }
+
+}  // extern "C"

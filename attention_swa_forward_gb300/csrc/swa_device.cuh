@@ -1,0 +1,151 @@
+// swa_device.cuh — device helpers shared by the forward and backward kernels:
+// addressing of BNSD / TND rows, the BAND window, tile loads, dropout bits and
+// writing a bf16 row into a 128-byte-swizzled shared-memory tile.
+#pragma once
+#include "sm103.cuh"
+#include "swa_internal.h"
+
+namespace swa {
+
+constexpr int kAtomBytes = 128 * 128;  // one atom column: 128 rows x 128 bytes
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// A resolved work item: which (batch, head, tile) this CTA owns, and the
+// geometry of its sequence.
+struct Item {
+  int b, n, tile;
+  SeqInfo s;
+};
+
+template <int CAP>
+__device__ __forceinline__ Item resolve_item(const SeqTable<CAP>& tab, const Geometry& g, int k) {
+  int lo = 0, hi = tab.count - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tab.d[mid].item_begin <= k) lo = mid; else hi = mid - 1;
+  }
+  const SeqDesc& d = tab.d[lo];
+  const int local = k - d.item_begin;
+  const int rank = local / d.heads;
+  const int h = local - rank * d.heads;
+  Item it;
+  it.tile = d.descending ? d.tiles - 1 - rank : rank;
+  if (d.b < 0) {
+    it.b = h / g.N;
+    it.n = h - it.b * g.N;
+    it.s.mask_base = static_cast<int64_t>(it.b) * g.N * g.S_q * static_cast<int64_t>(g.S_kv);
+  } else {
+    it.b = d.b;
+    it.n = h;
+    it.s.mask_base = d.mask_base;
+  }
+  it.s.q_start = d.q_start;
+  it.s.q_len = d.q_len;
+  it.s.kv_start = d.kv_start;
+  it.s.kv_len = d.kv_len;
+  return it;
+}
+
+// Element offset of local query row i of (b, n): BNSD [B,N,S,D] or TND [T,N,D].
+__device__ __forceinline__ int64_t q_elem(const Geometry& g, const SeqInfo& s, int b, int n, int i) {
+  return g.layout == 0 ? ((static_cast<int64_t>(b) * g.N + n) * g.S_q + i) * g.D
+                       : (static_cast<int64_t>(s.q_start + i) * g.N + n) * g.D;
+}
+__device__ __forceinline__ int64_t kv_elem(const Geometry& g, const SeqInfo& s, int b, int n, int j) {
+  return g.layout == 0 ? ((static_cast<int64_t>(b) * g.N + n) * g.S_kv + j) * g.D
+                       : (static_cast<int64_t>(s.kv_start + j) * g.N + n) * g.D;
+}
+// Index of the softmax statistics of local query row i: [B,N,S] or [T,N].
+__device__ __forceinline__ int64_t stat_index(const Geometry& g, const SeqInfo& s, int b, int n, int i) {
+  return g.layout == 0 ? (static_cast<int64_t>(b) * g.N + n) * g.S_q + i
+                       : static_cast<int64_t>(s.q_start + i) * g.N + n;
+}
+
+// Keys visible to local query row i: [lo, hi] (empty when lo > hi).
+// sparse_mode 4 (BAND): i - pre <= j <= i + next; rows past the sequence see nothing.
+__device__ __forceinline__ void key_window(const Geometry& g, const SeqInfo& s, int i, int& lo, int& hi) {
+  lo = 0;
+  hi = s.kv_len - 1;
+  if (g.sparse_mode == 4) {
+    lo = max(lo, i - g.pre);
+    hi = min(hi, i + g.next);
+  }
+  if (i >= s.q_len) {
+    lo = 1;
+    hi = 0;
+  }
+}
+
+// Is every (i, j) of the query tile [q0, q0+128) x key tile [j0, j0+128) visible?
+__device__ __forceinline__ bool tile_fully_visible(const Geometry& g, const SeqInfo& s, int q0, int j0) {
+  if (q0 + 127 >= s.q_len || j0 + 127 >= s.kv_len) return false;
+  if (g.sparse_mode != 4) return true;
+  return j0 >= q0 + 127 - g.pre && j0 + 127 <= q0 + g.next;
+}
+
+// TMA load of 128 rows x D columns starting at local row `row0` of (b, n) into
+// D/64 consecutive atom columns.  BNSD maps are (d, s, n, b); TND maps are
+// (d, n, t, 1) and take the sequence's start row.
+template <int D>
+__device__ __forceinline__ void tma_rows(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, const Geometry& g,
+                                         int b, int n, int start, int row0) {
+#pragma unroll
+  for (int a = 0; a < D / 64; ++a) {
+    if (g.layout == 0)
+      tma_load_4d(dst + a * kAtomBytes, map, bar, a * 64, row0, n, b);
+    else
+      tma_load_4d(dst + a * kAtomBytes, map, bar, a * 64, n, start + row0, 0);
+  }
+}
+
+// 128 dropout keep bits of row i for keys [j0, j0+128): bit t of the result
+// (word t >> 5) is key j0 + t.  Bits past the sequence's last key are 0.
+// Element order: mask_base + (n*Sq + i)*Skv + j, least significant bit first.
+__device__ __forceinline__ void load_keep_bits(const uint8_t* __restrict__ mask, const SeqInfo& s, int n, int i,
+                                               int j0, uint32_t (&bits)[4]) {
+  const int cnt = min(128, s.kv_len - j0);
+  const int64_t e0 = s.mask_base + (static_cast<int64_t>(n) * s.q_len + i) * s.kv_len + j0;
+  uint32_t w[5] = {0u, 0u, 0u, 0u, 0u};
+  const int sh = static_cast<int>(e0 & 7);
+  const uint8_t* p = mask + (e0 >> 3);
+  if ((e0 & 127) == 0 && cnt == 128) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else {
+    const int nbytes = (sh + cnt + 7) >> 3;
+#pragma unroll
+    for (int t = 0; t < 17; ++t)
+      if (t < nbytes) w[t >> 2] |= static_cast<uint32_t>(__ldg(p + t)) << ((t & 3) * 8);
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) bits[k] = __funnelshift_r(w[k], w[k + 1], sh);
+  if (cnt < 128) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int lo = k * 32;
+      const uint32_t keep = cnt >= lo + 32 ? 0xFFFFFFFFu : (cnt <= lo ? 0u : ((1u << (cnt - lo)) - 1u));
+      bits[k] &= keep;
+    }
+  }
+}
+
+// Write 8 bf16 (one 16-byte chunk) of row r, chunk index c (0..15 over a
+// 128-wide row spanning two atom columns) into a swizzled tile.
+__device__ __forceinline__ void st_chunk_sw128(uint8_t* tile, int r, int c, uint4 v) {
+  uint8_t* dst = tile + (c >> 3) * kAtomBytes + r * 128 + ((((c & 7) ^ r) & 7) << 4);
+  *reinterpret_cast<uint4*>(dst) = v;
+}
+
+__device__ __forceinline__ uint4 pack8(const float* x) {
+  uint4 v;
+  v.x = pack_bf16x2(x[0], x[1]);
+  v.y = pack_bf16x2(x[2], x[3]);
+  v.z = pack_bf16x2(x[4], x[5]);
+  v.w = pack_bf16x2(x[6], x[7]);
+  return v;
+}
+
+}  // namespace swa

@@ -1,0 +1,324 @@
+// swa_fwd.cu — sliding-window attention forward on sm_103a.
+//
+// Computes, per query row i (FlashAttentionVarLenScore doc, "计算公式"):
+//   O_i = sum_j softmax_j(scale * q_i.k_j over visible j) * z_ij / keep * v_j
+// plus softmax_max_i and softmax_sum_i (before dropout), with the online
+// (blockwise) softmax of the PyPTO-Gym article's forward ("前向公式"; the
+// statistics it saves for the backward).
+//
+// One CTA = one 128-row query tile of one (batch, head); it walks only the
+// 128-key tiles that intersect the BAND window.  Warp roles:
+//   warps 0-3  softmax + epilogue, one thread per query row (TMEM lane)
+//   warp  4    TMA producer: Q once, K/V through a 2-stage ring
+//   warp  5    tcgen05 issuer: S = Q K^T into a double-buffered TMEM tile,
+//              O += P V with P (bf16) written to shared memory by warps 0-3
+// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D).
+#include "swa_device.cuh"
+
+namespace swa {
+namespace {
+
+template <int D>
+struct FwdSmem {
+  static constexpr int kTileBytes = kTileM * D * 2;
+  alignas(1024) uint8_t q[kTileBytes];
+  alignas(1024) uint8_t k[2][kTileBytes];
+  alignas(1024) uint8_t v[2][kTileBytes];
+  alignas(1024) uint8_t p[kTileM * kTileN * 2];
+  uint64_t q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], s_free[2], p_full, o_done, mma_drain;
+  uint32_t tmem_base;
+};
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 256;
+constexpr float kLn2 = 0.6931471805599453f;
+// Rescale O only when the running max grows by more than 2^8 (log2 units);
+// until then the stale max is kept and p may reach 256, far from overflow.
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D, bool DROP, int CAP>
+__global__ void __launch_bounds__(192, 1)
+    swa_fwd_kernel(const FwdArgs a, const __grid_constant__ SeqTable<CAP> tab, const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                   const __grid_constant__ CUtensorMap mv) {
+  extern __shared__ uint8_t smem_raw[];
+  FwdSmem<D>& s = *reinterpret_cast<FwdSmem<D>*>(align1024(smem_raw));
+  constexpr int kTileBytes = FwdSmem<D>::kTileBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Geometry& g = a.g;
+  const Item w = resolve_item(tab, a.g, static_cast<int>(blockIdx.x));
+  const SeqInfo sq = w.s;
+  const int q0 = w.tile * kTileM;
+  const int q_last = min(q0 + kTileM - 1, sq.q_len - 1);
+
+  // key tiles touched by this query tile
+  int lo = 0, hi = sq.kv_len - 1;
+  if (g.sparse_mode == 4) {
+    lo = max(lo, q0 - g.pre);
+    hi = min(hi, q_last + g.next);
+  }
+  int kv_t0 = 0, n_kv = 0;
+  if (lo <= hi) {
+    kv_t0 = lo / kTileN;
+    n_kv = hi / kTileN - kv_t0 + 1;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&s.q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.k_full[i], 1);
+      mbar_init(&s.v_full[i], 1);
+      mbar_init(&s.kv_empty[i], 1);
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.s_free[i], kTileM);
+    }
+    mbar_init(&s.p_full, kTileM);
+    mbar_init(&s.o_done, 1);
+    mbar_init(&s.mma_drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&s.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = s.tmem_base;
+
+  if (warp == 4) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0 && n_kv > 0) {
+      tma_prefetch_desc(&mq);
+      tma_prefetch_desc(&mk);
+      tma_prefetch_desc(&mv);
+      mbar_arrive_expect_tx(&s.q_full, kTileBytes);
+      tma_rows<D>(s.q, &mq, &s.q_full, g, w.b, w.n, sq.q_start, q0);
+      int issued = 0;
+      for (int it = 0; it < n_kv; ++it) {
+        const int st = it & 1;
+        if (it >= 2 && !mbar_wait(&s.kv_empty[st], ((it >> 1) - 1) & 1, a.err, kErrFwdLoad)) break;
+        const int j0 = (kv_t0 + it) * kTileN;
+        mbar_arrive_expect_tx(&s.k_full[st], kTileBytes);
+        tma_rows<D>(s.k[st], &mk, &s.k_full[st], g, w.b, w.n, sq.kv_start, j0);
+        mbar_arrive_expect_tx(&s.v_full[st], kTileBytes);
+        tma_rows<D>(s.v[st], &mv, &s.v_full[st], g, w.b, w.n, sq.kv_start, j0);
+        ++issued;
+      }
+      // every copy issued has landed before the CTA may exit
+      mbar_wait_drain(&s.q_full, 0);
+      for (int st = 0; st < 2; ++st) {
+        const int uses = (issued - st + 1) / 2;
+        if (uses > 0) {
+          mbar_wait_drain(&s.k_full[st], (uses - 1) & 1);
+          mbar_wait_drain(&s.v_full[st], (uses - 1) & 1);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ----------------------------------------------------- tcgen05 issuer --
+    if (lane == 0 && n_kv > 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(kTileM, kTileN, false, false);
+      constexpr uint32_t kIdO = idesc_bf16_f32(kTileM, D, false, true);
+      const uint32_t q_addr = smem_u32(s.q), p_addr = smem_u32(s.p);
+      bool ok = mbar_wait(&s.q_full, 0, a.err, kErrFwdMma);
+      for (int it = 0; ok && it <= n_kv; ++it) {
+        if (it < n_kv) {
+          const int st = it & 1;
+          if (!mbar_wait(&s.k_full[st], (it >> 1) & 1, a.err, kErrFwdMma)) break;
+          if (it >= 2 && !mbar_wait(&s.s_free[st], ((it >> 1) - 1) & 1, a.err, kErrFwdMma)) break;
+          tc_fence_after_sync();
+          const uint32_t k_addr = smem_u32(s.k[st]);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
+            umma_bf16_ss(tmem + st * kTileN, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
+                         kIdS, kk > 0);
+          }
+          umma_commit(&s.s_full[st]);
+        }
+        if (it >= 1) {
+          const int pj = it - 1, pst = pj & 1;
+          if (!mbar_wait(&s.p_full, pj & 1, a.err, kErrFwdMma)) break;
+          if (!mbar_wait(&s.v_full[pst], (pj >> 1) & 1, a.err, kErrFwdMma)) break;
+          tc_fence_after_sync();
+          const uint32_t v_addr = smem_u32(s.v[pst]);
+#pragma unroll
+          for (int kk = 0; kk < kTileN / 16; ++kk) {
+            const uint32_t aoff = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
+            umma_bf16_ss(tmem + kColO, sdesc_sw128(p_addr + aoff, 16, 1024),
+                         sdesc_sw128(v_addr + kk * 2048, kAtomBytes, 1024), kIdO, (pj > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&s.o_done);
+          umma_commit(&s.kv_empty[pst]);
+        }
+      }
+      umma_commit(&s.mma_drain);
+      mbar_wait_drain(&s.mma_drain, 0);
+    }
+  } else {
+    // ------------------------------------------ softmax + epilogue (rows) --
+    const int r = threadIdx.x;  // 0..127 == TMEM lane
+    const int i = q0 + r;
+    const bool row_valid = i < sq.q_len;
+    int wlo, whi;
+    key_window(g, sq, i, wlo, whi);
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float c = g.scale_log2;
+    float m_use = -INFINITY, m_true = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int it = 0; it < n_kv; ++it) {
+      const int sb = it & 1;
+      if (!mbar_wait(&s.s_full[sb], (it >> 1) & 1, a.err, kErrFwdSoftmax)) { ok = false; break; }
+      tc_fence_after_sync();
+      float x[kTileN];
+#pragma unroll
+      for (int ch = 0; ch < kTileN / 32; ++ch) {
+        uint32_t t32[32];
+        tmem_ld_32x32b_x32(tmem + lane_off + sb * kTileN + ch * 32, t32);
+        tmem_ld_wait(t32);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) x[ch * 32 + t] = __uint_as_float(t32[t]);
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&s.s_free[sb]);
+
+      const int j0 = (kv_t0 + it) * kTileN;
+      float mx = -INFINITY;
+      if (tile_fully_visible(g, sq, q0, j0)) {
+#pragma unroll
+        for (int t = 0; t < kTileN; ++t) {
+          x[t] *= c;
+          mx = fmaxf(mx, x[t]);
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < kTileN; ++t) {
+          const int j = j0 + t;
+          x[t] = (j >= wlo && j <= whi) ? x[t] * c : -INFINITY;
+          mx = fmaxf(mx, x[t]);
+        }
+      }
+      const float m_new = fmaxf(m_true, mx);
+      m_true = m_new;
+      const bool need = m_new > m_use + kRescaleThreshold;
+      const bool warp_need = __any_sync(0xFFFFFFFFu, need);
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2_approx(m_use - m_new);
+        m_use = m_new;
+      }
+      const float msub = (m_use == -INFINITY) ? 0.f : m_use;
+      float rs = 0.f;
+#pragma unroll
+      for (int t = 0; t < kTileN; ++t) {
+        x[t] = ex2_approx(x[t] - msub);
+        rs += x[t];
+      }
+      l = l * alpha + rs;
+      if (DROP) {
+        uint32_t bits[4] = {0u, 0u, 0u, 0u};
+        if (row_valid) load_keep_bits(a.mask, sq, w.n, i, j0, bits);
+#pragma unroll
+        for (int t = 0; t < kTileN; ++t)
+          if (!((bits[t >> 5] >> (t & 31)) & 1u)) x[t] = 0.f;
+      }
+      // The previous P V must be done before P is overwritten or O rescaled.
+      if (it >= 1) {
+        if (!mbar_wait(&s.o_done, (it - 1) & 1, a.err, kErrFwdSoftmax)) { ok = false; break; }
+        tc_fence_after_sync();
+        if (warp_need) {
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t t32[32];
+            const uint32_t addr = tmem + lane_off + kColO + ch * 32;
+            tmem_ld_32x32b_x32(addr, t32);
+            tmem_ld_wait(t32);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) t32[t] = __float_as_uint(__uint_as_float(t32[t]) * alpha);
+            tmem_st_32x32b_x32(addr, t32);
+          }
+          tmem_st_wait();
+        }
+      }
+#pragma unroll
+      for (int ch = 0; ch < kTileN / 8; ++ch) st_chunk_sw128(s.p, r, ch, pack8(&x[ch * 8]));
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(&s.p_full);
+    }
+    if (ok && n_kv > 0) {
+      ok = mbar_wait(&s.o_done, (n_kv - 1) & 1, a.err, kErrFwdSoftmax);
+      tc_fence_after_sync();
+    }
+    if (ok) {
+      // epilogue: O = acc / (l * keep), statistics before dropout
+      const float inv = (l > 0.f) ? g.inv_keep / l : 0.f;
+      __nv_bfloat16* orow = a.out + q_elem(g, sq, w.b, w.n, i);
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        float o[32];
+        if (n_kv > 0) {
+          uint32_t t32[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + kColO + ch * 32, t32);
+          tmem_ld_wait(t32);
+#pragma unroll
+          for (int t = 0; t < 32; ++t) o[t] = __uint_as_float(t32[t]) * inv;
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) o[t] = 0.f;
+        }
+        if (row_valid) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(orow + ch * 32)[q4] = pack8(&o[q4 * 8]);
+        }
+      }
+      if (row_valid) {
+        const int64_t si = stat_index(g, sq, w.b, w.n, i);
+        const bool empty = (m_true == -INFINITY);
+        a.smax[si] = empty ? -INFINITY : m_true * kLn2;
+        a.ssum[si] = empty ? 0.f : l * ex2_approx(m_use - m_true);
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, bool DROP, int CAP>
+cudaError_t launch_fwd_t(const FwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
+                         const CUtensorMap& mv, cudaStream_t stream) {
+  const size_t smem = sizeof(FwdSmem<D>) + 1024;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(swa_fwd_kernel<D, DROP, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  swa_fwd_kernel<D, DROP, CAP><<<tab.n_items, 192, smem, stream>>>(a, tab, mq, mk, mv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+template <int CAP>
+cudaError_t launch_forward(const FwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
+                           const CUtensorMap& mv, cudaStream_t stream) {
+  if (tab.n_items == 0) return cudaSuccess;
+  const bool drop = a.g.has_mask != 0;
+  if (a.g.D == 64) return drop ? launch_fwd_t<64, true>(a, tab, mq, mk, mv, stream)
+                               : launch_fwd_t<64, false>(a, tab, mq, mk, mv, stream);
+  return drop ? launch_fwd_t<128, true>(a, tab, mq, mk, mv, stream)
+              : launch_fwd_t<128, false>(a, tab, mq, mk, mv, stream);
+}
+
+template cudaError_t launch_forward<kSmallTable>(const FwdArgs&, const SeqTable<kSmallTable>&, const CUtensorMap&,
+                                                 const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+template cudaError_t launch_forward<kLargeTable>(const FwdArgs&, const SeqTable<kLargeTable>&, const CUtensorMap&,
+                                                 const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+
+}  // namespace swa

@@ -1,0 +1,124 @@
+// swa_internal.h — shapes shared by the host scheduler and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace swa {
+
+constexpr int kTileM = 128;  // query rows per tile (tcgen05 M)
+constexpr int kTileN = 128;  // key rows per tile
+
+// One sequence of the batch as a kernel sees it.  BNSD: q_start = kv_start = 0
+// (rows are addressed through b); TND: start rows inside [0, T).
+struct SeqInfo {
+  int32_t q_start, q_len, kv_start, kv_len;
+  int64_t mask_base;  // dropout bit index of (n = 0, i = 0, j = 0) of this batch
+};
+
+// Work description passed to a kernel as a parameter (no device upload):
+// a run of `heads * tiles` work items per entry.  A work item is one 128-row
+// query tile (forward) or key tile (backward) of one (batch, head).  For BNSD a
+// single entry covers all B*N heads (b < 0; b = head / N); for TND each entry
+// is one sequence (b >= 0; head = n).  Entries are ordered heaviest first and
+// `descending` visits the tiles of an entry from the last one, so that the
+// CTAs that start first carry the most work.
+struct SeqDesc {
+  int32_t q_start, q_len, kv_start, kv_len;
+  int64_t mask_base;
+  int32_t item_begin;  // first work item of this entry
+  int32_t b;           // TND batch index, -1 for BNSD
+  int32_t tiles;       // 128-row tiles per head
+  int32_t heads;       // N (TND) or B*N (BNSD)
+  int32_t descending;
+  int32_t pad;
+};
+static_assert(sizeof(SeqDesc) == 48, "SeqDesc layout");
+
+template <int CAP>
+struct SeqTable {
+  int32_t count;    // entries used
+  int32_t n_items;  // work items of this launch
+  int64_t pad;
+  SeqDesc d[CAP];
+};
+constexpr int kSmallTable = 16;
+constexpr int kLargeTable = 512;
+
+// Workspace header (first 256 bytes of every workspace).
+struct WsHeader {
+  int32_t error;       // 0 = fine; otherwise the code of the wait that gave up
+  int32_t pad[63];
+};
+constexpr size_t kHeaderBytes = 256;
+
+// Error codes a kernel stores into WsHeader::error.
+enum : int32_t {
+  kErrFwdLoad = 1,
+  kErrFwdMma = 2,
+  kErrFwdSoftmax = 3,
+  kErrBwdLoad = 11,
+  kErrBwdMma = 12,
+  kErrBwdCompute = 13,
+};
+
+struct Geometry {
+  int32_t layout;  // 0 = BNSD, 1 = TND
+  int32_t N, D;
+  int32_t S_q, S_kv;  // BNSD (per-batch lengths)
+  int32_t sparse_mode;
+  int32_t pre, next;  // clamped into +-(max sequence length + 1)
+  float scale;        // score scale
+  float scale_log2;   // scale * log2(e)
+  float inv_keep;     // 1 / keep_prob
+  int32_t has_mask;   // drop_mask given
+};
+
+struct FwdArgs {
+  Geometry g;
+  const uint8_t* mask;
+  __nv_bfloat16* out;
+  float* smax;
+  float* ssum;
+  int32_t* err;
+};
+
+struct BwdArgs {
+  Geometry g;
+  const uint8_t* mask;
+  const float* lse2;   // per query row: softmax_max*log2(e) + log2(softmax_sum); +inf for empty rows
+  const float* dsum;   // per query row: D = rowsum(dY * O)
+  float* dq_acc;       // fp32, q's layout: sum_j dS_ij k_j (scale applied at conversion)
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int32_t* err;
+};
+
+struct PrepArgs {
+  Geometry g;
+  int64_t rows;  // query rows x heads
+  int32_t* err;  // workspace error word, cleared here before the backward kernel runs
+  const __nv_bfloat16* dy;
+  const __nv_bfloat16* out;
+  const float* smax;
+  const float* ssum;
+  float* lse2;
+  float* dsum;
+  float* dq_acc;
+};
+
+// Kernel launchers (defined in the .cu files).  Each returns the launch's
+// cudaError_t.
+template <int CAP>
+cudaError_t launch_forward(const FwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
+                           const CUtensorMap& mv, cudaStream_t stream);
+template <int CAP>
+cudaError_t launch_backward(const BwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
+                            const CUtensorMap& mv, const CUtensorMap& mdy, cudaStream_t stream);
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream);
+cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int64_t n_elems, float scale,
+                              cudaStream_t stream);
+
+}  // namespace swa

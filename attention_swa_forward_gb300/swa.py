@@ -1,0 +1,217 @@
+"""Thin Python binding of libswa's C ABI (include/swa.h).
+
+Argument marshalling only: every step of the attention computation runs in the
+CUDA kernels of libswa.so.  PyTorch supplies device memory and streams.  If the
+compiled library is missing, every call raises -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libswa.so")
+
+SWA_OK = 0
+SWA_ERR_PARAM_NULLPTR = 161001
+SWA_ERR_PARAM_INVALID = 161002
+SWA_ERR_UNSUPPORTED = 161100
+SWA_ERR_WORKSPACE = 161101
+SWA_ERR_CUDA = 161102
+SWA_ERR_TIMEOUT = 161103
+LAYOUTS = {"BNSD": 0, "TND": 1}
+
+
+class SwaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"libswa status {status}: {message}")
+        self.status = status
+
+
+class SwaParams(ctypes.Structure):
+    """Mirror of swa_params_t."""
+
+    _fields_ = [
+        ("layout", ctypes.c_int32),
+        ("B", ctypes.c_int64),
+        ("N", ctypes.c_int64),
+        ("D", ctypes.c_int64),
+        ("S_q", ctypes.c_int64),
+        ("S_kv", ctypes.c_int64),
+        ("T_q", ctypes.c_int64),
+        ("T_kv", ctypes.c_int64),
+        ("cu_seqlens_q", ctypes.POINTER(ctypes.c_int64)),
+        ("cu_seqlens_kv", ctypes.POINTER(ctypes.c_int64)),
+        ("scale", ctypes.c_double),
+        ("pre_tokens", ctypes.c_int64),
+        ("next_tokens", ctypes.c_int64),
+        ("sparse_mode", ctypes.c_int32),
+        ("keep_prob", ctypes.c_double),
+    ]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    """Load libswa.so (built in-tree by ``build.build()``); raise if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: build it with attention_swa_forward_gb300.build.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            P = ctypes.POINTER(SwaParams)
+            vp, sz = ctypes.c_void_p, ctypes.c_size_t
+            st = ctypes.c_int
+            L.swa_params_default.argtypes = [P]
+            L.swa_params_default.restype = None
+            L.swa_forward_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
+            L.swa_forward_workspace_size.restype = st
+            L.swa_backward_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
+            L.swa_backward_workspace_size.restype = st
+            L.swa_forward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.swa_forward.restype = st
+            L.swa_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.swa_backward.restype = st
+            L.swa_workspace_status.argtypes = [vp, vp]
+            L.swa_workspace_status.restype = st
+            L.swa_set_timing_events.argtypes = [vp, vp, vp, vp]
+            L.swa_set_timing_events.restype = None
+            L.swa_last_error.argtypes = []
+            L.swa_last_error.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def exported_symbols():
+    return ["swa_params_default", "swa_forward_workspace_size", "swa_forward", "swa_backward_workspace_size",
+            "swa_backward", "swa_workspace_status", "swa_set_timing_events", "swa_last_error"]
+
+
+def _check(status: int):
+    if status != SWA_OK:
+        raise SwaError(status, lib().swa_last_error().decode())
+
+
+class Params:
+    """swa_params_t built from a geometry object (fields as in ``workloads.Geometry``)."""
+
+    def __init__(self, geom):
+        self.geom = geom
+        self.c = SwaParams()
+        lib().swa_params_default(ctypes.byref(self.c))
+        c = self.c
+        c.layout = LAYOUTS[geom.layout]
+        c.B, c.N, c.D = geom.B, geom.N, geom.D
+        self._cu_q = self._cu_kv = None
+        if geom.layout == "BNSD":
+            c.S_q, c.S_kv = geom.S_q, geom.S_kv
+        else:
+            self._cu_q = (ctypes.c_int64 * len(geom.cu_seqlens_q))(*[int(x) for x in geom.cu_seqlens_q])
+            self._cu_kv = (ctypes.c_int64 * len(geom.cu_seqlens_kv))(*[int(x) for x in geom.cu_seqlens_kv])
+            c.cu_seqlens_q = ctypes.cast(self._cu_q, ctypes.POINTER(ctypes.c_int64))
+            c.cu_seqlens_kv = ctypes.cast(self._cu_kv, ctypes.POINTER(ctypes.c_int64))
+            c.T_q = max(int(x) for x in geom.cu_seqlens_q)
+            c.T_kv = max(int(x) for x in geom.cu_seqlens_kv)
+        c.scale = float(geom.scale)
+        c.pre_tokens = int(geom.pre_tokens)
+        c.next_tokens = int(geom.next_tokens)
+        c.sparse_mode = int(geom.sparse_mode)
+        c.keep_prob = float(geom.keep_prob)
+
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+# ------------------------------------------------------------ raw C calls --
+def swa_forward_workspace_size(params: Params) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().swa_forward_workspace_size(params.ref(), ctypes.byref(n)))
+    return n.value
+
+
+def swa_backward_workspace_size(params: Params) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().swa_backward_workspace_size(params.ref(), ctypes.byref(n)))
+    return n.value
+
+
+def swa_forward(params: Params, q, k, v, drop_mask, out, softmax_max, softmax_sum, workspace, workspace_bytes,
+                stream) -> int:
+    """Raw call with integer device pointers; returns the status code."""
+    return lib().swa_forward(params.ref(), q, k, v, drop_mask, out, softmax_max, softmax_sum, workspace,
+                             workspace_bytes, stream)
+
+
+def swa_backward(params: Params, q, k, v, dy, out, softmax_max, softmax_sum, drop_mask, dq, dk, dv, workspace,
+                 workspace_bytes, stream) -> int:
+    return lib().swa_backward(params.ref(), q, k, v, dy, out, softmax_max, softmax_sum, drop_mask, dq, dk, dv,
+                              workspace, workspace_bytes, stream)
+
+
+def swa_workspace_status(workspace, stream) -> int:
+    return lib().swa_workspace_status(workspace, stream)
+
+
+def swa_set_timing_events(fwd_start=None, fwd_stop=None, bwd_start=None, bwd_stop=None):
+    """Raw cudaEvent_t handles (ints) recorded around the main kernels; None clears."""
+    lib().swa_set_timing_events(fwd_start, fwd_stop, bwd_start, bwd_stop)
+
+
+def swa_last_error() -> str:
+    return lib().swa_last_error().decode()
+
+
+# ------------------------------------------------------- torch convenience --
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def forward(geom, q, k, v, drop_mask=None, out=None, softmax_max=None, softmax_sum=None, workspace=None,
+            stream=None):
+    """Enqueue swa_forward on device tensors; returns (out, softmax_max, softmax_sum)."""
+    p = Params(geom)
+    dev = q.device
+    out = torch.empty_like(q) if out is None else out
+    stat_shape = tuple(geom.stat_shape()) if hasattr(geom, "stat_shape") else None
+    if softmax_max is None:
+        softmax_max = torch.empty(stat_shape, dtype=torch.float32, device=dev)
+    if softmax_sum is None:
+        softmax_sum = torch.empty(stat_shape, dtype=torch.float32, device=dev)
+    need = swa_forward_workspace_size(p)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _check(swa_forward(p, _ptr(q), _ptr(k), _ptr(v), _ptr(drop_mask), _ptr(out), _ptr(softmax_max),
+                       _ptr(softmax_sum), _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+    return out, softmax_max, softmax_sum
+
+
+def backward(geom, q, k, v, dy, out, softmax_max, softmax_sum, drop_mask=None, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """Enqueue swa_backward on device tensors; returns (dq, dk, dv)."""
+    p = Params(geom)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = swa_backward_workspace_size(p)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(swa_backward(p, _ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(out), _ptr(softmax_max), _ptr(softmax_sum),
+                        _ptr(drop_mask), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
+                        _stream_handle(stream)))
+    return dq, dk, dv
+
+
+def check_workspace(workspace, stream=None):
+    """Wait for the stream and raise if a kernel gave up a bounded wait."""
+    _check(swa_workspace_status(_ptr(workspace), _stream_handle(stream)))

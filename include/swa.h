@@ -1,0 +1,158 @@
+/*
+ * swa.h — C ABI of libswa: sliding-window (BAND) / unmasked FlashAttention
+ * forward and backward on GB300 (sm_103a).
+ *
+ * The operation (FlashAttentionVarLenScore doc, "计算公式"; PyPTO-Gym
+ * FlashAttentionScoreGrad article, "前向公式" / "反向公式"):
+ *
+ *   forward   O = Dropout(Softmax(Mask(scale * Q K^T)), keep_prob) V
+ *             softmax_max_i = max_{j visible} scale * q_i.k_j
+ *             softmax_sum_i = sum_{j visible} exp(scale * q_i.k_j - softmax_max_i)
+ *   backward  P  = exp(scale * Q K^T - softmax_max) / softmax_sum
+ *             D  = rowsum(dY * O)
+ *             dP = (dY V^T) * z / keep_prob
+ *             dS = P * (dP - D)
+ *             dV = (P * z / keep_prob)^T dY,  dQ = scale dS K,  dK = scale dS^T Q
+ *
+ * Mask ("sparse_mode", FlashAttentionVarLenScore doc, parameter
+ * sparseModeOptional; the split into swa_forward / swa_backward limited to
+ * modes 0 and 4 follows the pzsr.cn article, §1.2 and §3):
+ *   0  no mask: query i sees every key of its sequence;
+ *   4  BAND: query i sees key j iff  i - pre_tokens <= j <= i + next_tokens
+ *      (indices local to the sequence, top-left aligned when Sq != Skv).
+ * A query row that sees no key gets out = 0, softmax_max = -inf,
+ * softmax_sum = 0 and a zero dq row; it contributes nothing to dk / dv.
+ *
+ * Dropout (doc parameter dropMaskOptional / keepProbOptional): drop_mask is
+ * a packed bit mask, 8 elements per byte, least significant bit first,
+ * 1 = keep.  Element order: BNSD e = ((b*N + n)*Sq + i)*Skv + j; TND
+ * e = sum_{b'<b} N*Sq_b'*Skv_b' + (n*Sq_b + i)*Skv_b + j (no padding).
+ * softmax_sum excludes dropout; kept probabilities are scaled by 1/keep_prob.
+ *
+ * Layouts (doc parameter list, inputLayout; PyPTO-Gym article, I/O table):
+ *   BNSD  q, dy, out, dq: [B, N, S_q, D];  k, v, dk, dv: [B, N, S_kv, D]
+ *         softmax_max / softmax_sum: [B, N, S_q] fp32
+ *   TND   q, dy, out, dq: [T_q, N, D];     k, v, dk, dv: [T_kv, N, D]
+ *         softmax_max / softmax_sum: [T_q, N] fp32
+ *   All tensors are dense, row-major, bf16 unless stated, device memory,
+ *   16-byte aligned.  D must be 64 or 128.
+ *
+ * Variable length (TND): cu_seqlens_q / cu_seqlens_kv are HOST arrays of
+ * length B holding cumulative sequence ends without a leading 0 (doc
+ * parameters actualSeqQLenOptional / actualSeqKvLenOptional).  A length-0
+ * sequence is allowed; a trailing run of zeros marks skipped batches
+ * (aclnnFlashAttentionUnpaddingScoreGradV2 article, §6.4).  The last
+ * non-zero entry must equal T.
+ *
+ * Two-phase calls (doc, "两段式接口"): ask for the workspace size, let the
+ * caller allocate it in device memory, then call.  The library allocates
+ * nothing, keeps no pointer after a call returns and reads host arrays only
+ * during the call.  Calls only enqueue work on `stream` (a cudaStream_t) and
+ * return; results are ready when the stream is.  A workspace may be reused
+ * by later calls on the same stream but not by calls running concurrently.
+ *
+ * Status codes follow the aclnn numbering (doc, "返回值").
+ */
+#ifndef SWA_H
+#define SWA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SWA_API __attribute__((visibility("default")))
+#else
+#define SWA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *swa_stream_t; /* same type as cudaStream_t */
+
+typedef enum { SWA_LAYOUT_BNSD = 0, SWA_LAYOUT_TND = 1 } swa_layout_t;
+
+typedef enum {
+  SWA_OK = 0,
+  SWA_ERR_PARAM_NULLPTR = 161001, /* a required pointer is NULL */
+  SWA_ERR_PARAM_INVALID = 161002, /* a value is outside its documented range */
+  SWA_ERR_UNSUPPORTED = 161100,   /* valid per the API but not built (e.g. D not in {64, 128}) */
+  SWA_ERR_WORKSPACE = 161101,     /* workspace NULL or smaller than the size query says */
+  SWA_ERR_CUDA = 161102,          /* a CUDA runtime call failed (text in swa_last_error) */
+  SWA_ERR_TIMEOUT = 161103        /* a kernel gave up a bounded wait (swa_workspace_status) */
+} swa_status_t;
+
+typedef struct {
+  int32_t layout;               /* swa_layout_t */
+  int64_t B, N, D;              /* batch, heads (headNum), head dim (64 or 128) */
+  int64_t S_q, S_kv;            /* BNSD sequence lengths (ignored for TND) */
+  int64_t T_q, T_kv;            /* TND total rows (ignored for BNSD) */
+  const int64_t *cu_seqlens_q;  /* TND: host, length B, cumulative ends (see above) */
+  const int64_t *cu_seqlens_kv; /* TND: host, length B */
+  double scale;                 /* score scale, default 1.0, usually D^-0.5 */
+  int64_t pre_tokens;           /* BAND left extent, default 2147483647 */
+  int64_t next_tokens;          /* BAND right extent, default 2147483647 */
+  int32_t sparse_mode;          /* 0 or 4 */
+  double keep_prob;             /* dropout keep probability in (0, 1], default 1.0 */
+} swa_params_t;
+
+/* Fill `p` with the documented defaults (FlashAttentionScore REG_OP
+ * attribute defaults): scale 1.0, keep_prob 1.0, pre/next 2147483647,
+ * sparse_mode 0; everything else zero / NULL. */
+SWA_API void swa_params_default(swa_params_t *p);
+
+/* Device workspace bytes that swa_forward needs for these parameters (a
+ * status word; the work schedule travels as a kernel parameter).  Errors: SWA_ERR_PARAM_NULLPTR, SWA_ERR_PARAM_INVALID, SWA_ERR_UNSUPPORTED. */
+SWA_API swa_status_t swa_forward_workspace_size(const swa_params_t *p, size_t *bytes);
+
+/* Forward (doc formula; PyPTO-Gym "前向公式").
+ *   q, k, v       device, bf16, layout per p->layout
+ *   drop_mask     device, packed keep bits, 16-byte aligned; NULL iff keep_prob == 1
+ *   out           device, bf16, q's shape
+ *   softmax_max   device, fp32, [B,N,S_q] or [T_q,N]
+ *   softmax_sum   device, fp32, same shape
+ *   workspace     device, >= swa_forward_workspace_size bytes, 256-byte aligned
+ * Errors: the size query's, plus SWA_ERR_WORKSPACE and SWA_ERR_CUDA.  Nothing
+ * is enqueued when a status other than SWA_OK is returned. */
+SWA_API swa_status_t swa_forward(const swa_params_t *p, const void *q, const void *k, const void *v,
+                         const uint8_t *drop_mask, void *out, float *softmax_max, float *softmax_sum,
+                         void *workspace, size_t workspace_bytes, swa_stream_t stream);
+
+/* Device workspace bytes that swa_backward needs: a status word, per query
+ * row D = rowsum(dY*O) and the log2-sum-exp of the forward statistics, and
+ * an fp32 dQ accumulator of q's shape. */
+SWA_API swa_status_t swa_backward_workspace_size(const swa_params_t *p, size_t *bytes);
+
+/* Backward (PyPTO-Gym "反向公式"; aclnnFlashAttentionUnpaddingScoreGradV2
+ * article §2.3).  out / softmax_max / softmax_sum are this library's forward
+ * results for the same q, k, v, drop_mask and parameters.
+ *   dy            device, bf16, q's shape (gradient of out)
+ *   dq, dk, dv    device, bf16, shapes of q, k, v; fully overwritten
+ * Errors: as swa_forward. */
+SWA_API swa_status_t swa_backward(const swa_params_t *p, const void *q, const void *k, const void *v, const void *dy,
+                          const void *out, const float *softmax_max, const float *softmax_sum,
+                          const uint8_t *drop_mask, void *dq, void *dk, void *dv, void *workspace,
+                          size_t workspace_bytes, swa_stream_t stream);
+
+/* Wait for `stream`, then report whether any kernel of the last call that
+ * used `workspace` gave up a bounded wait: SWA_OK or SWA_ERR_TIMEOUT
+ * (SWA_ERR_CUDA if the stream itself failed). */
+SWA_API swa_status_t swa_workspace_status(const void *workspace, swa_stream_t stream);
+
+/* Measurement support.  When non-NULL, the following calls on this thread
+ * record `start` on their stream immediately before launching their main
+ * attention kernel and `stop` immediately after it: fwd_* around the forward
+ * kernel of swa_forward, bwd_* around the key-major kernel of swa_backward.
+ * The events are cudaEvent_t handles owned by the caller; pass NULL to stop
+ * recording.  No other effect on the computation. */
+SWA_API void swa_set_timing_events(void *fwd_start, void *fwd_stop, void *bwd_start, void *bwd_stop);
+
+/* Text describing the last non-OK status returned on this thread. */
+SWA_API const char *swa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWA_H */

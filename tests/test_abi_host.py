@@ -1,0 +1,159 @@
+"""Host-side checks of the C ABI (no GPU): the library builds and loads, exports
+every symbol include/swa.h declares, the ctypes mirror matches the C struct,
+and every argument check returns its documented status code before any CUDA
+work is enqueued."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from attention_swa_forward_gb300 import build as B
+from attention_swa_forward_gb300 import swa
+from attention_swa_forward_gb300.workloads import WORKLOADS, Geometry
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return swa.lib()
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "swa.h")).read()
+    return sorted(set(re.findall(r"SWA_API\s+[\w\s\*]+?\b(swa_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_symbols()
+    assert declared, "no declarations found"
+    out = subprocess.run(["nm", "-D", "--defined-only", swa.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (swa_\w+)", out))
+    assert set(declared) == exported, (declared, exported)
+    for name in declared:
+        assert hasattr(lib, name)
+    assert sorted(swa.exported_symbols()) == declared
+
+
+def test_ctypes_struct_matches_c_layout(tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "swa.h"\n'
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu\\n\", sizeof(swa_params_t),"
+        " offsetof(swa_params_t, B), offsetof(swa_params_t, cu_seqlens_q), offsetof(swa_params_t, scale),"
+        " offsetof(swa_params_t, sparse_mode), offsetof(swa_params_t, keep_prob));return 0;}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
+    P = swa.SwaParams
+    want = [ctypes.sizeof(P), P.B.offset, P.cu_seqlens_q.offset, P.scale.offset, P.sparse_mode.offset,
+            P.keep_prob.offset]
+    assert got == want
+
+
+def test_defaults_match_documented_attributes(lib):
+    p = swa.SwaParams()
+    lib.swa_params_default(ctypes.byref(p))
+    assert p.scale == 1.0 and p.keep_prob == 1.0
+    assert p.pre_tokens == 2147483647 and p.next_tokens == 2147483647
+    assert p.sparse_mode == 0
+
+
+def _size(geom, backward=False):
+    p = swa.Params(geom)
+    n = ctypes.c_size_t(0)
+    fn = swa.lib().swa_backward_workspace_size if backward else swa.lib().swa_forward_workspace_size
+    return fn(p.ref(), ctypes.byref(n)), n.value
+
+
+BASE = dict(layout="BNSD", B=1, N=2, D=128, S_q=256, S_kv=256, scale=0.1, sparse_mode=4, pre_tokens=64,
+            next_tokens=0)
+
+
+@pytest.mark.parametrize("change,status", [
+    ({}, swa.SWA_OK),
+    ({"sparse_mode": 1}, swa.SWA_ERR_PARAM_INVALID),
+    ({"sparse_mode": 3}, swa.SWA_ERR_PARAM_INVALID),
+    ({"keep_prob": 0.0}, swa.SWA_ERR_PARAM_INVALID),
+    ({"keep_prob": 1.5}, swa.SWA_ERR_PARAM_INVALID),
+    ({"keep_prob": float("nan")}, swa.SWA_ERR_PARAM_INVALID),
+    ({"N": 0}, swa.SWA_ERR_PARAM_INVALID),
+    ({"N": 257}, swa.SWA_ERR_PARAM_INVALID),
+    ({"B": 0}, swa.SWA_ERR_PARAM_INVALID),
+    ({"D": 96}, swa.SWA_ERR_UNSUPPORTED),
+    ({"D": 1000}, swa.SWA_ERR_PARAM_INVALID),
+    ({"S_q": 0}, swa.SWA_ERR_PARAM_INVALID),
+    ({"pre_tokens": -10, "next_tokens": 5}, swa.SWA_ERR_PARAM_INVALID),
+    ({"pre_tokens": -10, "next_tokens": 5, "sparse_mode": 0}, swa.SWA_OK),
+    ({"pre_tokens": -1, "next_tokens": 2}, swa.SWA_OK),
+    ({"scale": float("inf")}, swa.SWA_ERR_PARAM_INVALID),
+    ({"D": 64}, swa.SWA_OK),
+])
+def test_parameter_checks(lib, change, status):
+    st, _ = _size(Geometry(**{**BASE, **change}))
+    assert st == status, swa.swa_last_error()
+    if status != swa.SWA_OK:
+        assert swa.swa_last_error()
+
+
+@pytest.mark.parametrize("cu_q,cu_kv,status", [
+    ([2, 5, 9], [2, 5, 9], swa.SWA_OK),
+    ([2, 5, 9, 0, 0], [2, 5, 9, 0, 0], swa.SWA_OK),   # trailing zeros skip batches
+    ([0, 5, 5, 9], [3, 3, 6, 9], swa.SWA_OK),         # length-0 sequences
+    ([2, 5, 4], [2, 5, 9], swa.SWA_ERR_PARAM_INVALID),  # decreasing
+    ([2, 5, 8], [2, 5, 9], swa.SWA_ERR_PARAM_INVALID),  # last != T
+    ([2, 5, 9, 0, 3], [2, 5, 9, 0, 0], swa.SWA_ERR_PARAM_INVALID),  # non-zero after the tail
+    ([2, 5, 0, 9], [2, 5, 0, 9], swa.SWA_ERR_PARAM_INVALID),  # tail before reaching T
+])
+def test_cumulative_lengths(lib, cu_q, cu_kv, status):
+    g = Geometry("TND", len(cu_q), 2, 64, cu_seqlens_q=cu_q, cu_seqlens_kv=cu_kv, sparse_mode=0)
+    p = swa.Params(g)
+    p.c.T_q = 9  # the T the caller states
+    p.c.T_kv = 9
+    n = ctypes.c_size_t(0)
+    assert swa.lib().swa_forward_workspace_size(p.ref(), ctypes.byref(n)) == status, swa.swa_last_error()
+
+
+def test_null_params_and_pointers(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.swa_forward_workspace_size(None, ctypes.byref(n)) == swa.SWA_ERR_PARAM_NULLPTR
+    p = swa.Params(Geometry(**BASE))
+    assert lib.swa_forward_workspace_size(p.ref(), None) == swa.SWA_ERR_PARAM_NULLPTR
+    fake = 1 << 20  # never dereferenced: every check below fails first
+    st = swa.swa_forward(p, None, fake, fake, None, fake, fake, fake, fake, 256, None)
+    assert st == swa.SWA_ERR_PARAM_NULLPTR
+    st = swa.swa_backward(p, fake, fake, fake, fake, fake, fake, fake, None, fake, None, fake, fake, 1 << 30, None)
+    assert st == swa.SWA_ERR_PARAM_NULLPTR
+    g = Geometry("TND", 1, 2, 64, cu_seqlens_q=[4], cu_seqlens_kv=[4])
+    pt = swa.Params(g)
+    pt.c.cu_seqlens_q = None
+    assert lib.swa_forward_workspace_size(pt.ref(), ctypes.byref(n)) == swa.SWA_ERR_PARAM_NULLPTR
+
+
+def test_dropout_mask_presence_and_alignment_and_workspace(lib):
+    fake = 1 << 20
+    p = swa.Params(Geometry(**{**BASE, "keep_prob": 0.9}))
+    assert swa.swa_forward(p, fake, fake, fake, None, fake, fake, fake, fake, 256, None) == swa.SWA_ERR_PARAM_INVALID
+    p1 = swa.Params(Geometry(**BASE))
+    assert swa.swa_forward(p1, fake, fake, fake, fake, fake, fake, fake, fake, 256, None) == swa.SWA_ERR_PARAM_INVALID
+    assert swa.swa_forward(p1, fake + 2, fake, fake, None, fake, fake, fake, fake, 256, None) == \
+        swa.SWA_ERR_PARAM_INVALID
+    assert swa.swa_forward(p1, fake, fake, fake, None, fake, fake, fake, None, 256, None) == swa.SWA_ERR_WORKSPACE
+    assert swa.swa_forward(p1, fake, fake, fake, None, fake, fake, fake, fake, 128, None) == swa.SWA_ERR_WORKSPACE
+    need = swa.swa_backward_workspace_size(p1)
+    assert swa.swa_backward(p1, fake, fake, fake, fake, fake, fake, fake, None, fake, fake, fake, fake, need - 256,
+                            None) == swa.SWA_ERR_WORKSPACE
+
+
+def test_workspace_sizes_scale_with_rows(lib):
+    g = WORKLOADS["bnsd_1x32x32768x128_band4096"].geom
+    st_f, f = _size(g)
+    st_b, b = _size(g, backward=True)
+    assert st_f == swa.SWA_OK and st_b == swa.SWA_OK
+    rows = g.B * g.S_q * g.N
+    assert f == 256
+    assert b >= rows * g.D * 4 + 2 * rows * 4  # fp32 dQ accumulator + D + lse2
+    assert b < rows * g.D * 4 + 2 * rows * 4 + 4096

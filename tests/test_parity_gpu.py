@@ -1,0 +1,323 @@
+"""GPU parity: libswa's CUDA path against the fp64 CPU oracle, element by
+element on seeded inputs, through the C ABI.
+
+Tolerances (bf16 inputs, fp32 accumulation): relative L2 <= 5e-3 for out and
+<= 1e-2 for dq / dk / dv; element-wise |got - ref| <= 2e-2 + 1e-2*|ref| for
+all four (the assert_allclose(rtol=1e-2, atol=2e-2) criterion of the PyPTO-Gym
+FlashAttentionScoreGrad article, "运行测试": a bare 2e-2 absolute bound is
+below the bf16 rounding of the result itself once |ref| exceeds ~4);
+relative error <= 1e-3 on softmax_max / softmax_sum; and the set of visible
+keys of every query row identical to the oracle's.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from attention_swa_forward_gb300 import build as B
+from attention_swa_forward_gb300 import swa
+from attention_swa_forward_gb300.workloads import WORKLOADS, Geometry, draw, draw_workload
+from oracle import swa_oracle as orc
+from tests.helpers import max_abs, rel_l2, to_problem
+
+pytestmark = pytest.mark.gpu
+
+TOL_OUT = 5e-3
+TOL_GRAD = 1e-2
+TOL_ABS = 2e-2
+TOL_REL_ELEM = 1e-2
+TOL_STAT = 1e-3
+
+
+def excess(got, ref):
+    """max over elements of |got - ref| - (atol + rtol*|ref|); <= 0 passes."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if got.size == 0:
+        return 0.0
+    return float(np.max(np.abs(got - ref) - (TOL_ABS + TOL_REL_ELEM * np.abs(ref))))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    B.build()
+    orc.build()
+    swa.lib()
+
+
+def run_gpu(inp, backward=True):
+    """Forward (+ backward) on cuda:0 through the binding; results as float64 numpy."""
+    g = inp.geom
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
+    mask = inp.drop_mask.to(dev) if inp.drop_mask is not None else None
+    out, smax, ssum = swa.forward(g, q, k, v, mask)
+    res = {"out": out, "smax": smax, "ssum": ssum}
+    ws_f = None
+    if backward:
+        dy = inp.dy.to(dev)
+        need = swa.swa_backward_workspace_size(swa.Params(g))
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        dq, dk, dv = swa.backward(g, q, k, v, dy, out, smax, ssum, mask, workspace=ws)
+        swa.check_workspace(ws)
+        res.update(dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    return {k_: t.cpu() for k_, t in res.items()}
+
+
+def as_np(res):
+    return {k_: t.double().numpy() for k_, t in res.items()}
+
+
+def stat_rel(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    both_inf = np.isneginf(got) & np.isneginf(ref)
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref)), "empty rows differ"
+    g, r = got[~both_inf], ref[~both_inf]
+    if g.size == 0:
+        return 0.0
+    return float(np.max(np.abs(g - r) / np.maximum(np.abs(r), 1.0)))
+
+
+def check_forward(res, out, smax, ssum, label=""):
+    assert np.all(np.isfinite(res["out"]))
+    e_out, a_out = rel_l2(res["out"], out), excess(res["out"], out)
+    assert e_out <= TOL_OUT and a_out <= 0.0, (label, "out", e_out, a_out, max_abs(res["out"], out))
+    assert stat_rel(res["smax"], smax) <= TOL_STAT, (label, "softmax_max")
+    assert stat_rel(res["ssum"], ssum) <= TOL_STAT, (label, "softmax_sum")
+
+
+def check_grads(res, dq, dk, dv, label=""):
+    for name, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
+        got = res[name]
+        assert np.all(np.isfinite(got)), (label, name)
+        e, a = rel_l2(got, ref), excess(got, ref)
+        assert e <= TOL_GRAD and a <= 0.0, (label, name, e, a, max_abs(got, ref))
+
+
+# ----------------------------------------------------------- small cases --
+SMALL = {
+    "bnsd_nomask_d64_ragged": dict(layout="BNSD", B=2, N=2, D=64, S_q=300, S_kv=300, scale=0.125, sparse_mode=0),
+    "bnsd_band_d128_ragged": dict(layout="BNSD", B=1, N=3, D=128, S_q=517, S_kv=517, scale=128 ** -0.5,
+                                  sparse_mode=4, pre_tokens=200, next_tokens=0),
+    "bnsd_symband_d64_dropout": dict(layout="BNSD", B=2, N=2, D=64, S_q=400, S_kv=400, scale=0.125, sparse_mode=4,
+                                     pre_tokens=70, next_tokens=90, keep_prob=0.8),
+    "bnsd_band_d128_dropout_ragged": dict(layout="BNSD", B=1, N=2, D=128, S_q=333, S_kv=333, scale=0.09,
+                                          sparse_mode=4, pre_tokens=150, next_tokens=40, keep_prob=0.7),
+    "bnsd_rect_band": dict(layout="BNSD", B=1, N=2, D=128, S_q=200, S_kv=450, scale=0.09, sparse_mode=4,
+                           pre_tokens=30, next_tokens=200),
+    "bnsd_rect_nomask_sq_gt_skv": dict(layout="BNSD", B=1, N=2, D=64, S_q=390, S_kv=130, scale=0.125, sparse_mode=0),
+    "bnsd_empty_rows": dict(layout="BNSD", B=1, N=2, D=64, S_q=260, S_kv=260, scale=0.125, sparse_mode=4,
+                            pre_tokens=-3, next_tokens=10),
+    "bnsd_wide_band": dict(layout="BNSD", B=1, N=2, D=128, S_q=256, S_kv=256, scale=0.09, sparse_mode=4,
+                           pre_tokens=2147483647, next_tokens=2147483647),
+    "bnsd_zero_band": dict(layout="BNSD", B=1, N=2, D=64, S_q=200, S_kv=200, scale=0.125, sparse_mode=4,
+                           pre_tokens=0, next_tokens=0),
+    "tnd_varlen_nomask": dict(layout="TND", B=5, N=2, D=128, cu_seqlens_q=[130, 130, 387, 388, 452],
+                              cu_seqlens_kv=[130, 130, 387, 388, 452], scale=0.09, sparse_mode=0),
+    "tnd_varlen_band_dropout_d64": dict(layout="TND", B=4, N=3, D=64, cu_seqlens_q=[200, 201, 460, 0],
+                                        cu_seqlens_kv=[200, 201, 460, 0], scale=0.125, sparse_mode=4,
+                                        pre_tokens=100, next_tokens=17, keep_prob=0.85),
+    "tnd_rect": dict(layout="TND", B=3, N=2, D=128, cu_seqlens_q=[50, 300, 310], cu_seqlens_kv=[170, 180, 420],
+                     scale=0.09, sparse_mode=4, pre_tokens=64, next_tokens=64),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_parity(name):
+    geom = Geometry(**SMALL[name])
+    inp = draw(geom, 5000 + sum(map(ord, name)))
+    pr = to_problem(geom)
+    out, smax, ssum = orc.forward(pr, inp.q, inp.k, inp.v, inp.drop_mask)
+    dq, dk, dv = orc.backward(pr, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask)
+    res = as_np(run_gpu(inp))
+    check_forward(res, out, smax, ssum, name)
+    check_grads(res, dq, dk, dv, name)
+
+
+def test_workload_small_config_full_parity():
+    inp = draw_workload("bnsd_1x2x256x64_nomask")
+    pr = to_problem(inp.geom)
+    out, smax, ssum = orc.forward(pr, inp.q, inp.k, inp.v)
+    dq, dk, dv = orc.backward(pr, inp.q, inp.k, inp.v, inp.dy)
+    res = as_np(run_gpu(inp))
+    check_forward(res, out, smax, ssum)
+    check_grads(res, dq, dk, dv)
+
+
+def test_repeat_calls_are_deterministic_forward():
+    geom = Geometry(**SMALL["bnsd_band_d128_ragged"])
+    inp = draw(geom, 77)
+    a = as_np(run_gpu(inp, backward=False))
+    b = as_np(run_gpu(inp, backward=False))
+    for k_ in a:
+        assert np.array_equal(a[k_], b[k_])
+
+
+# ------------------------------------------------------ masked set, exact --
+def _mask_probe(geom, which):
+    """Inputs whose statistics expose the visible key range exactly.
+    which = 'count': q = 0 -> softmax_sum_i = |V_i|.
+    which = 'hi' / 'lo': s_ij = +j / -j -> softmax_max_i = max / -min visible j."""
+    g = Geometry(**{**geom.as_dict(), "scale": 1.0, "keep_prob": 1.0})
+    inp = draw(g, 9)
+    q = torch.zeros_like(inp.q)
+    k = torch.zeros_like(inp.k)
+    if which != "count":
+        sign = 1.0 if which == "hi" else -1.0
+        q[..., 0] = sign
+        q[..., 1] = sign * 256.0
+        if g.layout == "BNSD":
+            j = torch.arange(g.S_kv)
+            k[..., 0] = (j % 256).float().to(torch.bfloat16)
+            k[..., 1] = (j // 256).float().to(torch.bfloat16)
+        else:
+            start = 0
+            for (lq, lk) in g.seq_lens():
+                j = torch.arange(lk)
+                k[start:start + lk, :, 0] = (j % 256).float()[:, None].to(torch.bfloat16)
+                k[start:start + lk, :, 1] = (j // 256).float()[:, None].to(torch.bfloat16)
+                start += lk
+    inp.q, inp.k = q, k
+    return g, inp
+
+
+MASKSETS = {
+    "band": dict(layout="BNSD", B=1, N=2, D=64, S_q=1000, S_kv=1000, sparse_mode=4, pre_tokens=300,
+                 next_tokens=5),
+    "band_negative_pre": dict(layout="BNSD", B=1, N=1, D=128, S_q=700, S_kv=700, sparse_mode=4, pre_tokens=-40,
+                              next_tokens=300),
+    "rect_band": dict(layout="BNSD", B=2, N=1, D=64, S_q=300, S_kv=900, sparse_mode=4, pre_tokens=10,
+                      next_tokens=500),
+    "long_band_4096": dict(layout="BNSD", B=1, N=1, D=128, S_q=32768, S_kv=32768, sparse_mode=4, pre_tokens=4096,
+                           next_tokens=0),
+    "tnd_band": dict(layout="TND", B=3, N=2, D=64, cu_seqlens_q=[300, 300, 1000], cu_seqlens_kv=[250, 260, 1100],
+                     sparse_mode=4, pre_tokens=129, next_tokens=255),
+    "nomask": dict(layout="BNSD", B=1, N=1, D=64, S_q=333, S_kv=555, sparse_mode=0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MASKSETS))
+def test_masked_set_exact(name):
+    geom = Geometry(**MASKSETS[name])
+    pr = to_problem(geom)
+    rows = np.arange(np.prod(geom.stat_shape()))
+    lo, hi = orc.key_ranges(pr, rows)
+    empty = lo > hi
+    g, inp = _mask_probe(geom, "count")
+    res = as_np(run_gpu(inp, backward=False))
+    count = res["ssum"].reshape(-1)
+    assert np.array_equal(count, np.where(empty, 0, hi - lo + 1).astype(np.float64))
+    for which, ref in (("hi", hi), ("lo", -lo)):
+        g, inp = _mask_probe(geom, which)
+        res = as_np(run_gpu(inp, backward=False))
+        m = res["smax"].reshape(-1)
+        assert np.all(np.isneginf(m[empty]))
+        got = m[~empty]
+        assert np.all(np.abs(got - ref[~empty]) < 0.25), which
+        assert np.array_equal(np.rint(got), ref[~empty].astype(np.float64)), which
+
+
+# ------------------------------------------------- full-size workloads -----
+def _sample_rows(geom, rng, n_random):
+    """Query-row ids (statistics index) at tile edges, band edges and random."""
+    total = int(np.prod(geom.stat_shape()))
+    picks = set(rng.integers(0, total, size=n_random).tolist())
+    if geom.layout == "BNSD":
+        S = geom.S_q
+        for bh in (0, geom.B * geom.N - 1):
+            for i in (0, 1, 127, 128, 129, S // 2, S - 129, S - 128, S - 1, min(S - 1, 4095), min(S - 1, 4096),
+                      min(S - 1, 4097)):
+                picks.add(bh * S + i)
+    else:
+        start = 0
+        for (lq, _) in geom.seq_lens():
+            for i in (0, 127, 128, lq - 1):
+                if 0 <= i < lq:
+                    picks.add((start + i) * geom.N + (i % geom.N))
+            start += lq
+    return np.array(sorted(p for p in picks if p < total), dtype=np.int64)
+
+
+def _sample_cols(geom, rng, n_random):
+    if geom.layout == "BNSD":
+        total = geom.B * geom.N * geom.S_kv
+        S = geom.S_kv
+        picks = {0, 127, 128, S - 1, total - 1, total - S, (geom.B * geom.N // 2) * S + S // 2}
+    else:
+        total = geom.T_kv * geom.N
+        picks = {0, total - 1}
+    picks |= set(rng.integers(0, total, size=n_random).tolist())
+    return np.array(sorted(picks), dtype=np.int64)
+
+
+def _invariants(geom, inp, res):
+    """Whole-tensor properties of the exact gradients (no dropout, no empty
+    rows), per head: sum_j dV_j = sum_i dY_i (rows of P sum to one) and
+    sum_j dK_j = 0 (rows of dS sum to zero)."""
+    if geom.keep_prob < 1.0:
+        return
+    if geom.layout == "BNSD":
+        heads = [((b, n), (b, n)) for b in range(geom.B) for n in range(geom.N)]
+        get_q = lambda t, h: t[h[0], h[1]]
+        get_k = get_q
+    else:
+        heads, qs, ks = [], 0, 0
+        for (lq, lk) in geom.seq_lens():
+            if lq and lk:
+                heads += [((qs, lq, n), (ks, lk, n)) for n in range(geom.N)]
+            qs += lq
+            ks += lk
+        get_q = lambda t, h: t[h[0]:h[0] + h[1], h[2]]
+        get_k = get_q
+    for hq, hk in heads:
+        s_dy = get_q(inp.dy, hq).double().sum(0).numpy()
+        s_dv = get_k(res["dv"], hk).double().sum(0).numpy()
+        assert np.linalg.norm(s_dv - s_dy) <= 1e-3 * np.linalg.norm(s_dy) + 0.05, "dV mass"
+        dkh = get_k(res["dk"], hk).double()
+        s_dk = dkh.sum(0).numpy()
+        walk = float(torch.sqrt((dkh ** 2).sum()))  # size of a sum of unrelated rows
+        assert np.linalg.norm(s_dk) <= 0.05 * walk + 1e-3, "dK rows of dS sum to zero"
+
+
+def _rows_f64(t, ids, D):
+    return t.reshape(-1, D)[torch.as_tensor(ids)].double().numpy()
+
+
+@pytest.mark.parametrize("name", [n for n in WORKLOADS if n != "bnsd_1x2x256x64_nomask"])
+def test_workload_full_size_sampled(name):
+    inp = draw_workload(name)
+    geom = inp.geom
+    pr = to_problem(geom)
+    res = run_gpu(inp)
+    for key in ("out", "dq", "dk", "dv", "smax", "ssum"):
+        assert not torch.isnan(res[key]).any(), key
+    # statistics bounds on every row: 1 <= softmax_sum <= |V_i|
+    rows_all = np.arange(int(np.prod(geom.stat_shape())))
+    lo, hi = orc.key_ranges(pr, rows_all)
+    ssum = res["ssum"].double().numpy().reshape(-1)
+    ne = lo <= hi
+    assert np.all(ssum[ne] >= 1.0 - 1e-4) and np.all(ssum[ne] <= (hi - lo + 1)[ne] * (1 + 1e-4))
+    _invariants(geom, inp, res)
+    rng = np.random.default_rng(sum(map(ord, name)))
+    D = geom.D
+    rows = _sample_rows(geom, rng, 24)
+    o, m, l = orc.forward_rows(pr, inp.q, inp.k, inp.v, inp.drop_mask, rows)
+    got_o = _rows_f64(res["out"], rows, D)
+    assert rel_l2(got_o, o) <= TOL_OUT and excess(got_o, o) <= 0.0
+    assert stat_rel(res["smax"].double().numpy().reshape(-1)[rows], m) <= TOL_STAT
+    assert stat_rel(ssum[rows], l) <= TOL_STAT
+    qrows = rows[:: max(1, len(rows) // 16)]
+    dq = orc.backward_dq_rows(pr, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask, qrows)
+    got = _rows_f64(res["dq"], qrows, D)
+    assert rel_l2(got, dq) <= TOL_GRAD and excess(got, dq) <= 0.0
+    cols = _sample_cols(geom, rng, 2 if geom.layout == "TND" else 6)
+    if geom.layout == "TND":
+        cols = cols[:4]
+    dk, dv = orc.backward_dkv_cols(pr, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask, cols)
+    got_k = _rows_f64(res["dk"], cols, D)
+    got_v = _rows_f64(res["dv"], cols, D)
+    assert rel_l2(got_k, dk) <= TOL_GRAD and excess(got_k, dk) <= 0.0
+    assert rel_l2(got_v, dv) <= TOL_GRAD and excess(got_v, dv) <= 0.0
