@@ -321,6 +321,17 @@ swa_status_t cuda_fail(cudaError_t e, const char* what) {
 
 }  // namespace
 
+// Error text for entry points defined in other translation units.
+swa_status_t swa::set_error(swa_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
 // ------------------------------------------------------------------ ABI --
 extern "C" {
 

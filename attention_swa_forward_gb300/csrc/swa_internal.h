@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "swa.h"
+
 namespace swa {
 
 constexpr int kTileM = 128;  // query rows per tile (tcgen05 M)
@@ -108,6 +110,9 @@ struct PrepArgs {
   float* dsum;
   float* dq_acc;
 };
+
+// Record `fmt` as the text of swa_last_error() on this thread; returns st.
+swa_status_t set_error(swa_status_t st, const char* fmt, ...);
 
 // Kernel launchers (defined in the .cu files).  Each returns the launch's
 // cudaError_t.

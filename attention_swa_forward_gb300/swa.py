@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
             L.swa_forward.restype = st
             L.swa_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
             L.swa_backward.restype = st
+            L.swa_backward_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+            L.swa_backward_noalloc.restype = st
             L.swa_workspace_status.argtypes = [vp, vp]
             L.swa_workspace_status.restype = st
             L.swa_set_timing_events.argtypes = [vp, vp, vp, vp]
@@ -90,7 +92,8 @@ def lib() -> ctypes.CDLL:
 
 def exported_symbols():
     return ["swa_params_default", "swa_forward_workspace_size", "swa_forward", "swa_backward_workspace_size",
-            "swa_backward", "swa_workspace_status", "swa_set_timing_events", "swa_last_error"]
+            "swa_backward", "swa_backward_noalloc", "swa_workspace_status", "swa_set_timing_events",
+            "swa_last_error"]
 
 
 def _check(status: int):
@@ -152,6 +155,13 @@ def swa_backward(params: Params, q, k, v, dy, out, softmax_max, softmax_sum, dro
                  workspace_bytes, stream) -> int:
     return lib().swa_backward(params.ref(), q, k, v, dy, out, softmax_max, softmax_sum, drop_mask, dq, dk, dv,
                               workspace, workspace_bytes, stream)
+
+
+def swa_backward_noalloc(params: Params, q, k, v, dy, out, softmax_max, softmax_sum, drop_mask, dq, dk, dv,
+                         stream) -> int:
+    """Raw call of the no-allocation backward (scratch compiled into the library)."""
+    return lib().swa_backward_noalloc(params.ref(), q, k, v, dy, out, softmax_max, softmax_sum, drop_mask, dq, dk,
+                                      dv, stream)
 
 
 def swa_workspace_status(workspace, stream) -> int:

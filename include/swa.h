@@ -135,6 +135,30 @@ SWA_API swa_status_t swa_backward(const swa_params_t *p, const void *q, const vo
                           const uint8_t *drop_mask, void *dq, void *dk, void *dv, void *workspace,
                           size_t workspace_bytes, swa_stream_t stream);
 
+/* swa_backward without a workspace argument, for callers that cannot hand the
+ * library device memory (the pages have no counterpart; this is an addition of
+ * this library).  Example callers: a plugin inside a framework that owns all
+ * device memory through its own pool and forbids extra cudaMalloc calls, or a
+ * latency-critical loop that must not allocate after start-up.
+ *
+ * Arguments and results are those of swa_backward.  The scratch it needs
+ * (status word, per-row D and log2-sum-exp, fp32 dQ accumulator) lives in a
+ * fixed 64 MiB device array compiled into the library: every GPU that loads
+ * the library keeps it until the process exits.  A problem needing more than
+ * 64 MiB of scratch (swa_backward_workspace_size) is rejected with
+ * SWA_ERR_WORKSPACE.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  All calls on a device share the array and
+ * each call clears what must start at zero, so calls whose kernels overlap on
+ * the GPU (concurrent streams, other threads) race and must be serialised by
+ * the caller.  Allocates nothing: no cudaMalloc, cudaFree or allocating
+ * library routine.  The status word of a bounded wait that gave up is not
+ * observable through this entry point. */
+SWA_API swa_status_t swa_backward_noalloc(const swa_params_t *p, const void *q, const void *k, const void *v,
+                                          const void *dy, const void *out, const float *softmax_max,
+                                          const float *softmax_sum, const uint8_t *drop_mask, void *dq, void *dk,
+                                          void *dv, swa_stream_t stream);
+
 /* Wait for `stream`, then report whether any kernel of the last call that
  * used `workspace` gave up a bounded wait: SWA_OK or SWA_ERR_TIMEOUT
  * (SWA_ERR_CUDA if the stream itself failed). */
