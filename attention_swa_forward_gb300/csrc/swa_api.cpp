@@ -272,26 +272,29 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 128 rows x 64 columns per box, 128-byte swizzle.  BNSD: (d, s, n, b);
 // TND: (d, n, t, 1).
-swa_status_t make_map(CUtensorMap* m, const void* ptr, const Plan& plan, bool q_side, const char* name) {
+swa_status_t make_map(CUtensorMap* m, const void* ptr, const Plan& plan, bool q_side, const char* name,
+                      bool fp32 = false) {
   auto fn = encode_fn();
   if (!fn) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const Geometry& g = plan.g;
   const cuuint64_t D = g.D, N = g.N;
+  const cuuint64_t es_bytes = fp32 ? 4 : 2;
+  const cuuint32_t box_x = fp32 ? 32 : 64;  // 128 bytes, one swizzle row
   cuuint64_t dims[4], strides[3];
   cuuint32_t box[4];
   const cuuint32_t es[4] = {1, 1, 1, 1};
   if (g.layout == 0) {
     const cuuint64_t S = q_side ? g.S_q : g.S_kv;
     dims[0] = D; dims[1] = S; dims[2] = N; dims[3] = static_cast<cuuint64_t>(plan.B);
-    strides[0] = D * 2; strides[1] = S * D * 2; strides[2] = N * S * D * 2;
-    box[0] = 64; box[1] = kTileM; box[2] = 1; box[3] = 1;
+    strides[0] = D * es_bytes; strides[1] = S * D * es_bytes; strides[2] = N * S * D * es_bytes;
+    box[0] = box_x; box[1] = kTileM; box[2] = 1; box[3] = 1;
   } else {
     const cuuint64_t T = static_cast<cuuint64_t>(q_side ? plan.q_rows : plan.kv_rows);
     dims[0] = D; dims[1] = N; dims[2] = T; dims[3] = 1;
-    strides[0] = D * 2; strides[1] = N * D * 2; strides[2] = T * N * D * 2;
-    box[0] = 64; box[1] = 1; box[2] = kTileM; box[3] = 1;
+    strides[0] = D * es_bytes; strides[1] = N * D * es_bytes; strides[2] = T * N * D * es_bytes;
+    box[0] = box_x; box[1] = 1; box[2] = kTileM; box[3] = 1;
   }
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+  CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
@@ -437,6 +440,8 @@ swa_status_t swa_backward(const swa_params_t* p, const void* q, const void* k, c
   float* lse2 = reinterpret_cast<float*>(ws + lay.lse2);
   float* dsum = reinterpret_cast<float*>(ws + lay.dsum);
   float* dq_acc = reinterpret_cast<float*>(ws + lay.dq_acc);
+  CUtensorMap mdq;
+  if ((st = make_map(&mdq, dq_acc, plan, true, "dq accumulator", true)) != SWA_OK) return st;
   const int64_t rows = plan.q_rows * plan.g.N;
 
   PrepArgs pa{};
@@ -466,8 +471,8 @@ swa_status_t swa_backward(const swa_params_t* p, const void* q, const void* k, c
   const std::vector<SeqDesc> descs = build_descs(plan, false);
   if (t_ev[2]) cudaEventRecord(t_ev[2], s);
   e = run_tables(
-      descs, [&](const SeqTable<kSmallTable>& t) { return launch_backward(a, t, mq, mk, mv, mdy, s); },
-      [&](const SeqTable<kLargeTable>& t) { return launch_backward(a, t, mq, mk, mv, mdy, s); });
+      descs, [&](const SeqTable<kSmallTable>& t) { return launch_backward(a, t, mq, mk, mv, mdy, mdq, s); },
+      [&](const SeqTable<kLargeTable>& t) { return launch_backward(a, t, mq, mk, mv, mdy, mdq, s); });
   if (t_ev[3]) cudaEventRecord(t_ev[3], s);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   // Key rows that no work item covers (skipped batches, length-0 sequences)

@@ -168,36 +168,57 @@ __global__ void __launch_bounds__(192, 1)
     bool ok = true;
     for (int it = 0; it < n_kv; ++it) {
       const int sb = it & 1;
-      if (!mbar_wait(&s.s_full[sb], (it >> 1) & 1, a.err, kErrFwdSoftmax)) { ok = false; break; }
+      // warp-uniform outcome: the tcgen05.ld below is warp-collective
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&s.s_full[sb], (it >> 1) & 1, a.err, kErrFwdSoftmax))) {
+        ok = false;
+        break;
+      }
       tc_fence_after_sync();
       float x[kTileN];
+      {
+        // all four loads in flight before the one wait
+        uint32_t t0[32], t1[32], t2[32], t3[32];
+        const uint32_t base = tmem + lane_off + sb * kTileN;
+        tmem_ld_32x32b_x32(base + 0, t0);
+        tmem_ld_32x32b_x32(base + 32, t1);
+        tmem_ld_32x32b_x32(base + 64, t2);
+        tmem_ld_32x32b_x32(base + 96, t3);
+        tmem_ld_wait(t0);
+        tmem_ld_wait(t1);
+        tmem_ld_wait(t2);
+        tmem_ld_wait(t3);
 #pragma unroll
-      for (int ch = 0; ch < kTileN / 32; ++ch) {
-        uint32_t t32[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + sb * kTileN + ch * 32, t32);
-        tmem_ld_wait(t32);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) x[ch * 32 + t] = __uint_as_float(t32[t]);
+        for (int t = 0; t < 32; ++t) {
+          x[t] = __uint_as_float(t0[t]);
+          x[32 + t] = __uint_as_float(t1[t]);
+          x[64 + t] = __uint_as_float(t2[t]);
+          x[96 + t] = __uint_as_float(t3[t]);
+        }
       }
       tc_fence_before_sync();
       mbar_arrive(&s.s_free[sb]);
 
       const int j0 = (kv_t0 + it) * kTileN;
-      float mx = -INFINITY;
+      // eight independent partial maxima: no 128-long dependency chain
+      float m8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) m8[u] = -INFINITY;
       if (tile_fully_visible(g, sq, q0, j0)) {
 #pragma unroll
         for (int t = 0; t < kTileN; ++t) {
           x[t] *= c;
-          mx = fmaxf(mx, x[t]);
+          m8[t & 7] = fmaxf(m8[t & 7], x[t]);
         }
       } else {
 #pragma unroll
         for (int t = 0; t < kTileN; ++t) {
           const int j = j0 + t;
           x[t] = (j >= wlo && j <= whi) ? x[t] * c : -INFINITY;
-          mx = fmaxf(mx, x[t]);
+          m8[t & 7] = fmaxf(m8[t & 7], x[t]);
         }
       }
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       const float m_new = fmaxf(m_true, mx);
       m_true = m_new;
       const bool need = m_new > m_use + kRescaleThreshold;
@@ -208,12 +229,15 @@ __global__ void __launch_bounds__(192, 1)
         m_use = m_new;
       }
       const float msub = (m_use == -INFINITY) ? 0.f : m_use;
-      float rs = 0.f;
+      float r8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) r8[u] = 0.f;
 #pragma unroll
       for (int t = 0; t < kTileN; ++t) {
         x[t] = ex2_approx(x[t] - msub);
-        rs += x[t];
+        r8[t & 7] += x[t];
       }
+      const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
       l = l * alpha + rs;
       if (DROP) {
         uint32_t bits[4] = {0u, 0u, 0u, 0u};
@@ -224,7 +248,10 @@ __global__ void __launch_bounds__(192, 1)
       }
       // The previous P V must be done before P is overwritten or O rescaled.
       if (it >= 1) {
-        if (!mbar_wait(&s.o_done, (it - 1) & 1, a.err, kErrFwdSoftmax)) { ok = false; break; }
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&s.o_done, (it - 1) & 1, a.err, kErrFwdSoftmax))) {
+          ok = false;
+          break;
+        }
         tc_fence_after_sync();
         if (warp_need) {
 #pragma unroll
@@ -247,7 +274,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_arrive(&s.p_full);
     }
     if (ok && n_kv > 0) {
-      ok = mbar_wait(&s.o_done, (n_kv - 1) & 1, a.err, kErrFwdSoftmax);
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s.o_done, (n_kv - 1) & 1, a.err, kErrFwdSoftmax));
       tc_fence_after_sync();
     }
     if (ok) {
