@@ -25,7 +25,7 @@ using namespace swa;
 namespace {
 
 thread_local std::string t_last_error = "no error";
-thread_local cudaEvent_t t_ev[4] = {nullptr, nullptr, nullptr, nullptr};  // fwd start/stop, bwd start/stop
+thread_local cudaEvent_t t_ev[6] = {};  // start/stop around: forward, dK/dV pass, dQ pass
 
 swa_status_t fail(swa_status_t st, const char* fmt, ...) {
   char buf[512];
@@ -272,14 +272,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 128 rows x 64 columns per box, 128-byte swizzle.  BNSD: (d, s, n, b);
 // TND: (d, n, t, 1).
-swa_status_t make_map(CUtensorMap* m, const void* ptr, const Plan& plan, bool q_side, const char* name,
-                      bool fp32 = false) {
+swa_status_t make_map(CUtensorMap* m, const void* ptr, const Plan& plan, bool q_side, const char* name) {
   auto fn = encode_fn();
   if (!fn) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const Geometry& g = plan.g;
   const cuuint64_t D = g.D, N = g.N;
-  const cuuint64_t es_bytes = fp32 ? 4 : 2;
-  const cuuint32_t box_x = fp32 ? 32 : 64;  // 128 bytes, one swizzle row
+  const cuuint64_t es_bytes = 2;
+  const cuuint32_t box_x = 64;  // 128 bytes, one swizzle row
   cuuint64_t dims[4], strides[3];
   cuuint32_t box[4];
   const cuuint32_t es[4] = {1, 1, 1, 1};
@@ -294,7 +293,7 @@ swa_status_t make_map(CUtensorMap* m, const void* ptr, const Plan& plan, bool q_
     strides[0] = D * es_bytes; strides[1] = N * D * es_bytes; strides[2] = T * N * D * es_bytes;
     box[0] = box_x; box[1] = 1; box[2] = kTileM; box[3] = 1;
   }
-  CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
@@ -306,15 +305,14 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct BwdLayout {
-  size_t lse2, dsum, dq_acc, total;
+  size_t lse2, dsum, total;
 };
 BwdLayout bwd_layout(const Plan& plan) {
   const size_t rows = static_cast<size_t>(plan.q_rows) * plan.g.N;
   BwdLayout l;
   l.lse2 = kHeaderBytes;
   l.dsum = l.lse2 + round256(rows * 4);
-  l.dq_acc = l.dsum + round256(rows * 4);
-  l.total = l.dq_acc + round256(rows * plan.g.D * 4);
+  l.total = l.dsum + round256(rows * 4);
   return l;
 }
 
@@ -439,9 +437,6 @@ swa_status_t swa_backward(const swa_params_t* p, const void* q, const void* k, c
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* lse2 = reinterpret_cast<float*>(ws + lay.lse2);
   float* dsum = reinterpret_cast<float*>(ws + lay.dsum);
-  float* dq_acc = reinterpret_cast<float*>(ws + lay.dq_acc);
-  CUtensorMap mdq;
-  if ((st = make_map(&mdq, dq_acc, plan, true, "dq accumulator", true)) != SWA_OK) return st;
   const int64_t rows = plan.q_rows * plan.g.N;
 
   PrepArgs pa{};
@@ -454,7 +449,6 @@ swa_status_t swa_backward(const swa_params_t* p, const void* q, const void* k, c
   pa.ssum = softmax_sum;
   pa.lse2 = lse2;
   pa.dsum = dsum;
-  pa.dq_acc = dq_acc;
   cudaError_t e = launch_prep(pa, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
 
@@ -464,21 +458,26 @@ swa_status_t swa_backward(const swa_params_t* p, const void* q, const void* k, c
   a.mask = drop_mask;
   a.lse2 = lse2;
   a.dsum = dsum;
-  a.dq_acc = dq_acc;
+  a.dq = static_cast<__nv_bfloat16*>(dq);
   a.dk = static_cast<__nv_bfloat16*>(dk);
   a.dv = static_cast<__nv_bfloat16*>(dv);
   a.err = reinterpret_cast<int32_t*>(ws);
-  const std::vector<SeqDesc> descs = build_descs(plan, false);
+  // key-major pass: dK, dV (one work item per key tile)
+  const std::vector<SeqDesc> kv_descs = build_descs(plan, false);
   if (t_ev[2]) cudaEventRecord(t_ev[2], s);
   e = run_tables(
-      descs, [&](const SeqTable<kSmallTable>& t) { return launch_backward(a, t, mq, mk, mv, mdy, mdq, s); },
-      [&](const SeqTable<kLargeTable>& t) { return launch_backward(a, t, mq, mk, mv, mdy, mdq, s); });
+      kv_descs, [&](const SeqTable<kSmallTable>& t) { return launch_backward_dkv(a, t, mq, mk, mv, mdy, s); },
+      [&](const SeqTable<kLargeTable>& t) { return launch_backward_dkv(a, t, mq, mk, mv, mdy, s); });
   if (t_ev[3]) cudaEventRecord(t_ev[3], s);
-  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
-  // Key rows that no work item covers (skipped batches, length-0 sequences)
-  // hold no data, so nothing else of dk / dv needs writing.
-  e = launch_dq_convert(dq_acc, static_cast<__nv_bfloat16*>(dq), rows * plan.g.D, plan.g.scale, s);
-  if (e != cudaSuccess) return cuda_fail(e, "dQ convert launch");
+  if (e != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
+  // query-major pass: dQ (one work item per query tile)
+  const std::vector<SeqDesc> q_descs = build_descs(plan, true);
+  if (t_ev[4]) cudaEventRecord(t_ev[4], s);
+  e = run_tables(
+      q_descs, [&](const SeqTable<kSmallTable>& t) { return launch_backward_dq(a, t, mq, mk, mv, mdy, s); },
+      [&](const SeqTable<kLargeTable>& t) { return launch_backward_dq(a, t, mq, mk, mv, mdy, s); });
+  if (t_ev[5]) cudaEventRecord(t_ev[5], s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward dQ launch");
   return SWA_OK;
 }
 
@@ -494,11 +493,8 @@ swa_status_t swa_workspace_status(const void* workspace, swa_stream_t stream) {
   return SWA_OK;
 }
 
-void swa_set_timing_events(void* fwd_start, void* fwd_stop, void* bwd_start, void* bwd_stop) {
-  t_ev[0] = static_cast<cudaEvent_t>(fwd_start);
-  t_ev[1] = static_cast<cudaEvent_t>(fwd_stop);
-  t_ev[2] = static_cast<cudaEvent_t>(bwd_start);
-  t_ev[3] = static_cast<cudaEvent_t>(bwd_stop);
+void swa_set_timing_events(void* const* events) {
+  for (int i = 0; i < 6; ++i) t_ev[i] = events ? static_cast<cudaEvent_t>(events[i]) : nullptr;
 }
 
 const char* swa_last_error(void) { return t_last_error.c_str(); }

@@ -1,9 +1,8 @@
-// swa_aux.cu — the two memory-bound passes around the backward kernel.
+// swa_aux.cu — the memory-bound pass before the backward kernels.
 //
 //  * preprocess: per query row, D = rowsum(dY * O) (PyPTO-Gym article,
-//    "反向公式"), lse2 = softmax_max*log2(e) + log2(softmax_sum) (+inf for an
-//    empty row, so that recomputed P is 0), and zero the fp32 dQ accumulator.
-//  * dQ convert: dQ = scale * dQ_acc rounded to bf16.
+//    "反向公式") and lse2 = softmax_max*log2(e) + log2(softmax_sum) (+inf for
+//    an empty row, so that the recomputed P is 0).
 //
 // Both layouts address a query row (b, n, i) / (t, n) the same way once
 // flattened: row id r -> elements [r*D, r*D + D), statistics index r.
@@ -47,28 +46,10 @@ __global__ void __launch_bounds__(256) swa_prep_kernel(const PrepArgs a) {
   }
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, m);
-  // zero this row of the dQ accumulator: D floats = D/4 float4
-  if (lane < D / 4) reinterpret_cast<float4*>(a.dq_acc + row * D)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (lane == 0) {
     const float l = a.ssum[row];
     a.dsum[row] = acc;
     a.lse2[row] = (l > 0.f) ? a.smax[row] * kLog2e + __log2f(l) : INFINITY;
-  }
-}
-
-// 8 elements per thread: two float4 loads, one 16-byte store.
-__global__ void __launch_bounds__(256) swa_dq_convert_kernel(const float* __restrict__ acc,
-                                                             __nv_bfloat16* __restrict__ dq, int64_t n8, float scale) {
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const float4 a0 = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i);
-    const float4 a1 = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
-    uint4 v;
-    v.x = pack_bf16x2(a0.x * scale, a0.y * scale);
-    v.y = pack_bf16x2(a0.z * scale, a0.w * scale);
-    v.z = pack_bf16x2(a1.x * scale, a1.y * scale);
-    v.w = pack_bf16x2(a1.z * scale, a1.w * scale);
-    reinterpret_cast<uint4*>(dq)[i] = v;
   }
 }
 
@@ -83,21 +64,6 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream) {
     swa_prep_kernel<64><<<static_cast<unsigned>(grid), block, 0, stream>>>(a);
   else
     swa_prep_kernel<128><<<static_cast<unsigned>(grid), block, 0, stream>>>(a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int64_t n_elems, float scale,
-                              cudaStream_t stream) {
-  if (n_elems == 0) return cudaSuccess;
-  const int64_t n8 = n_elems / 8;
-  int dev = 0, sms = 152;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int block = 256;
-  int64_t grid = (n8 + block - 1) / block;
-  const int64_t cap = static_cast<int64_t>(sms) * 8;
-  if (grid > cap) grid = cap;
-  swa_dq_convert_kernel<<<static_cast<unsigned>(grid), block, 0, stream>>>(dq_acc, dq, n8, scale);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,354 @@
+// swa_bwd_dq.cu — sliding-window attention backward, query-major pass: dQ.
+//
+// Per (query tile i, key tile j) pair inside the BAND (PyPTO-Gym article,
+// "反向公式", the dQ row of the formulas):
+//   S  = Q K^T,  P = exp2(S*scale*log2e - lse2),  dP = dY V^T,
+//   dS = P * (dP * z/keep - D),  dQ += dS K,  dQ = scale * dQ at the end.
+// dQ accumulates in TMEM over the key tiles of the band and is written once:
+// no accumulation through global memory (the measured fp32 reduce-add ceiling
+// of the L2 would otherwise bound the backward), and the result is
+// deterministic.
+//
+// One CTA = one 128-row query tile of one (batch, head).  Warps:
+//   warps 0-7  compute: warp w owns TMEM lanes 32*(w%4).. (query rows) and key
+//              columns 64*(w/4).. of each tile; in the epilogue, dQ columns
+//              [w/4 * D/2, +D/2)
+//   warp  8    TMA producer: Q, dY once; K, V through a 2-stage ring
+//   warp  9    tcgen05 issuer
+// TMEM columns: two S/dP buffers [0,128) and [128,256) (S is read into
+// registers, then dP is written over it), dQ [256,256+D), and two bf16 dS
+// buffers [384,448), [448,512) that the dQ MMA reads as its A operand.
+// Issue order per key tile j: dP(j) (once S(j) is in registers), S(j+1) into
+// the other buffer, dQ(j) (once dS(j) is in TMEM).
+#include "swa_device.cuh"
+
+namespace swa {
+namespace {
+
+template <int D>
+struct DqSmem {
+  static constexpr int kTileBytes = kTileM * D * 2;
+  alignas(1024) uint8_t q[kTileBytes];
+  alignas(1024) uint8_t dy[kTileBytes];
+  alignas(1024) uint8_t k[2][kTileBytes];
+  alignas(1024) uint8_t v[2][kTileBytes];
+  uint64_t qdy_full, k_full[2], v_full[2], kv_empty[2];
+  uint64_t s_full[2], s_loaded[2], dp_full[2], dp_loaded[2], ds_full[2], ds_free[2], mma_drain;
+  uint32_t tmem_base;
+};
+static_assert(sizeof(DqSmem<128>) + 1024 <= 232448, "shared memory budget");
+
+constexpr int kThreads = 320;
+constexpr int kComputeThreads = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColDQ = 256, kColDS = 384;  // dS buffer b at kColDS + 64*b
+constexpr uint32_t kBarVote = 1;
+
+__device__ __forceinline__ bool compute_wait(uint64_t* bar, uint32_t parity, int* err) {
+  return named_barrier_and(kBarVote, kComputeThreads, mbar_wait(bar, parity, err, kErrBwdCompute));
+}
+
+template <int D, bool DROP, int CAP>
+__global__ void __launch_bounds__(kThreads, 1)
+    swa_bwd_dq_kernel(const BwdArgs a, const __grid_constant__ SeqTable<CAP> tab, const __grid_constant__ CUtensorMap mq,
+                      const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                      const __grid_constant__ CUtensorMap mdy) {
+  extern __shared__ uint8_t smem_raw[];
+  DqSmem<D>& s = *reinterpret_cast<DqSmem<D>*>(align1024(smem_raw));
+  constexpr int kTileBytes = DqSmem<D>::kTileBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Geometry& g = a.g;
+  const Item w = resolve_item(tab, a.g, static_cast<int>(blockIdx.x));
+  const SeqInfo sq = w.s;
+  const int q0 = w.tile * kTileM;
+  const int q_last = min(q0 + kTileM - 1, sq.q_len - 1);
+
+  // key tiles touched by this query tile
+  int lo = 0, hi = sq.kv_len - 1;
+  if (g.sparse_mode == 4) {
+    lo = max(lo, q0 - g.pre);
+    hi = min(hi, q_last + g.next);
+  }
+  int kv_t0 = 0, n_kv = 0;
+  if (lo <= hi) {
+    kv_t0 = lo / kTileN;
+    n_kv = hi / kTileN - kv_t0 + 1;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&s.qdy_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s.k_full[b], 1);
+      mbar_init(&s.v_full[b], 1);
+      mbar_init(&s.kv_empty[b], 1);
+      mbar_init(&s.s_full[b], 1);
+      mbar_init(&s.s_loaded[b], kComputeThreads);
+      mbar_init(&s.dp_full[b], 1);
+      mbar_init(&s.dp_loaded[b], kComputeThreads);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s.ds_full[b], kComputeThreads);
+      mbar_init(&s.ds_free[b], 1);
+    }
+    mbar_init(&s.mma_drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&s.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = s.tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0 && n_kv > 0) {
+      tma_prefetch_desc(&mq);
+      tma_prefetch_desc(&mk);
+      tma_prefetch_desc(&mv);
+      tma_prefetch_desc(&mdy);
+      mbar_arrive_expect_tx(&s.qdy_full, 2 * kTileBytes);
+      tma_rows<D>(s.q, &mq, &s.qdy_full, g, w.b, w.n, sq.q_start, q0);
+      tma_rows<D>(s.dy, &mdy, &s.qdy_full, g, w.b, w.n, sq.q_start, q0);
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int b = j & 1;
+        if (j >= 2 && !mbar_wait(&s.kv_empty[b], ((j >> 1) - 1) & 1, a.err, kErrBwdLoad)) break;
+        const int jr = (kv_t0 + j) * kTileN;
+        mbar_arrive_expect_tx(&s.k_full[b], kTileBytes);
+        tma_rows<D>(s.k[b], &mk, &s.k_full[b], g, w.b, w.n, sq.kv_start, jr);
+        mbar_arrive_expect_tx(&s.v_full[b], kTileBytes);
+        tma_rows<D>(s.v[b], &mv, &s.v_full[b], g, w.b, w.n, sq.kv_start, jr);
+        ++issued;
+      }
+      // every copy issued has landed before the CTA may exit
+      mbar_wait_drain(&s.qdy_full, 0);
+      for (int b = 0; b < 2; ++b) {
+        const int uses = (issued - b + 1) / 2;
+        if (uses > 0) {
+          mbar_wait_drain(&s.k_full[b], (uses - 1) & 1);
+          mbar_wait_drain(&s.v_full[b], (uses - 1) & 1);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ----------------------------------------------------- tcgen05 issuer --
+    if (lane == 0 && n_kv > 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(kTileM, kTileN, false, false);  // S, dP
+      constexpr uint32_t kIdQ = idesc_bf16_f32(kTileM, D, false, true);        // dQ
+      const uint32_t q_addr = smem_u32(s.q), dy_addr = smem_u32(s.dy);
+      auto issue_s = [&](int j) {  // S(j) = Q K_j^T into buffer j % 2
+        const int b = j & 1;
+        const uint32_t k_addr = smem_u32(s.k[b]);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
+          umma_bf16_ss(tmem + b * 128, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
+                       kIdS, kk > 0);
+        }
+        umma_commit(&s.s_full[b]);
+      };
+      bool ok = mbar_wait(&s.qdy_full, 0, a.err, kErrBwdMma) && mbar_wait(&s.k_full[0], 0, a.err, kErrBwdMma);
+      if (ok) {
+        tc_fence_after_sync();
+        issue_s(0);
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int b = j & 1;
+        const uint32_t u = (j >> 1) & 1;
+        if (!mbar_wait(&s.s_loaded[b], u, a.err, kErrBwdMma)) break;
+        if (!mbar_wait(&s.v_full[b], u, a.err, kErrBwdMma)) break;
+        tc_fence_after_sync();
+        const uint32_t v_addr = smem_u32(s.v[b]);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // dP(j) = dY V_j^T over the consumed S(j)
+          const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
+          umma_bf16_ss(tmem + b * 128, sdesc_sw128(dy_addr + off, 16, 1024), sdesc_sw128(v_addr + off, 16, 1024),
+                       kIdS, kk > 0);
+        }
+        umma_commit(&s.dp_full[b]);
+        if (j + 1 < n_kv) {  // S(j+1) into the other buffer, once its dP(j-1) was read
+          const int nb = (j + 1) & 1;
+          if (j + 1 >= 2 && !mbar_wait(&s.dp_loaded[nb], (((j + 1) >> 1) - 1) & 1, a.err, kErrBwdMma)) break;
+          if (!mbar_wait(&s.k_full[nb], ((j + 1) >> 1) & 1, a.err, kErrBwdMma)) break;
+          tc_fence_after_sync();
+          issue_s(j + 1);
+        }
+        if (!mbar_wait(&s.ds_full[b], u, a.err, kErrBwdMma)) break;
+        tc_fence_after_sync();
+        const uint32_t k_addr = smem_u32(s.k[b]);
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)  // dQ += dS(j) K_j  (A = dS in TMEM, K dim = keys)
+          umma_bf16_ts(tmem + kColDQ, tmem + kColDS + b * 64 + kk * 8,
+                       sdesc_sw128(k_addr + kk * 2048, kAtomBytes, 1024), kIdQ, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&s.ds_free[b]);
+        umma_commit(&s.kv_empty[b]);
+      }
+      umma_commit(&s.mma_drain);
+      mbar_wait_drain(&s.mma_drain, 0);
+    }
+  } else {
+    // ------------------------------------------- compute warps (0..7) -----
+    const int wq = warp & 3, h = warp >> 2;  // lane quarter, key-column half
+    const int r = wq * 32 + lane;            // TMEM lane = query row of the tile
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const int cbase = h * 64;
+    const float c = g.scale_log2;
+    const int i = q0 + r;
+    const bool row_valid = i < sq.q_len;
+    int wlo, whi;
+    key_window(g, sq, i, wlo, whi);
+    float lse2 = INFINITY, drow = 0.f;
+    if (row_valid) {
+      const int64_t si = stat_index(g, sq, w.b, w.n, i);
+      lse2 = a.lse2[si];
+      drow = a.dsum[si];
+    }
+    auto fetch_bits = [&](int j, uint32_t& kb0, uint32_t& kb1) {
+      kb0 = kb1 = 0xFFFFFFFFu;
+      if (DROP && row_valid) {
+        uint32_t bits[4];
+        load_keep_bits(a.mask, sq, w.n, i, (kv_t0 + j) * kTileN, bits);
+        kb0 = h ? bits[2] : bits[0];
+        kb1 = h ? bits[3] : bits[1];
+      }
+    };
+    uint32_t n_kb0 = 0xFFFFFFFFu, n_kb1 = 0xFFFFFFFFu;
+    if (DROP && n_kv > 0) fetch_bits(0, n_kb0, n_kb1);
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int b = j & 1;
+      const uint32_t u = (j >> 1) & 1;
+      const uint32_t kb0 = n_kb0, kb1 = n_kb1;
+      if (DROP && j + 1 < n_kv) fetch_bits(j + 1, n_kb0, n_kb1);
+      const int jb = (kv_t0 + j) * kTileN;
+      const bool full = tile_fully_visible(g, sq, q0, jb);
+
+      // ---- S -> P (kept in registers)
+      if (!compute_wait(&s.s_full[b], u, a.err)) { ok = false; break; }
+      tc_fence_after_sync();
+      float p[64];
+      {
+        uint32_t s0[32], s1[32];
+        tmem_ld_32x32b_x32(tmem + lane_off + b * 128 + cbase, s0);
+        tmem_ld_32x32b_x32(tmem + lane_off + b * 128 + cbase + 32, s1);
+        tmem_ld_wait(s0);
+        tmem_ld_wait(s1);
+        tc_fence_before_sync();
+        mbar_arrive(&s.s_loaded[b]);
+#pragma unroll
+        for (int t = 0; t < 64; ++t) {
+          const int jj = jb + cbase + t;
+          const bool vis = full || (jj >= wlo && jj <= whi);
+          const float sv = __uint_as_float(t < 32 ? s0[t] : s1[t - 32]);
+          p[t] = vis ? ex2_approx(sv * c - lse2) : 0.f;
+        }
+      }
+      // ---- dP -> dS (packed bf16)
+      if (!compute_wait(&s.dp_full[b], u, a.err)) { ok = false; break; }
+      tc_fence_after_sync();
+      uint32_t dk[32];
+      {
+        uint32_t d0[32], d1[32];
+        tmem_ld_32x32b_x32(tmem + lane_off + b * 128 + cbase, d0);
+        tmem_ld_32x32b_x32(tmem + lane_off + b * 128 + cbase + 32, d1);
+        tmem_ld_wait(d0);
+        tmem_ld_wait(d1);
+        tc_fence_before_sync();
+        mbar_arrive(&s.dp_loaded[b]);
+#pragma unroll
+        for (int t2 = 0; t2 < 32; ++t2) {
+          float dv[2];
+#pragma unroll
+          for (int uu = 0; uu < 2; ++uu) {
+            const int t = 2 * t2 + uu;
+            float dp = __uint_as_float(t < 32 ? d0[t] : d1[t - 32]);
+            if (DROP) {
+              const bool keep = ((t < 32 ? kb0 : kb1) >> (t & 31)) & 1u;
+              dp = keep ? dp * g.inv_keep : 0.f;
+            }
+            dv[uu] = p[t] * (dp - drow);
+          }
+          dk[t2] = pack_bf16x2(dv[0], dv[1]);
+        }
+      }
+      // ---- dS -> TMEM buffer b (after dQ(j-2) has read it)
+      if (j >= 2 && !compute_wait(&s.ds_free[b], u ^ 1, a.err)) { ok = false; break; }
+      tmem_st_32x32b_x32(tmem + lane_off + kColDS + b * 64 + h * 32, dk);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&s.ds_full[b]);
+    }
+    if (ok && n_kv > 0) ok = compute_wait(&s.ds_free[(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1, a.err);  // every MMA done
+    if (ok) {
+      tc_fence_after_sync();
+      // epilogue: dQ = scale * acc, row r, columns [h*D/2, h*D/2 + D/2)
+      constexpr int kCols = D / 2;
+      __nv_bfloat16* dst = a.dq + q_elem(g, sq, w.b, w.n, i) + h * kCols;
+#pragma unroll
+      for (int ch = 0; ch < kCols / 32; ++ch) {
+        float o[32];
+        if (n_kv > 0) {
+          uint32_t t32[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + kColDQ + h * kCols + ch * 32, t32);
+          tmem_ld_wait(t32);
+#pragma unroll
+          for (int t = 0; t < 32; ++t) o[t] = __uint_as_float(t32[t]) * g.scale;
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) o[t] = 0.f;
+        }
+        if (row_valid) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(dst + ch * 32)[q4] = pack8(&o[q4 * 8]);
+        }
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, bool DROP, int CAP>
+cudaError_t launch_dq_t(const BwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
+                        const CUtensorMap& mv, const CUtensorMap& mdy, cudaStream_t stream) {
+  const size_t smem = sizeof(DqSmem<D>) + 1024;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(swa_bwd_dq_kernel<D, DROP, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  swa_bwd_dq_kernel<D, DROP, CAP><<<tab.n_items, kThreads, smem, stream>>>(a, tab, mq, mk, mv, mdy);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+template <int CAP>
+cudaError_t launch_backward_dq(const BwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq,
+                               const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdy,
+                               cudaStream_t stream) {
+  if (tab.n_items == 0) return cudaSuccess;
+  const bool drop = a.g.has_mask != 0;
+  if (a.g.D == 64) return drop ? launch_dq_t<64, true>(a, tab, mq, mk, mv, mdy, stream)
+                               : launch_dq_t<64, false>(a, tab, mq, mk, mv, mdy, stream);
+  return drop ? launch_dq_t<128, true>(a, tab, mq, mk, mv, mdy, stream)
+              : launch_dq_t<128, false>(a, tab, mq, mk, mv, mdy, stream);
+}
+
+template cudaError_t launch_backward_dq<kSmallTable>(const BwdArgs&, const SeqTable<kSmallTable>&, const CUtensorMap&,
+                                                     const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                                     cudaStream_t);
+template cudaError_t launch_backward_dq<kLargeTable>(const BwdArgs&, const SeqTable<kLargeTable>&, const CUtensorMap&,
+                                                     const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                                     cudaStream_t);
+
+}  // namespace swa

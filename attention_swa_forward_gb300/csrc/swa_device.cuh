@@ -101,21 +101,6 @@ __device__ __forceinline__ void tma_rows(uint8_t* dst, const CUtensorMap* map, u
   }
 }
 
-// TMA reduce-add of a 128-row fp32 tile, D columns as D/32 swizzled boxes of
-// 128 rows x 32 floats, into the accumulator with q's layout.  Same
-// coordinate orders as tma_rows.
-template <int D>
-__device__ __forceinline__ void tma_reduce_rows(const uint8_t* src, const CUtensorMap* map, const Geometry& g, int b,
-                                                int n, int start, int row0) {
-#pragma unroll
-  for (int a = 0; a < D / 32; ++a) {
-    if (g.layout == 0)
-      tma_reduce_add_4d(map, src + a * kAtomBytes, a * 32, row0, n, b);
-    else
-      tma_reduce_add_4d(map, src + a * kAtomBytes, a * 32, n, start + row0, 0);
-  }
-}
-
 // 128 dropout keep bits of row i for keys [j0, j0+128): bit t of the result
 // (word t >> 5) is key j0 + t.  Bits past the sequence's last key are 0.
 // Element order: mask_base + (n*Sq + i)*Skv + j, least significant bit first.

@@ -92,8 +92,8 @@ struct BwdArgs {
   const uint8_t* mask;
   const float* lse2;   // per query row: softmax_max*log2(e) + log2(softmax_sum); +inf for empty rows
   const float* dsum;   // per query row: D = rowsum(dY * O)
-  float* dq_acc;       // fp32, q's layout: sum_j dS_ij k_j (scale applied at conversion), written by TMA reduce
-  __nv_bfloat16* dk;
+  __nv_bfloat16* dq;   // written by the query-major pass
+  __nv_bfloat16* dk;   // written by the key-major pass
   __nv_bfloat16* dv;
   int32_t* err;
 };
@@ -108,7 +108,6 @@ struct PrepArgs {
   const float* ssum;
   float* lse2;
   float* dsum;
-  float* dq_acc;
 };
 
 // Record `fmt` as the text of swa_last_error() on this thread; returns st.
@@ -120,11 +119,13 @@ template <int CAP>
 cudaError_t launch_forward(const FwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, cudaStream_t stream);
 template <int CAP>
-cudaError_t launch_backward(const BwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
-                            const CUtensorMap& mv, const CUtensorMap& mdy, const CUtensorMap& mdq,
-                            cudaStream_t stream);
+cudaError_t launch_backward_dkv(const BwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq,
+                                const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdy,
+                                cudaStream_t stream);
+template <int CAP>
+cudaError_t launch_backward_dq(const BwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq,
+                               const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdy,
+                               cudaStream_t stream);
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream);
-cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int64_t n_elems, float scale,
-                              cudaStream_t stream);
 
 }  // namespace swa

@@ -82,7 +82,7 @@ def lib() -> ctypes.CDLL:
             L.swa_backward_noalloc.restype = st
             L.swa_workspace_status.argtypes = [vp, vp]
             L.swa_workspace_status.restype = st
-            L.swa_set_timing_events.argtypes = [vp, vp, vp, vp]
+            L.swa_set_timing_events.argtypes = [vp]
             L.swa_set_timing_events.restype = None
             L.swa_last_error.argtypes = []
             L.swa_last_error.restype = ctypes.c_char_p
@@ -168,9 +168,19 @@ def swa_workspace_status(workspace, stream) -> int:
     return lib().swa_workspace_status(workspace, stream)
 
 
-def swa_set_timing_events(fwd_start=None, fwd_stop=None, bwd_start=None, bwd_stop=None):
-    """Raw cudaEvent_t handles (ints) recorded around the main kernels; None clears."""
-    lib().swa_set_timing_events(fwd_start, fwd_stop, bwd_start, bwd_stop)
+_timing_handles = None
+
+
+def swa_set_timing_events(events=None):
+    """Six raw cudaEvent_t handles (ints): forward, dK/dV and dQ start/stop pairs;
+    None stops recording."""
+    global _timing_handles
+    if events is None:
+        _timing_handles = None
+        lib().swa_set_timing_events(None)
+        return
+    _timing_handles = (ctypes.c_void_p * 6)(*events)
+    lib().swa_set_timing_events(_timing_handles)
 
 
 def swa_last_error() -> str:

@@ -41,7 +41,8 @@ METRIC = "SWA fwd+bwd TFLOPS (unmasked FLOPs, bf16) and % of GB300 bf16 dense pe
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
-KERNEL_SOURCES = ["attention_swa_forward_gb300/csrc/swa_fwd.cu", "attention_swa_forward_gb300/csrc/swa_bwd.cu",
+KERNEL_SOURCES = ["attention_swa_forward_gb300/csrc/swa_fwd.cu", "attention_swa_forward_gb300/csrc/swa_bwd_dkv.cu",
+                  "attention_swa_forward_gb300/csrc/swa_bwd_dq.cu",
                   "attention_swa_forward_gb300/csrc/swa_device.cuh", "attention_swa_forward_gb300/csrc/sm103.cuh"]
 
 
@@ -296,7 +297,7 @@ def run_swa(args, name: str):
     swa.check_workspace(ws_b)
 
     # ---- timed region: K steps, kernel events around the main kernels
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     for quad in evs:  # materialise the event handles on this stream
         for e in quad:
             e.record(stream)
@@ -311,7 +312,7 @@ def run_swa(args, name: str):
     sampler.mark(True)
     t_start.record(stream)
     for i in range(args.steps):
-        swa.swa_set_timing_events(*(e.cuda_event for e in evs[i]))
+        swa.swa_set_timing_events([e.cuda_event for e in evs[i]])
         step()
     t_end.record(stream)
     swa.swa_set_timing_events()
@@ -322,7 +323,8 @@ def run_swa(args, name: str):
     swa.check_workspace(ws_b)
     sec = t_start.elapsed_time(t_end) / 1e3 / args.steps
     fwd_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
-    bwd_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    dkv_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    dq_ms = sum(e[4].elapsed_time(e[5]) for e in evs) / args.steps
     sec_max = max_over_ranks(sec, ws, dev)
     value = whole_job_value(fl["total"], ws, sec_max)
 
@@ -366,9 +368,14 @@ def run_swa(args, name: str):
 
     peaks, source = load_peaks()
     peak_sust = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    # algorithmic FLOPs per launch: forward 4*D per visible pair (QK^T, PV);
+    # dK/dV pass 8*D (QK^T, dY V^T, P^T dY, dS^T Q); dQ pass 6*D (QK^T,
+    # dY V^T, dS K).  Only 14*D per pair counts toward the metric.
+    pairs_d = fl["pairs"] * g.D
     kernels = {
-        "swa_fwd_kernel": {"ms": fwd_ms, "tflops": fl["fwd"] / (fwd_ms / 1e3) / 1e12},
-        "swa_bwd_kernel": {"ms": bwd_ms, "tflops": fl["bwd"] / (bwd_ms / 1e3) / 1e12},
+        "swa_fwd_kernel": {"ms": fwd_ms, "tflops": 4.0 * pairs_d / (fwd_ms / 1e3) / 1e12},
+        "swa_bwd_dkv_kernel": {"ms": dkv_ms, "tflops": 8.0 * pairs_d / (dkv_ms / 1e3) / 1e12},
+        "swa_bwd_dq_kernel": {"ms": dq_ms, "tflops": 6.0 * pairs_d / (dq_ms / 1e3) / 1e12},
     }
     dom = max(kernels, key=lambda kname: kernels[kname]["ms"])
     traffic = None
@@ -392,7 +399,7 @@ def run_swa(args, name: str):
         "pct_of_bf16_peak": 100.0 * value / ws / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]),
         "flops_per_step": fl["total"], "visible_pairs": fl["pairs"],
         "roofline": roofline, "e2e": e2e,
-        "gpu_launches": args.steps * (n_tables_f + 3 * n_tables_b),
+        "gpu_launches": args.steps * (n_tables_f + 1 + 2 * n_tables_b),
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:

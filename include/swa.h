@@ -119,9 +119,9 @@ SWA_API swa_status_t swa_forward(const swa_params_t *p, const void *q, const voi
                          const uint8_t *drop_mask, void *out, float *softmax_max, float *softmax_sum,
                          void *workspace, size_t workspace_bytes, swa_stream_t stream);
 
-/* Device workspace bytes that swa_backward needs: a status word, per query
- * row D = rowsum(dY*O) and the log2-sum-exp of the forward statistics, and
- * an fp32 dQ accumulator of q's shape. */
+/* Device workspace bytes that swa_backward needs: a status word, and per
+ * query row D = rowsum(dY*O) and the log2-sum-exp of the forward statistics
+ * (8 bytes per query row and head). */
 SWA_API swa_status_t swa_backward_workspace_size(const swa_params_t *p, size_t *bytes);
 
 /* Backward (PyPTO-Gym "反向公式"; aclnnFlashAttentionUnpaddingScoreGradV2
@@ -142,7 +142,7 @@ SWA_API swa_status_t swa_backward(const swa_params_t *p, const void *q, const vo
  * latency-critical loop that must not allocate after start-up.
  *
  * Arguments and results are those of swa_backward.  The scratch it needs
- * (status word, per-row D and log2-sum-exp, fp32 dQ accumulator) lives in a
+ * (status word, per-row D and log2-sum-exp) lives in a
  * fixed 64 MiB device array compiled into the library: every GPU that loads
  * the library keeps it until the process exits.  A problem needing more than
  * 64 MiB of scratch (swa_backward_workspace_size) is rejected with
@@ -164,13 +164,13 @@ SWA_API swa_status_t swa_backward_noalloc(const swa_params_t *p, const void *q, 
  * (SWA_ERR_CUDA if the stream itself failed). */
 SWA_API swa_status_t swa_workspace_status(const void *workspace, swa_stream_t stream);
 
-/* Measurement support.  When non-NULL, the following calls on this thread
- * record `start` on their stream immediately before launching their main
- * attention kernel and `stop` immediately after it: fwd_* around the forward
- * kernel of swa_forward, bwd_* around the key-major kernel of swa_backward.
- * The events are cudaEvent_t handles owned by the caller; pass NULL to stop
- * recording.  No other effect on the computation. */
-SWA_API void swa_set_timing_events(void *fwd_start, void *fwd_stop, void *bwd_start, void *bwd_stop);
+/* Measurement support.  `events` is NULL (stop recording) or an array of six
+ * cudaEvent_t handles owned by the caller: {forward start, forward stop,
+ * dK/dV start, dK/dV stop, dQ start, dQ stop}.  Later calls on this thread
+ * record each pair on their stream immediately around the corresponding
+ * attention kernel launch (swa_forward's forward kernel; swa_backward's
+ * key-major dK/dV kernel and query-major dQ kernel).  No other effect. */
+SWA_API void swa_set_timing_events(void *const *events);
 
 /* Text describing the last non-OK status returned on this thread. */
 SWA_API const char *swa_last_error(void);

@@ -77,9 +77,9 @@ def test_noalloc_matches_workspace_backward(lib):
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch(lib):
-    # 1 x 32 x 32768 x 128 needs ~545 MB of scratch: rejected on the host
-    # before any device work (no GPU needed for this check)
-    g = Geometry("BNSD", 1, 32, 128, S_q=32768, S_kv=32768, scale=0.088, sparse_mode=4, pre_tokens=4096,
+    # 4 x 256 x 16384 query rows need 8 bytes each (134 MB) of scratch:
+    # rejected on the host before any device work (no GPU needed)
+    g = Geometry("BNSD", 4, 256, 128, S_q=16384, S_kv=16384, scale=0.088, sparse_mode=4, pre_tokens=4096,
                  next_tokens=0)
     p = swa.Params(g)
     fake = 1 << 20
