@@ -9,28 +9,33 @@
 // One CTA = one 128-row query tile of one (batch, head); it walks only the
 // 128-key tiles that intersect the BAND window.  Warp roles:
 //   warps 0-3  softmax + epilogue, one thread per query row (TMEM lane)
-//   warp  4    TMA producer: Q once, K/V through a 2-stage ring
+//   warp  4    TMA producer: Q once; K and V through separate 3-stage rings
+//              (a K stage is released as soon as its S is computed)
 //   warp  5    tcgen05 issuer: S = Q K^T into a double-buffered TMEM tile,
-//              O += P V with P (bf16) written to shared memory by warps 0-3
-// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D).
+//              then O += P V with P (bf16) taken from TMEM as the A operand
+// TMEM columns: S0 [0,128), S1 [128,256), O [256,256+D), P0 [384,448),
+// P1 [448,512).
 #include "swa_device.cuh"
 
 namespace swa {
 namespace {
 
+constexpr int kStages = 3;
+
 template <int D>
 struct FwdSmem {
   static constexpr int kTileBytes = kTileM * D * 2;
   alignas(1024) uint8_t q[kTileBytes];
-  alignas(1024) uint8_t k[2][kTileBytes];
-  alignas(1024) uint8_t v[2][kTileBytes];
-  alignas(1024) uint8_t p[kTileM * kTileN * 2];
-  uint64_t q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], s_free[2], p_full, o_done, mma_drain;
+  alignas(1024) uint8_t k[kStages][kTileBytes];
+  alignas(1024) uint8_t v[kStages][kTileBytes];
+  uint64_t q_full, k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
+  uint64_t s_full[2], s_free[2], p_full[2], o_done, mma_drain;
   uint32_t tmem_base;
 };
+static_assert(sizeof(FwdSmem<128>) + 1024 <= 232448, "shared memory budget");
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColO = 256, kColP = 384;  // P buffer b at kColP + 64*b
 constexpr float kLn2 = 0.6931471805599453f;
 // Rescale O only when the running max grows by more than 2^8 (log2 units);
 // until then the stale max is kept and p may reach 256, far from overflow.
@@ -38,8 +43,8 @@ constexpr float kRescaleThreshold = 8.0f;
 
 template <int D, bool DROP, int CAP>
 __global__ void __launch_bounds__(192, 1)
-    swa_fwd_kernel(const FwdArgs a, const __grid_constant__ SeqTable<CAP> tab, const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                   const __grid_constant__ CUtensorMap mv) {
+    swa_fwd_kernel(const FwdArgs a, const __grid_constant__ SeqTable<CAP> tab, const __grid_constant__ CUtensorMap mq,
+                   const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
   extern __shared__ uint8_t smem_raw[];
   FwdSmem<D>& s = *reinterpret_cast<FwdSmem<D>*>(align1024(smem_raw));
   constexpr int kTileBytes = FwdSmem<D>::kTileBytes;
@@ -64,14 +69,17 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&s.q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.v_full[i], 1);
-      mbar_init(&s.kv_empty[i], 1);
+      mbar_init(&s.k_empty[i], 1);
+      mbar_init(&s.v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.s_free[i], kTileM);
+      mbar_init(&s.p_full[i], kTileM);
     }
-    mbar_init(&s.p_full, kTileM);
     mbar_init(&s.o_done, 1);
     mbar_init(&s.mma_drain, 1);
     fence_mbar_init();
@@ -93,25 +101,26 @@ __global__ void __launch_bounds__(192, 1)
       tma_prefetch_desc(&mv);
       mbar_arrive_expect_tx(&s.q_full, kTileBytes);
       tma_rows<D>(s.q, &mq, &s.q_full, g, w.b, w.n, sq.q_start, q0);
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       for (int it = 0; it < n_kv; ++it) {
-        const int st = it & 1;
-        if (it >= 2 && !mbar_wait(&s.kv_empty[st], ((it >> 1) - 1) & 1, a.err, kErrFwdLoad)) break;
+        const int st = it % kStages;
+        const uint32_t use = it / kStages;
         const int j0 = (kv_t0 + it) * kTileN;
+        if (it >= kStages && !mbar_wait(&s.k_empty[st], (use - 1) & 1, a.err, kErrFwdLoad)) break;
         mbar_arrive_expect_tx(&s.k_full[st], kTileBytes);
         tma_rows<D>(s.k[st], &mk, &s.k_full[st], g, w.b, w.n, sq.kv_start, j0);
+        ++k_issued;
+        if (it >= kStages && !mbar_wait(&s.v_empty[st], (use - 1) & 1, a.err, kErrFwdLoad)) break;
         mbar_arrive_expect_tx(&s.v_full[st], kTileBytes);
         tma_rows<D>(s.v[st], &mv, &s.v_full[st], g, w.b, w.n, sq.kv_start, j0);
-        ++issued;
+        ++v_issued;
       }
       // every copy issued has landed before the CTA may exit
       mbar_wait_drain(&s.q_full, 0);
-      for (int st = 0; st < 2; ++st) {
-        const int uses = (issued - st + 1) / 2;
-        if (uses > 0) {
-          mbar_wait_drain(&s.k_full[st], (uses - 1) & 1);
-          mbar_wait_drain(&s.v_full[st], (uses - 1) & 1);
-        }
+      for (int st = 0; st < kStages; ++st) {
+        const int uk = (k_issued - st + kStages - 1) / kStages, uv = (v_issued - st + kStages - 1) / kStages;
+        if (uk > 0) mbar_wait_drain(&s.k_full[st], (uk - 1) & 1);
+        if (uv > 0) mbar_wait_drain(&s.v_full[st], (uv - 1) & 1);
       }
     }
   } else if (warp == 5) {
@@ -119,38 +128,43 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0 && n_kv > 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kTileM, kTileN, false, false);
       constexpr uint32_t kIdO = idesc_bf16_f32(kTileM, D, false, true);
-      const uint32_t q_addr = smem_u32(s.q), p_addr = smem_u32(s.p);
-      bool ok = mbar_wait(&s.q_full, 0, a.err, kErrFwdMma);
-      for (int it = 0; ok && it <= n_kv; ++it) {
-        if (it < n_kv) {
-          const int st = it & 1;
-          if (!mbar_wait(&s.k_full[st], (it >> 1) & 1, a.err, kErrFwdMma)) break;
-          if (it >= 2 && !mbar_wait(&s.s_free[st], ((it >> 1) - 1) & 1, a.err, kErrFwdMma)) break;
-          tc_fence_after_sync();
-          const uint32_t k_addr = smem_u32(s.k[st]);
+      const uint32_t q_addr = smem_u32(s.q);
+      auto issue_s = [&](int it) {  // S(it) = Q K_it^T into S buffer it % 2
+        const int st = it % kStages, sb = it & 1;
+        const uint32_t k_addr = smem_u32(s.k[st]);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-            umma_bf16_ss(tmem + st * kTileN, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                         kIdS, kk > 0);
-          }
-          umma_commit(&s.s_full[st]);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
+          umma_bf16_ss(tmem + sb * kTileN, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
+                       kIdS, kk > 0);
         }
-        if (it >= 1) {
-          const int pj = it - 1, pst = pj & 1;
-          if (!mbar_wait(&s.p_full, pj & 1, a.err, kErrFwdMma)) break;
-          if (!mbar_wait(&s.v_full[pst], (pj >> 1) & 1, a.err, kErrFwdMma)) break;
+        umma_commit(&s.s_full[sb]);
+        umma_commit(&s.k_empty[st]);
+      };
+      bool ok = mbar_wait(&s.q_full, 0, a.err, kErrFwdMma) && mbar_wait(&s.k_full[0], 0, a.err, kErrFwdMma);
+      if (ok) {
+        tc_fence_after_sync();
+        issue_s(0);
+      }
+      for (int it = 0; ok && it < n_kv; ++it) {
+        if (it + 1 < n_kv) {  // next S while softmax(it) runs
+          const int nt = it + 1, nsb = nt & 1;
+          if (nt >= 2 && !mbar_wait(&s.s_free[nsb], ((nt >> 1) - 1) & 1, a.err, kErrFwdMma)) break;
+          if (!mbar_wait(&s.k_full[nt % kStages], (nt / kStages) & 1, a.err, kErrFwdMma)) break;
           tc_fence_after_sync();
-          const uint32_t v_addr = smem_u32(s.v[pst]);
-#pragma unroll
-          for (int kk = 0; kk < kTileN / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-            umma_bf16_ss(tmem + kColO, sdesc_sw128(p_addr + aoff, 16, 1024),
-                         sdesc_sw128(v_addr + kk * 2048, kAtomBytes, 1024), kIdO, (pj > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(&s.o_done);
-          umma_commit(&s.kv_empty[pst]);
+          issue_s(nt);
         }
+        const int pb = it & 1, st = it % kStages;
+        if (!mbar_wait(&s.p_full[pb], (it >> 1) & 1, a.err, kErrFwdMma)) break;
+        if (!mbar_wait(&s.v_full[st], (it / kStages) & 1, a.err, kErrFwdMma)) break;
+        tc_fence_after_sync();
+        const uint32_t v_addr = smem_u32(s.v[st]);
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)  // O += P V  (A = P in TMEM)
+          umma_bf16_ts(tmem + kColO, tmem + kColP + pb * 64 + kk * 8, sdesc_sw128(v_addr + kk * 2048, kAtomBytes, 1024),
+                       kIdO, (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&s.o_done);
+        umma_commit(&s.v_empty[st]);
       }
       umma_commit(&s.mma_drain);
       mbar_wait_drain(&s.mma_drain, 0);
@@ -246,7 +260,14 @@ __global__ void __launch_bounds__(192, 1)
         for (int t = 0; t < kTileN; ++t)
           if (!((bits[t >> 5] >> (t & 31)) & 1u)) x[t] = 0.f;
       }
-      // The previous P V must be done before P is overwritten or O rescaled.
+      uint32_t pk0[32], pk1[32];
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        pk0[t] = pack_bf16x2(x[2 * t], x[2 * t + 1]);
+        pk1[t] = pack_bf16x2(x[64 + 2 * t], x[64 + 2 * t + 1]);
+      }
+      // PV(it-1) must be done before O is rescaled; it also frees P buffer
+      // (it & 1), last read by PV(it-2).
       if (it >= 1) {
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&s.o_done, (it - 1) & 1, a.err, kErrFwdSoftmax))) {
           ok = false;
@@ -264,14 +285,13 @@ __global__ void __launch_bounds__(192, 1)
             for (int t = 0; t < 32; ++t) t32[t] = __float_as_uint(__uint_as_float(t32[t]) * alpha);
             tmem_st_32x32b_x32(addr, t32);
           }
-          tmem_st_wait();
         }
       }
-#pragma unroll
-      for (int ch = 0; ch < kTileN / 8; ++ch) st_chunk_sw128(s.p, r, ch, pack8(&x[ch * 8]));
-      fence_proxy_async_smem();
+      tmem_st_32x32b_x32(tmem + lane_off + kColP + sb * 64, pk0);
+      tmem_st_32x32b_x32(tmem + lane_off + kColP + sb * 64 + 32, pk1);
+      tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&s.p_full);
+      mbar_arrive(&s.p_full[sb]);
     }
     if (ok && n_kv > 0) {
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s.o_done, (n_kv - 1) & 1, a.err, kErrFwdSoftmax));
