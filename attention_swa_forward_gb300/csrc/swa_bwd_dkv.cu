@@ -14,54 +14,80 @@
 // tiles of the band with dK / dV accumulating in TMEM.  Warps:
 //   warps 0-7  compute: warp w owns TMEM lanes 32*(w%4).. (key rows) and query
 //              columns 64*(w/4).. of each tile; then dV (w<4) or dK (w>=4)
-//   warp  8    producer: K, V once; Q, dY by TMA through 2-stage rings, and
-//              the tile's per-query lse2 / D (and dropout bits) into shared
+//   warp  8    producer: K, V once; Q (3-stage ring) and dY (2 stages) by TMA,
+//              and each tile's per-query lse2 / D (and dropout bits) into shared
 //   warp  9    tcgen05 issuer
 // TMEM: two 128-column regions R0, R1, dV [256,256+D), dK [256+D,256+2D).
-// Tile i computes S^T into R(i%2) and dP^T into R((i+1)%2); once both are in
-// registers, P^T and dS^T (bf16) are stored into R(i%2) and feed dV / dK as
-// the TMEM A operand, while S^T(i+1) already runs in R((i+1)%2).
+// Query tile i lives in R(i%2): S^T(i) is computed there; once every thread has
+// it in registers, dP^T(i) is computed over it; each thread then stores its
+// P^T / dS^T (bf16) into the very columns it read, and dV / dK take them as
+// the TMEM A operand.  Issue order per tile: dP^T(i), S^T(i+1) (into the other
+// region, once dK(i-1) has finished reading it), dV(i), dK(i): the tensor pipe
+// always has the next GEMM queued while the compute warps work.
 #include "swa_device.cuh"
 
 namespace swa {
 namespace {
 
-template <int D>
+template <bool DROP>
+struct KeepBits {
+  uint32_t w[2][kTileM][4];  // dropout keep bits: [stage][query row][key word]
+};
+template <>
+struct KeepBits<false> {};
+
+template <int D, bool DROP>
 struct DkvSmem {
   static constexpr int kTileBytes = kTileM * D * 2;
+  // a third Q stage lets Q(i+2) load while tile i computes; it does not fit
+  // next to the dropout bits at D = 128
+  static constexpr int kQStages = (DROP && D == 128) ? 2 : 3;
   alignas(1024) uint8_t k[kTileBytes];
   alignas(1024) uint8_t v[kTileBytes];
-  alignas(1024) uint8_t q[2][kTileBytes];
+  alignas(1024) uint8_t q[kQStages][kTileBytes];
   alignas(1024) uint8_t dy[2][kTileBytes];
-  float lse2[2][kTileM];   // per query column of the tile in that stage (+inf: row outside)
+  float lse2[2][kTileM];  // per query column of the tile in that stage (+inf: row outside)
   float dsum[2][kTileM];
-  uint32_t keep[2][kTileM][4];  // dropout keep bits: [query row][key word]
-  uint64_t kv_full, q_full[2], q_empty[2], dy_full[2], dy_empty[2], stat_full[2];
-  uint64_t s_full, dp_full, sdp_loaded, pds_full, pds_free, mma_drain;
+  KeepBits<DROP> keep;
+  uint64_t kv_full, q_full[kQStages], q_empty[kQStages], dy_full[2], dy_empty[2], stat_full[2];
+  uint64_t s_full[2], s_loaded, dp_full, pds_full, pds_free, mma_done, mma_drain;
   uint32_t tmem_base;
 };
-static_assert(sizeof(DkvSmem<128>) + 1024 <= 232448, "shared memory budget");
+constexpr size_t kMaxSmem = 232448;
+static_assert(sizeof(DkvSmem<128, false>) <= kMaxSmem, "shared memory budget");
+static_assert(sizeof(DkvSmem<128, true>) + 1024 <= kMaxSmem, "shared memory budget");
+// Whether the launch can add 1 KB of slack to align the dynamic shared memory
+// base to 1024 bytes; without it the kernel checks the alignment itself.
+template <int D, bool DROP>
+constexpr bool kDkvSlack = sizeof(DkvSmem<D, DROP>) + 1024 <= kMaxSmem;
 
 constexpr int kThreads = 320;
 constexpr int kComputeThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColDV = 256;
-constexpr uint32_t kBarVote = 1;
 
+// Warp-uniform bounded wait of the compute warps.  A warp vote (not a
+// CTA-wide barrier) keeps each warp converged for its warp-collective TMEM
+// accesses; no compute step reads what another warp wrote in TMEM.
 __device__ __forceinline__ bool compute_wait(uint64_t* bar, uint32_t parity, int* err) {
-  return named_barrier_and(kBarVote, kComputeThreads, mbar_wait(bar, parity, err, kErrBwdCompute));
+  return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, err, kErrBwdCompute));
 }
-__device__ __forceinline__ uint32_t region_s(int it) { return (it & 1) * 128u; }         // S^T, then P^T / dS^T
-__device__ __forceinline__ uint32_t region_dp(int it) { return ((it + 1) & 1) * 128u; }  // dP^T
+__device__ __forceinline__ uint32_t region(int it) { return (it & 1) * 128u; }
 
 template <int D, bool DROP, int CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_bwd_dkv_kernel(const BwdArgs a, const __grid_constant__ SeqTable<CAP> tab,
                        const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                        const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdy) {
+  using Smem = DkvSmem<D, DROP>;
+  constexpr int kQS = Smem::kQStages;
   extern __shared__ uint8_t smem_raw[];
-  DkvSmem<D>& s = *reinterpret_cast<DkvSmem<D>*>(align1024(smem_raw));
-  constexpr int kTileBytes = DkvSmem<D>::kTileBytes;
+  if (!kDkvSlack<D, DROP> && (smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicCAS(a.err, 0, kErrSmemAlign);
+    return;
+  }
+  Smem& s = *reinterpret_cast<Smem*>(align1024(smem_raw));
+  constexpr int kTileBytes = Smem::kTileBytes;
   constexpr uint32_t kColDK = kColDV + D;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Geometry& g = a.g;
@@ -84,18 +110,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&s.kv_full, 1);
-    for (int st = 0; st < 2; ++st) {
+    for (int st = 0; st < kQS; ++st) {
       mbar_init(&s.q_full[st], 1);
       mbar_init(&s.q_empty[st], 1);
+    }
+    for (int st = 0; st < 2; ++st) {
       mbar_init(&s.dy_full[st], 1);
       mbar_init(&s.dy_empty[st], 1);
       mbar_init(&s.stat_full[st], 32);
+      mbar_init(&s.s_full[st], 1);
     }
-    mbar_init(&s.s_full, 1);
+    mbar_init(&s.s_loaded, kComputeThreads);
     mbar_init(&s.dp_full, 1);
-    mbar_init(&s.sdp_loaded, kComputeThreads);
     mbar_init(&s.pds_full, kComputeThreads);
     mbar_init(&s.pds_free, 1);
+    mbar_init(&s.mma_done, 1);
     mbar_init(&s.mma_drain, 1);
     fence_mbar_init();
   }
@@ -123,14 +152,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       int q_issued = 0, dy_issued = 0;
       for (int it = 0; it < n_q; ++it) {
         const int i0 = (q_t0 + it) * kTileM;
-        const int st = it & 1;
-        if (it >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait(&s.q_empty[st], ((it >> 1) - 1) & 1, a.err, kErrBwdLoad)))
+        const int qs = it % kQS;
+        // Q(it) reuses the stage of Q(it - kQS), free once dK of that tile is done
+        if (it >= kQS &&
+            !__all_sync(0xFFFFFFFFu, mbar_wait(&s.q_empty[qs], ((it / kQS) - 1) & 1, a.err, kErrBwdLoad)))
           break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&s.q_full[st], kTileBytes);
-          tma_rows<D>(s.q[st], &mq, &s.q_full[st], g, w.b, w.n, sq.q_start, i0);
+          mbar_arrive_expect_tx(&s.q_full[qs], kTileBytes);
+          tma_rows<D>(s.q[qs], &mq, &s.q_full[qs], g, w.b, w.n, sq.q_start, i0);
         }
         ++q_issued;
+        // dY and the statistics reuse stage (it & 1) once dV(it - 2) is done,
+        // which also means the compute warps are through with tile it - 2
+        const int st = it & 1;
+        if (it >= 2 &&
+            !__all_sync(0xFFFFFFFFu, mbar_wait(&s.dy_empty[st], ((it >> 1) - 1) & 1, a.err, kErrBwdLoad)))
+          break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&s.dy_full[st], kTileBytes);
+          tma_rows<D>(s.dy[st], &mdy, &s.dy_full[st], g, w.b, w.n, sq.q_start, i0);
+        }
+        ++dy_issued;
         // per-query statistics (and keep bits) of this tile: 4 rows per lane
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
@@ -142,31 +184,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t si = stat_index(g, sq, w.b, w.n, i);
             l2 = a.lse2[si];
             dd = a.dsum[si];
-            if (DROP) load_keep_bits(a.mask, sq, w.n, i, j0, bits);
+            if constexpr (DROP) load_keep_bits(a.mask, sq, w.n, i, j0, bits);
           }
           s.lse2[st][c] = l2;
           s.dsum[st][c] = dd;
-          if (DROP) {
+          if constexpr (DROP) {
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) s.keep[st][c][q4] = bits[q4];
+            for (int q4 = 0; q4 < 4; ++q4) s.keep.w[st][c][q4] = bits[q4];
           }
         }
         mbar_arrive(&s.stat_full[st]);
-        if (it >= 2 &&
-            !__all_sync(0xFFFFFFFFu, mbar_wait(&s.dy_empty[st], ((it >> 1) - 1) & 1, a.err, kErrBwdLoad)))
-          break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&s.dy_full[st], kTileBytes);
-          tma_rows<D>(s.dy[st], &mdy, &s.dy_full[st], g, w.b, w.n, sq.q_start, i0);
-        }
-        ++dy_issued;
       }
       // every copy issued has landed before the CTA may exit
       if (lane == 0) {
         mbar_wait_drain(&s.kv_full, 0);
-        for (int st = 0; st < 2; ++st) {
-          const int uq = (q_issued - st + 1) / 2, ud = (dy_issued - st + 1) / 2;
+        for (int st = 0; st < kQS; ++st) {
+          const int uq = (q_issued - st + kQS - 1) / kQS;
           if (uq > 0) mbar_wait_drain(&s.q_full[st], (uq - 1) & 1);
+        }
+        for (int st = 0; st < 2; ++st) {
+          const int ud = (dy_issued - st + 1) / 2;
           if (ud > 0) mbar_wait_drain(&s.dy_full[st], (ud - 1) & 1);
         }
       }
@@ -177,64 +214,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdT = idesc_bf16_f32(kTileN, kTileM, false, false);  // S^T, dP^T
       constexpr uint32_t kIdKV = idesc_bf16_f32(kTileN, D, false, true);       // dV, dK (A = P^T / dS^T in TMEM)
       const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
-      auto issue_st = [&](int it) {  // S^T = K Q^T into region_s(it)
-        const uint32_t q_addr = smem_u32(s.q[it & 1]);
+      auto issue_ss = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {  // 128 x 128 x D, both K-major
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-          umma_bf16_ss(tmem + region_s(it), sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024),
-                       kIdT, kk > 0);
+          umma_bf16_ss(tmem + d_col, sdesc_sw128(a_addr + off, 16, 1024), sdesc_sw128(b_addr + off, 16, 1024), kIdT,
+                       kk > 0);
         }
-        umma_commit(&s.s_full);
       };
-      auto issue_dpt = [&](int it) {  // dP^T = V dY^T into region_dp(it)
-        const uint32_t dy_addr = smem_u32(s.dy[it & 1]);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-          umma_bf16_ss(tmem + region_dp(it), sdesc_sw128(v_addr + off, 16, 1024),
-                       sdesc_sw128(dy_addr + off, 16, 1024), kIdT, kk > 0);
-        }
-        umma_commit(&s.dp_full);
-      };
-      bool ok = mbar_wait(&s.kv_full, 0, a.err, kErrBwdMma) && mbar_wait(&s.q_full[0], 0, a.err, kErrBwdMma) &&
-                mbar_wait(&s.dy_full[0], 0, a.err, kErrBwdMma);
+      bool ok = mbar_wait(&s.kv_full, 0, a.err, kErrBwdMma) && mbar_wait(&s.q_full[0], 0, a.err, kErrBwdMma);
       if (ok) {
         tc_fence_after_sync();
-        issue_st(0);
-        issue_dpt(0);
+        issue_ss(region(0), k_addr, smem_u32(s.q[0]));  // S^T(0) = K Q(0)^T
+        umma_commit(&s.s_full[0]);
       }
       for (int it = 0; ok && it < n_q; ++it) {
-        const int st = it & 1;
-        const uint32_t ph = it & 1;
-        // region_dp(it) is free once S^T(it) / dP^T(it) are in registers
-        if (!mbar_wait(&s.sdp_loaded, ph, a.err, kErrBwdMma)) break;
-        if (it + 1 < n_q) {
-          if (!mbar_wait(&s.q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, a.err, kErrBwdMma)) break;
-          tc_fence_after_sync();
-          issue_st(it + 1);
-        }
-        if (!mbar_wait(&s.pds_full, ph, a.err, kErrBwdMma)) break;
+        const int st = it & 1, qs = it % kQS;
+        // dP^T(it) over S^T(it), once every compute thread has read S^T(it)
+        if (!mbar_wait(&s.s_loaded, it & 1, a.err, kErrBwdMma)) break;
+        if (!mbar_wait(&s.dy_full[st], (it >> 1) & 1, a.err, kErrBwdMma)) break;
         tc_fence_after_sync();
-        const uint32_t dy_addr = smem_u32(s.dy[st]), q_addr = smem_u32(s.q[st]);
-        const uint32_t ra = tmem + region_s(it);
+        issue_ss(region(it), v_addr, smem_u32(s.dy[st]));  // dP^T = V dY^T
+        umma_commit(&s.dp_full);
+        if (it + 1 < n_q) {
+          // S^T(it+1) into the other region, once dK(it-1) has read it
+          if (it >= 1 && !mbar_wait(&s.pds_free, (it - 1) & 1, a.err, kErrBwdMma)) break;
+          const int nq = (it + 1) % kQS;
+          if (!mbar_wait(&s.q_full[nq], ((it + 1) / kQS) & 1, a.err, kErrBwdMma)) break;
+          tc_fence_after_sync();
+          issue_ss(region(it + 1), k_addr, smem_u32(s.q[nq]));
+          umma_commit(&s.s_full[(it + 1) & 1]);
+        }
+        // dV, dK from the P^T / dS^T the compute warps stored in region(it):
+        // query columns [64h, 64h+64) of the tile hold P^T in columns
+        // [64h, 64h+32) and dS^T in [64h+32, 64h+64), two bf16 per column
+        if (!mbar_wait(&s.pds_full, it & 1, a.err, kErrBwdMma)) break;
+        tc_fence_after_sync();
+        const uint32_t ra = tmem + region(it);
+        const uint32_t dy_addr = smem_u32(s.dy[st]), q_addr = smem_u32(s.q[qs]);
 #pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk)  // dV += P^T dY  (K dim = query rows)
-          umma_bf16_ts(tmem + kColDV, ra + kk * 8, sdesc_sw128(dy_addr + kk * 2048, kAtomBytes, 1024), kIdKV,
-                       (it > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + kColDV, ra + (kk >> 2) * 64 + (kk & 3) * 8,
+                       sdesc_sw128(dy_addr + kk * 2048, kAtomBytes, 1024), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&s.dy_empty[st]);
 #pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk)  // dK += dS^T Q
-          umma_bf16_ts(tmem + kColDK, ra + 64 + kk * 8, sdesc_sw128(q_addr + kk * 2048, kAtomBytes, 1024), kIdKV,
-                       (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&s.q_empty[st]);
+          umma_bf16_ts(tmem + kColDK, ra + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
+                       sdesc_sw128(q_addr + kk * 2048, kAtomBytes, 1024), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&s.q_empty[qs]);
         umma_commit(&s.pds_free);
-        if (it + 1 < n_q) {  // dP^T(i+1) reuses region_s(it) once dV / dK(it) have read it
-          if (!mbar_wait(&s.pds_free, ph, a.err, kErrBwdMma)) break;
-          if (!mbar_wait(&s.dy_full[(it + 1) & 1], ((it + 1) >> 1) & 1, a.err, kErrBwdMma)) break;
-          tc_fence_after_sync();
-          issue_dpt(it + 1);
-        }
+        if (it == n_q - 1) umma_commit(&s.mma_done);
       }
       umma_commit(&s.mma_drain);
       mbar_wait_drain(&s.mma_drain, 0);
@@ -262,17 +291,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = it & 1;
       const int i0 = (q_t0 + it) * kTileM;
       const bool full = tile_fully_visible(g, sq, i0, j0);
-      if (!compute_wait(&s.s_full, it & 1, a.err)) { ok = false; break; }
+      const uint32_t col = tmem + lane_off + region(it) + cbase;
+      if (!compute_wait(&s.s_full[st], (it >> 1) & 1, a.err)) { ok = false; break; }
       if (!compute_wait(&s.stat_full[st], (it >> 1) & 1, a.err)) { ok = false; break; }
       tc_fence_after_sync();
       // ---- S^T -> P^T (registers)
       float p[64];
       {
         uint32_t s0[32], s1[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + region_s(it) + cbase, s0);
-        tmem_ld_32x32b_x32(tmem + lane_off + region_s(it) + cbase + 32, s1);
+        tmem_ld_32x32b_x32(col, s0);
+        tmem_ld_32x32b_x32(col + 32, s1);
         tmem_ld_wait(s0);
         tmem_ld_wait(s1);
+        tc_fence_before_sync();
+        mbar_arrive(&s.s_loaded);  // region(it) may now receive dP^T(it)
 #pragma unroll
         for (int t4 = 0; t4 < 16; ++t4) {
           const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[st][cbase + t4 * 4]);
@@ -283,22 +315,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i = i0 + cbase + t;
             const bool vis = full || (i >= qlo && i <= qhi);
             const float sv = __uint_as_float(t < 32 ? s0[t] : s1[t - 32]);
-            p[t] = vis ? ex2_approx(sv * c - lv[u]) : 0.f;
+            const float e = ex2_approx(sv * c - lv[u]);  // unconditional: a select, not a branch
+            p[t] = vis ? e : 0.f;
           }
         }
       }
-      // ---- dP^T -> dS^T; P^T*z/keep and dS^T packed bf16
+      // ---- dP^T -> dS^T; P^T*z/keep and dS^T packed bf16 into the same columns
       if (!compute_wait(&s.dp_full, it & 1, a.err)) { ok = false; break; }
       tc_fence_after_sync();
       uint32_t pk[32], dk[32];
       {
         uint32_t d0[32], d1[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + region_dp(it) + cbase, d0);
-        tmem_ld_32x32b_x32(tmem + lane_off + region_dp(it) + cbase + 32, d1);
+        tmem_ld_32x32b_x32(col, d0);
+        tmem_ld_32x32b_x32(col + 32, d1);
         tmem_ld_wait(d0);
         tmem_ld_wait(d1);
-        tc_fence_before_sync();
-        mbar_arrive(&s.sdp_loaded);
 #pragma unroll
         for (int t4 = 0; t4 < 16; ++t4) {
           const float4 d4 = *reinterpret_cast<const float4*>(&s.dsum[st][cbase + t4 * 4]);
@@ -309,8 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t = t4 * 4 + u;
             float dp = __uint_as_float(t < 32 ? d0[t] : d1[t - 32]);
             float pt = p[t];
-            if (DROP) {
-              const bool keep = (s.keep[st][cbase + t][wq] >> lane) & 1u;  // bit (query, key r)
+            if constexpr (DROP) {
+              const bool keep = (s.keep.w[st][cbase + t][wq] >> lane) & 1u;  // bit (query, key r)
               pt = keep ? p[t] * g.inv_keep : 0.f;
               dp = keep ? dp * g.inv_keep : 0.f;
             }
@@ -323,19 +354,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           dk[t4 * 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
         }
       }
-      // ---- P^T, dS^T -> TMEM region_s(it) (its S^T is consumed)
-      tmem_st_32x32b_x32(tmem + lane_off + region_s(it) + h * 32, pk);
-      tmem_st_32x32b_x32(tmem + lane_off + region_s(it) + 64 + h * 32, dk);
+      tmem_st_32x32b_x32(col, pk);
+      tmem_st_32x32b_x32(col + 32, dk);
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(&s.pds_full);
     }
-    if (ok && n_q > 0) ok = compute_wait(&s.pds_free, (n_q - 1) & 1, a.err);  // every MMA done
+    if (ok && n_q > 0) ok = compute_wait(&s.mma_done, 0, a.err);  // every MMA done
     if (ok) {
       tc_fence_after_sync();
       // epilogue: thread r owns key row j0 + r; warps 0-3 write dV, 4-7 dK
       const bool kv_valid = j < sq.kv_len;
-      const uint32_t col = h == 0 ? kColDV : kColDK;
+      const uint32_t dcol = h == 0 ? kColDV : kColDK;
       const float mul = h == 0 ? 1.f : g.scale;
       __nv_bfloat16* dst = (h == 0 ? a.dv : a.dk) + kv_elem(g, sq, w.b, w.n, j);
 #pragma unroll
@@ -343,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float o[32];
         if (n_q > 0) {
           uint32_t t32[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + col + ch * 32, t32);
+          tmem_ld_32x32b_x32(tmem + lane_off + dcol + ch * 32, t32);
           tmem_ld_wait(t32);
 #pragma unroll
           for (int t = 0; t < 32; ++t) o[t] = __uint_as_float(t32[t]) * mul;
@@ -369,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool DROP, int CAP>
 cudaError_t launch_dkv_t(const BwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, const CUtensorMap& mdy, cudaStream_t stream) {
-  const size_t smem = sizeof(DkvSmem<D>) + 1024;
+  const size_t smem = sizeof(DkvSmem<D, DROP>) + (kDkvSlack<D, DROP> ? 1024 : 0);
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(swa_bwd_dkv_kernel<D, DROP, CAP>,

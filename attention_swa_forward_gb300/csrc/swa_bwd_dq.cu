@@ -42,10 +42,12 @@ constexpr int kThreads = 320;
 constexpr int kComputeThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColDQ = 256, kColDS = 384;  // dS buffer b at kColDS + 64*b
-constexpr uint32_t kBarVote = 1;
 
+// Warp-uniform bounded wait of the compute warps.  A warp vote (not a
+// CTA-wide barrier) keeps each warp converged for its warp-collective TMEM
+// accesses; no compute step reads what another warp wrote in TMEM.
 __device__ __forceinline__ bool compute_wait(uint64_t* bar, uint32_t parity, int* err) {
-  return named_barrier_and(kBarVote, kComputeThreads, mbar_wait(bar, parity, err, kErrBwdCompute));
+  return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, err, kErrBwdCompute));
 }
 
 template <int D, bool DROP, int CAP>
@@ -243,7 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int jj = jb + cbase + t;
           const bool vis = full || (jj >= wlo && jj <= whi);
           const float sv = __uint_as_float(t < 32 ? s0[t] : s1[t - 32]);
-          p[t] = vis ? ex2_approx(sv * c - lse2) : 0.f;
+          const float e = ex2_approx(sv * c - lse2);  // unconditional: a select, not a branch
+          p[t] = vis ? e : 0.f;
         }
       }
       // ---- dP -> dS (packed bf16)

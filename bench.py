@@ -272,7 +272,8 @@ def run_swa(args, name: str):
     swa.lib()
 
     w = WORKLOADS[name]
-    inp = draw(w.geom, w.seed, w.lengths)
+    geom = w.geom if args.heads is None else Geometry(**{**w.geom.as_dict(), "N": args.heads})
+    inp = draw(geom, w.seed, w.lengths)
     g = inp.geom
     fl = flops(g)
     p = swa.Params(g)
@@ -395,7 +396,7 @@ def run_swa(args, name: str):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": sec_max * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, shapes of the workload)",
-        "config": workload_config(g, name),
+        "config": workload_config(g, name if args.heads is None else f"{name} with N={g.N}"),
         "pct_of_bf16_peak": 100.0 * value / ws / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]),
         "flops_per_step": fl["total"], "visible_pairs": fl["pairs"],
         "roofline": roofline, "e2e": e2e,
@@ -419,6 +420,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=8192, help="positions per oracle sample (reference arm)")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="override the workload's head count N (smaller profiling captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
