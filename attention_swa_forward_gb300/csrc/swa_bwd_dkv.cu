@@ -16,14 +16,17 @@
 //              columns 64*(w/4).. of each tile; then dV (w<4) or dK (w>=4)
 //   warp  8    producer: K, V once; Q (3-stage ring) and dY (2 stages) by TMA,
 //              and each tile's per-query lse2 / D (and dropout bits) into shared
-//   warp  9    tcgen05 issuer
+//   warp  9    tcgen05 issuer of S^T and dP^T (SS)
+//   warp 10    tcgen05 issuer of dV and dK (TS)
 // TMEM: two 128-column regions R0, R1, dV [256,256+D), dK [256+D,256+2D).
 // Query tile i lives in R(i%2): S^T(i) is computed there; once every thread has
 // it in registers, dP^T(i) is computed over it; each thread then stores its
 // P^T / dS^T (bf16) into the very columns it read, and dV / dK take them as
 // the TMEM A operand.  Issue order per tile: dP^T(i), S^T(i+1) (into the other
 // region, once dK(i-1) has finished reading it), dV(i), dK(i): the tensor pipe
-// always has the next GEMM queued while the compute warps work.
+// always has the next GEMM queued while the compute warps work.  Two issuing
+// threads keep it fed: its queue is shallow, so every barrier wait of a
+// single issuer between GEMMs left it idle.
 #include "swa_device.cuh"
 
 namespace swa {
@@ -50,7 +53,9 @@ struct DkvSmem {
   float dsum[2][kTileM];
   KeepBits<DROP> keep;
   uint64_t kv_full, q_full[kQStages], q_empty[kQStages], dy_full[2], dy_empty[2], stat_full[2];
-  uint64_t s_full[2], s_loaded, dp_full, pds_full, pds_free, mma_done, mma_drain;
+  // per-region barriers where the two issuers hand off, so that no waiter
+  // can be a full phase behind
+  uint64_t s_full[2], s_loaded, dp_full, pds_full[2], region_free[2], mma_done, drain_sdp, drain_kv;
   uint32_t tmem_base;
 };
 constexpr size_t kMaxSmem = 232448;
@@ -61,7 +66,7 @@ static_assert(sizeof(DkvSmem<128, true>) + 1024 <= kMaxSmem, "shared memory budg
 template <int D, bool DROP>
 constexpr bool kDkvSlack = sizeof(DkvSmem<D, DROP>) + 1024 <= kMaxSmem;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kComputeThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColDV = 256;
@@ -122,10 +127,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&s.s_loaded, kComputeThreads);
     mbar_init(&s.dp_full, 1);
-    mbar_init(&s.pds_full, kComputeThreads);
-    mbar_init(&s.pds_free, 1);
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(&s.pds_full[r], kComputeThreads);
+      mbar_init(&s.region_free[r], 1);
+    }
     mbar_init(&s.mma_done, 1);
-    mbar_init(&s.mma_drain, 1);
+    mbar_init(&s.drain_sdp, 1);
+    mbar_init(&s.drain_kv, 1);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -212,7 +220,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------- tcgen05 issuer --
     if (lane == 0 && n_q > 0) {
       constexpr uint32_t kIdT = idesc_bf16_f32(kTileN, kTileM, false, false);  // S^T, dP^T
-      constexpr uint32_t kIdKV = idesc_bf16_f32(kTileN, D, false, true);       // dV, dK (A = P^T / dS^T in TMEM)
       const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
       auto issue_ss = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {  // 128 x 128 x D, both K-major
 #pragma unroll
@@ -229,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&s.s_full[0]);
       }
       for (int it = 0; ok && it < n_q; ++it) {
-        const int st = it & 1, qs = it % kQS;
+        const int st = it & 1;
         // dP^T(it) over S^T(it), once every compute thread has read S^T(it)
         if (!mbar_wait(&s.s_loaded, it & 1, a.err, kErrBwdMma)) break;
         if (!mbar_wait(&s.dy_full[st], (it >> 1) & 1, a.err, kErrBwdMma)) break;
@@ -238,17 +245,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&s.dp_full);
         if (it + 1 < n_q) {
           // S^T(it+1) into the other region, once dK(it-1) has read it
-          if (it >= 1 && !mbar_wait(&s.pds_free, (it - 1) & 1, a.err, kErrBwdMma)) break;
+          if (it >= 1 && !mbar_wait(&s.region_free[(it - 1) & 1], ((it - 1) >> 1) & 1, a.err, kErrBwdMma)) break;
           const int nq = (it + 1) % kQS;
           if (!mbar_wait(&s.q_full[nq], ((it + 1) / kQS) & 1, a.err, kErrBwdMma)) break;
           tc_fence_after_sync();
           issue_ss(region(it + 1), k_addr, smem_u32(s.q[nq]));
           umma_commit(&s.s_full[(it + 1) & 1]);
         }
+      }
+      umma_commit(&s.drain_sdp);
+      mbar_wait_drain(&s.drain_sdp, 0);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------- dV / dK issuer --
+    if (lane == 0 && n_q > 0) {
+      constexpr uint32_t kIdKV = idesc_bf16_f32(kTileN, D, false, true);  // A = P^T / dS^T in TMEM
+      for (int it = 0; it < n_q; ++it) {
+        const int st = it & 1, qs = it % kQS;
         // dV, dK from the P^T / dS^T the compute warps stored in region(it):
         // query columns [64h, 64h+64) of the tile hold P^T in columns
         // [64h, 64h+32) and dS^T in [64h+32, 64h+64), two bf16 per column
-        if (!mbar_wait(&s.pds_full, it & 1, a.err, kErrBwdMma)) break;
+        if (!mbar_wait(&s.pds_full[st], (it >> 1) & 1, a.err, kErrBwdMma)) break;
         tc_fence_after_sync();
         const uint32_t ra = tmem + region(it);
         const uint32_t dy_addr = smem_u32(s.dy[st]), q_addr = smem_u32(s.q[qs]);
@@ -256,17 +273,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kTileM / 16; ++kk)  // dV += P^T dY  (K dim = query rows)
           umma_bf16_ts(tmem + kColDV, ra + (kk >> 2) * 64 + (kk & 3) * 8,
                        sdesc_sw128(dy_addr + kk * 2048, kAtomBytes, 1024), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&s.dy_empty[st]);
+        umma_commit(&s.dy_empty[st]);  // dP^T(it) read dY(it) too; it finished before P^T(it) existed
 #pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk)  // dK += dS^T Q
           umma_bf16_ts(tmem + kColDK, ra + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
                        sdesc_sw128(q_addr + kk * 2048, kAtomBytes, 1024), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&s.q_empty[qs]);
-        umma_commit(&s.pds_free);
+        umma_commit(&s.q_empty[qs]);  // likewise S^T(it) for Q(it)
+        umma_commit(&s.region_free[st]);
         if (it == n_q - 1) umma_commit(&s.mma_done);
       }
-      umma_commit(&s.mma_drain);
-      mbar_wait_drain(&s.mma_drain, 0);
+      umma_commit(&s.drain_kv);
+      mbar_wait_drain(&s.drain_kv, 0);
     }
   } else {
     // ------------------------------------------- compute warps (0..7) -----
@@ -305,18 +322,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait(s1);
         tc_fence_before_sync();
         mbar_arrive(&s.s_loaded);  // region(it) may now receive dP^T(it)
+        // Two copies of the loop: tiles entirely inside the window (nearly
+        // all of them) need no per-element mask.  In the masked copy the
+        // exp2 is unconditional and the comparisons use non-short-circuit
+        // operators, so the mask compiles to selects, not branches.
+        if (full) {
 #pragma unroll
-        for (int t4 = 0; t4 < 16; ++t4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[st][cbase + t4 * 4]);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          for (int t4 = 0; t4 < 16; ++t4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[st][cbase + t4 * 4]);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int t = t4 * 4 + u;
-            const int i = i0 + cbase + t;
-            const bool vis = full || (i >= qlo && i <= qhi);
-            const float sv = __uint_as_float(t < 32 ? s0[t] : s1[t - 32]);
-            const float e = ex2_approx(sv * c - lv[u]);  // unconditional: a select, not a branch
-            p[t] = vis ? e : 0.f;
+            for (int u = 0; u < 4; ++u) {
+              const int t = t4 * 4 + u;
+              p[t] = ex2_approx(__uint_as_float(t < 32 ? s0[t] : s1[t - 32]) * c - lv[u]);
+            }
+          }
+        } else {
+          const int lo_t = qlo - (i0 + cbase), hi_t = qhi - (i0 + cbase);  // visible t in [lo_t, hi_t]
+#pragma unroll
+          for (int t4 = 0; t4 < 16; ++t4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[st][cbase + t4 * 4]);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int t = t4 * 4 + u;
+              const float e = ex2_approx(__uint_as_float(t < 32 ? s0[t] : s1[t - 32]) * c - lv[u]);
+              p[t] = ((t >= lo_t) & (t <= hi_t)) ? e : 0.f;
+            }
           }
         }
       }
@@ -358,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_32x32b_x32(col + 32, dk);
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&s.pds_full);
+      mbar_arrive(&s.pds_full[st]);
     }
     if (ok && n_q > 0) ok = compute_wait(&s.mma_done, 0, a.err);  // every MMA done
     if (ok) {

@@ -13,8 +13,13 @@
 //   warps 0-7  compute: warp w owns TMEM lanes 32*(w%4).. (query rows) and key
 //              columns 64*(w/4).. of each tile; in the epilogue, dQ columns
 //              [w/4 * D/2, +D/2)
-//   warp  8    TMA producer: Q, dY once; K, V through a 2-stage ring
-//   warp  9    tcgen05 issuer
+//   warp  8    TMA producer: Q, dY once; K through a 3-stage ring (a K tile
+//              is read by S and, last, by dQ) and V through a 2-stage ring
+//              (read by dP only, so it is released early)
+//   warp  9    tcgen05 issuer of S and dP (both SS)
+//   warp 10    tcgen05 issuer of dQ += dS K (TS)
+// Two issuing threads keep the tensor pipe fed: its queue is shallow, so
+// every barrier wait of a single issuer between GEMMs left it idle.
 // TMEM columns: two S/dP buffers [0,128) and [128,256) (S is read into
 // registers, then dP is written over it), dQ [256,256+D), and two bf16 dS
 // buffers [384,448), [448,512) that the dQ MMA reads as its A operand.
@@ -30,15 +35,15 @@ struct DqSmem {
   static constexpr int kTileBytes = kTileM * D * 2;
   alignas(1024) uint8_t q[kTileBytes];
   alignas(1024) uint8_t dy[kTileBytes];
-  alignas(1024) uint8_t k[2][kTileBytes];
+  alignas(1024) uint8_t k[3][kTileBytes];
   alignas(1024) uint8_t v[2][kTileBytes];
-  uint64_t qdy_full, k_full[2], v_full[2], kv_empty[2];
-  uint64_t s_full[2], s_loaded[2], dp_full[2], dp_loaded[2], ds_full[2], ds_free[2], mma_drain;
+  uint64_t qdy_full, k_full[3], k_empty[3], v_full[2], v_empty[2];
+  uint64_t s_full[2], s_loaded[2], dp_full[2], dp_loaded[2], ds_full[2], ds_free[2], drain_sdp, drain_dq;
   uint32_t tmem_base;
 };
 static_assert(sizeof(DqSmem<128>) + 1024 <= 232448, "shared memory budget");
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kComputeThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColDQ = 256, kColDS = 384;  // dS buffer b at kColDS + 64*b
@@ -79,10 +84,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&s.qdy_full, 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 3; ++b) {
       mbar_init(&s.k_full[b], 1);
+      mbar_init(&s.k_empty[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&s.v_full[b], 1);
-      mbar_init(&s.kv_empty[b], 1);
+      mbar_init(&s.v_empty[b], 1);
       mbar_init(&s.s_full[b], 1);
       mbar_init(&s.s_loaded[b], kComputeThreads);
       mbar_init(&s.dp_full[b], 1);
@@ -92,7 +100,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.ds_full[b], kComputeThreads);
       mbar_init(&s.ds_free[b], 1);
     }
-    mbar_init(&s.mma_drain, 1);
+    mbar_init(&s.drain_sdp, 1);
+    mbar_init(&s.drain_dq, 1);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -114,36 +123,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&s.qdy_full, 2 * kTileBytes);
       tma_rows<D>(s.q, &mq, &s.qdy_full, g, w.b, w.n, sq.q_start, q0);
       tma_rows<D>(s.dy, &mdy, &s.qdy_full, g, w.b, w.n, sq.q_start, q0);
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_kv; ++j) {
-        const int b = j & 1;
-        if (j >= 2 && !mbar_wait(&s.kv_empty[b], ((j >> 1) - 1) & 1, a.err, kErrBwdLoad)) break;
         const int jr = (kv_t0 + j) * kTileN;
-        mbar_arrive_expect_tx(&s.k_full[b], kTileBytes);
-        tma_rows<D>(s.k[b], &mk, &s.k_full[b], g, w.b, w.n, sq.kv_start, jr);
-        mbar_arrive_expect_tx(&s.v_full[b], kTileBytes);
-        tma_rows<D>(s.v[b], &mv, &s.v_full[b], g, w.b, w.n, sq.kv_start, jr);
-        ++issued;
+        const int kb = j % 3, vb = j & 1;
+        // K(j) reuses the stage of K(j-3), free once dQ(j-3) is done
+        if (j >= 3 && !mbar_wait(&s.k_empty[kb], ((j / 3) - 1) & 1, a.err, kErrBwdLoad)) break;
+        mbar_arrive_expect_tx(&s.k_full[kb], kTileBytes);
+        tma_rows<D>(s.k[kb], &mk, &s.k_full[kb], g, w.b, w.n, sq.kv_start, jr);
+        ++k_issued;
+        // V(j) reuses the stage of V(j-2), free once dP(j-2) is done
+        if (j >= 2 && !mbar_wait(&s.v_empty[vb], ((j >> 1) - 1) & 1, a.err, kErrBwdLoad)) break;
+        mbar_arrive_expect_tx(&s.v_full[vb], kTileBytes);
+        tma_rows<D>(s.v[vb], &mv, &s.v_full[vb], g, w.b, w.n, sq.kv_start, jr);
+        ++v_issued;
       }
       // every copy issued has landed before the CTA may exit
       mbar_wait_drain(&s.qdy_full, 0);
+      for (int b = 0; b < 3; ++b) {
+        const int uses = (k_issued - b + 2) / 3;
+        if (uses > 0) mbar_wait_drain(&s.k_full[b], (uses - 1) & 1);
+      }
       for (int b = 0; b < 2; ++b) {
-        const int uses = (issued - b + 1) / 2;
-        if (uses > 0) {
-          mbar_wait_drain(&s.k_full[b], (uses - 1) & 1);
-          mbar_wait_drain(&s.v_full[b], (uses - 1) & 1);
-        }
+        const int uses = (v_issued - b + 1) / 2;
+        if (uses > 0) mbar_wait_drain(&s.v_full[b], (uses - 1) & 1);
       }
     }
   } else if (warp == 9) {
     // ----------------------------------------------------- tcgen05 issuer --
     if (lane == 0 && n_kv > 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kTileM, kTileN, false, false);  // S, dP
-      constexpr uint32_t kIdQ = idesc_bf16_f32(kTileM, D, false, true);        // dQ
       const uint32_t q_addr = smem_u32(s.q), dy_addr = smem_u32(s.dy);
       auto issue_s = [&](int j) {  // S(j) = Q K_j^T into buffer j % 2
         const int b = j & 1;
-        const uint32_t k_addr = smem_u32(s.k[b]);
+        const uint32_t k_addr = smem_u32(s.k[j % 3]);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
@@ -161,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = j & 1;
         const uint32_t u = (j >> 1) & 1;
         if (!mbar_wait(&s.s_loaded[b], u, a.err, kErrBwdMma)) break;
-        if (!mbar_wait(&s.v_full[b], u, a.err, kErrBwdMma)) break;
+        if (!mbar_wait(&s.v_full[b], u, a.err, kErrBwdMma)) break;  // V stage j % 2 == b
         tc_fence_after_sync();
         const uint32_t v_addr = smem_u32(s.v[b]);
 #pragma unroll
@@ -171,25 +184,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                        kIdS, kk > 0);
         }
         umma_commit(&s.dp_full[b]);
+        umma_commit(&s.v_empty[b]);
         if (j + 1 < n_kv) {  // S(j+1) into the other buffer, once its dP(j-1) was read
           const int nb = (j + 1) & 1;
           if (j + 1 >= 2 && !mbar_wait(&s.dp_loaded[nb], (((j + 1) >> 1) - 1) & 1, a.err, kErrBwdMma)) break;
-          if (!mbar_wait(&s.k_full[nb], ((j + 1) >> 1) & 1, a.err, kErrBwdMma)) break;
+          if (!mbar_wait(&s.k_full[(j + 1) % 3], ((j + 1) / 3) & 1, a.err, kErrBwdMma)) break;
           tc_fence_after_sync();
           issue_s(j + 1);
         }
-        if (!mbar_wait(&s.ds_full[b], u, a.err, kErrBwdMma)) break;
+      }
+      umma_commit(&s.drain_sdp);
+      mbar_wait_drain(&s.drain_sdp, 0);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------ dQ += dS K issuer --
+    if (lane == 0 && n_kv > 0) {
+      constexpr uint32_t kIdQ = idesc_bf16_f32(kTileM, D, false, true);
+      for (int j = 0; j < n_kv; ++j) {
+        const int b = j & 1;
+        if (!mbar_wait(&s.ds_full[b], (j >> 1) & 1, a.err, kErrBwdMma)) break;
         tc_fence_after_sync();
-        const uint32_t k_addr = smem_u32(s.k[b]);
+        const uint32_t k_addr = smem_u32(s.k[j % 3]);
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)  // dQ += dS(j) K_j  (A = dS in TMEM, K dim = keys)
           umma_bf16_ts(tmem + kColDQ, tmem + kColDS + b * 64 + kk * 8,
                        sdesc_sw128(k_addr + kk * 2048, kAtomBytes, 1024), kIdQ, (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&s.ds_free[b]);
-        umma_commit(&s.kv_empty[b]);
+        // K(j) was also read by S(j), which finished before dS(j) existed
+        umma_commit(&s.k_empty[j % 3]);
       }
-      umma_commit(&s.mma_drain);
-      mbar_wait_drain(&s.mma_drain, 0);
+      umma_commit(&s.drain_dq);
+      mbar_wait_drain(&s.drain_dq, 0);
     }
   } else {
     // ------------------------------------------- compute warps (0..7) -----
@@ -240,13 +265,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait(s1);
         tc_fence_before_sync();
         mbar_arrive(&s.s_loaded[b]);
+        // Two copies of the loop: tiles entirely inside the window (nearly
+        // all of them) need no per-element mask.  In the masked copy the
+        // exp2 is unconditional and the comparisons use non-short-circuit
+        // operators, so the mask compiles to selects, not branches.
+        if (full) {
 #pragma unroll
-        for (int t = 0; t < 64; ++t) {
-          const int jj = jb + cbase + t;
-          const bool vis = full || (jj >= wlo && jj <= whi);
-          const float sv = __uint_as_float(t < 32 ? s0[t] : s1[t - 32]);
-          const float e = ex2_approx(sv * c - lse2);  // unconditional: a select, not a branch
-          p[t] = vis ? e : 0.f;
+          for (int t = 0; t < 64; ++t)
+            p[t] = ex2_approx(__uint_as_float(t < 32 ? s0[t] : s1[t - 32]) * c - lse2);
+        } else {
+          const int lo_t = wlo - (jb + cbase), hi_t = whi - (jb + cbase);  // visible t in [lo_t, hi_t]
+#pragma unroll
+          for (int t = 0; t < 64; ++t) {
+            const float e = ex2_approx(__uint_as_float(t < 32 ? s0[t] : s1[t - 32]) * c - lse2);
+            p[t] = ((t >= lo_t) & (t <= hi_t)) ? e : 0.f;
+          }
         }
       }
       // ---- dP -> dS (packed bf16)

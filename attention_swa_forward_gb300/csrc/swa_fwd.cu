@@ -11,8 +11,12 @@
 //   warps 0-3  softmax + epilogue, one thread per query row (TMEM lane)
 //   warp  4    TMA producer: Q once; K and V through separate 3-stage rings
 //              (a K stage is released as soon as its S is computed)
-//   warp  5    tcgen05 issuer: S = Q K^T into a double-buffered TMEM tile,
-//              then O += P V with P (bf16) taken from TMEM as the A operand
+//   warp  5    tcgen05 issuer of S = Q K^T into a double-buffered TMEM tile
+//   warp  6    tcgen05 issuer of O += P V, P (bf16) taken from TMEM as the
+//              A operand
+// Two issuing threads keep the tensor pipe fed: its queue is shallow, so
+// every barrier wait of a single issuer between GEMMs left it idle; with two,
+// one waits while the other's GEMM runs.
 // TMEM columns: S0 [0,128), S1 [128,256), O [256,256+D), P0 [384,448),
 // P1 [448,512).
 #include "swa_device.cuh"
@@ -29,7 +33,7 @@ struct FwdSmem {
   alignas(1024) uint8_t k[kStages][kTileBytes];
   alignas(1024) uint8_t v[kStages][kTileBytes];
   uint64_t q_full, k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
-  uint64_t s_full[2], s_free[2], p_full[2], o_done, mma_drain;
+  uint64_t s_full[2], s_free[2], p_full[2], o_done, drain_s, drain_pv;
   uint32_t tmem_base;
 };
 static_assert(sizeof(FwdSmem<128>) + 1024 <= 232448, "shared memory budget");
@@ -42,7 +46,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
 
 template <int D, bool DROP, int CAP>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     swa_fwd_kernel(const FwdArgs a, const __grid_constant__ SeqTable<CAP> tab, const __grid_constant__ CUtensorMap mq,
                    const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
   extern __shared__ uint8_t smem_raw[];
@@ -81,7 +85,8 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&s.p_full[i], kTileM);
     }
     mbar_init(&s.o_done, 1);
-    mbar_init(&s.mma_drain, 1);
+    mbar_init(&s.drain_s, 1);
+    mbar_init(&s.drain_pv, 1);
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -124,13 +129,17 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else if (warp == 5) {
-    // ----------------------------------------------------- tcgen05 issuer --
+    // ------------------------------------------------ S = Q K^T issuer --
     if (lane == 0 && n_kv > 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kTileM, kTileN, false, false);
-      constexpr uint32_t kIdO = idesc_bf16_f32(kTileM, D, false, true);
       const uint32_t q_addr = smem_u32(s.q);
-      auto issue_s = [&](int it) {  // S(it) = Q K_it^T into S buffer it % 2
+      bool ok = mbar_wait(&s.q_full, 0, a.err, kErrFwdMma);
+      for (int it = 0; ok && it < n_kv; ++it) {
         const int st = it % kStages, sb = it & 1;
+        // S buffer sb was last read by the softmax of tile it - 2
+        if (it >= 2 && !mbar_wait(&s.s_free[sb], ((it >> 1) - 1) & 1, a.err, kErrFwdMma)) break;
+        if (!mbar_wait(&s.k_full[st], (it / kStages) & 1, a.err, kErrFwdMma)) break;
+        tc_fence_after_sync();
         const uint32_t k_addr = smem_u32(s.k[st]);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -140,20 +149,15 @@ __global__ void __launch_bounds__(192, 1)
         }
         umma_commit(&s.s_full[sb]);
         umma_commit(&s.k_empty[st]);
-      };
-      bool ok = mbar_wait(&s.q_full, 0, a.err, kErrFwdMma) && mbar_wait(&s.k_full[0], 0, a.err, kErrFwdMma);
-      if (ok) {
-        tc_fence_after_sync();
-        issue_s(0);
       }
-      for (int it = 0; ok && it < n_kv; ++it) {
-        if (it + 1 < n_kv) {  // next S while softmax(it) runs
-          const int nt = it + 1, nsb = nt & 1;
-          if (nt >= 2 && !mbar_wait(&s.s_free[nsb], ((nt >> 1) - 1) & 1, a.err, kErrFwdMma)) break;
-          if (!mbar_wait(&s.k_full[nt % kStages], (nt / kStages) & 1, a.err, kErrFwdMma)) break;
-          tc_fence_after_sync();
-          issue_s(nt);
-        }
+      umma_commit(&s.drain_s);
+      mbar_wait_drain(&s.drain_s, 0);
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------- O += P V issuer --
+    if (lane == 0 && n_kv > 0) {
+      constexpr uint32_t kIdO = idesc_bf16_f32(kTileM, D, false, true);
+      for (int it = 0; it < n_kv; ++it) {
         const int pb = it & 1, st = it % kStages;
         if (!mbar_wait(&s.p_full[pb], (it >> 1) & 1, a.err, kErrFwdMma)) break;
         if (!mbar_wait(&s.v_full[st], (it / kStages) & 1, a.err, kErrFwdMma)) break;
@@ -166,8 +170,8 @@ __global__ void __launch_bounds__(192, 1)
         umma_commit(&s.o_done);
         umma_commit(&s.v_empty[st]);
       }
-      umma_commit(&s.mma_drain);
-      mbar_wait_drain(&s.mma_drain, 0);
+      umma_commit(&s.drain_pv);
+      mbar_wait_drain(&s.drain_pv, 0);
     }
   } else {
     // ------------------------------------------ softmax + epilogue (rows) --
@@ -227,7 +231,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int t = 0; t < kTileN; ++t) {
           const int j = j0 + t;
-          x[t] = (j >= wlo && j <= whi) ? x[t] * c : -INFINITY;
+          x[t] = ((j >= wlo) & (j <= whi)) ? x[t] * c : -INFINITY;  // selects, not branches
           m8[t & 7] = fmaxf(m8[t & 7], x[t]);
         }
       }
@@ -346,7 +350,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, const SeqTable<CAP>& tab, const CUten
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  swa_fwd_kernel<D, DROP, CAP><<<tab.n_items, 192, smem, stream>>>(a, tab, mq, mk, mv);
+  swa_fwd_kernel<D, DROP, CAP><<<tab.n_items, 224, smem, stream>>>(a, tab, mq, mk, mv);
   return cudaGetLastError();
 }
 
