@@ -20,11 +20,11 @@
 //   warp 10    tcgen05 issuer of dQ += dS K (TS)
 // Two issuing threads keep the tensor pipe fed: its queue is shallow, so
 // every barrier wait of a single issuer between GEMMs left it idle.
-// TMEM columns: two S/dP buffers [0,128) and [128,256) (S is read into
-// registers, then dP is written over it), dQ [256,256+D), and two bf16 dS
+// TMEM columns: S [0,128), dP [128,256), dQ [256,256+D), and two bf16 dS
 // buffers [384,448), [448,512) that the dQ MMA reads as its A operand.
-// Issue order per key tile j: dP(j) (once S(j) is in registers), S(j+1) into
-// the other buffer, dQ(j) (once dS(j) is in TMEM).
+// S(j+1) is issued as soon as the compute warps hold S(j) in registers and
+// dP(j+1) as soon as they hold dP(j), so both are ready before the compute
+// warps reach them; dQ(j) follows dS(j).
 #include "swa_device.cuh"
 
 namespace swa {
@@ -38,7 +38,7 @@ struct DqSmem {
   alignas(1024) uint8_t k[3][kTileBytes];
   alignas(1024) uint8_t v[2][kTileBytes];
   uint64_t qdy_full, k_full[3], k_empty[3], v_full[2], v_empty[2];
-  uint64_t s_full[2], s_loaded[2], dp_full[2], dp_loaded[2], ds_full[2], ds_free[2], drain_sdp, drain_dq;
+  uint64_t s_full, s_loaded, dp_full, dp_loaded, ds_full[2], ds_free[2], drain_sdp, drain_dq;
   uint32_t tmem_base;
 };
 static_assert(sizeof(DqSmem<128>) + 1024 <= 232448, "shared memory budget");
@@ -46,7 +46,7 @@ static_assert(sizeof(DqSmem<128>) + 1024 <= 232448, "shared memory budget");
 constexpr int kThreads = 352;
 constexpr int kComputeThreads = 256;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColDQ = 256, kColDS = 384;  // dS buffer b at kColDS + 64*b
+constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384;  // dS buffer b at kColDS + 64*b
 
 // Warp-uniform bounded wait of the compute warps.  A warp vote (not a
 // CTA-wide barrier) keeps each warp converged for its warp-collective TMEM
@@ -91,15 +91,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s.v_full[b], 1);
       mbar_init(&s.v_empty[b], 1);
-      mbar_init(&s.s_full[b], 1);
-      mbar_init(&s.s_loaded[b], kComputeThreads);
-      mbar_init(&s.dp_full[b], 1);
-      mbar_init(&s.dp_loaded[b], kComputeThreads);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s.ds_full[b], kComputeThreads);
       mbar_init(&s.ds_free[b], 1);
     }
+    mbar_init(&s.s_full, 1);
+    mbar_init(&s.s_loaded, kComputeThreads);
+    mbar_init(&s.dp_full, 1);
+    mbar_init(&s.dp_loaded, kComputeThreads);
     mbar_init(&s.drain_sdp, 1);
     mbar_init(&s.drain_dq, 1);
     fence_mbar_init();
@@ -154,44 +154,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_kv > 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kTileM, kTileN, false, false);  // S, dP
       const uint32_t q_addr = smem_u32(s.q), dy_addr = smem_u32(s.dy);
-      auto issue_s = [&](int j) {  // S(j) = Q K_j^T into buffer j % 2
-        const int b = j & 1;
+      auto issue_s = [&](int j) {  // S(j) = Q K_j^T
         const uint32_t k_addr = smem_u32(s.k[j % 3]);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-          umma_bf16_ss(tmem + b * 128, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                       kIdS, kk > 0);
+          umma_bf16_ss(tmem + kColS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), kIdS,
+                       kk > 0);
         }
-        umma_commit(&s.s_full[b]);
+        umma_commit(&s.s_full);
       };
+      auto issue_dp = [&](int j) {  // dP(j) = dY V_j^T
+        const uint32_t v_addr = smem_u32(s.v[j & 1]);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
+          umma_bf16_ss(tmem + kColDP, sdesc_sw128(dy_addr + off, 16, 1024), sdesc_sw128(v_addr + off, 16, 1024), kIdS,
+                       kk > 0);
+        }
+        umma_commit(&s.dp_full);
+        umma_commit(&s.v_empty[j & 1]);
+      };
+      // S(j+1) may be issued once the compute warps hold S(j) in registers,
+      // dP(j+1) once they hold dP(j): neither waits for the other's consumer.
       bool ok = mbar_wait(&s.qdy_full, 0, a.err, kErrBwdMma) && mbar_wait(&s.k_full[0], 0, a.err, kErrBwdMma);
       if (ok) {
         tc_fence_after_sync();
         issue_s(0);
+        ok = mbar_wait(&s.v_full[0], 0, a.err, kErrBwdMma);
       }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int b = j & 1;
-        const uint32_t u = (j >> 1) & 1;
-        if (!mbar_wait(&s.s_loaded[b], u, a.err, kErrBwdMma)) break;
-        if (!mbar_wait(&s.v_full[b], u, a.err, kErrBwdMma)) break;  // V stage j % 2 == b
+      if (ok) {
         tc_fence_after_sync();
-        const uint32_t v_addr = smem_u32(s.v[b]);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // dP(j) = dY V_j^T over the consumed S(j)
-          const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-          umma_bf16_ss(tmem + b * 128, sdesc_sw128(dy_addr + off, 16, 1024), sdesc_sw128(v_addr + off, 16, 1024),
-                       kIdS, kk > 0);
-        }
-        umma_commit(&s.dp_full[b]);
-        umma_commit(&s.v_empty[b]);
-        if (j + 1 < n_kv) {  // S(j+1) into the other buffer, once its dP(j-1) was read
-          const int nb = (j + 1) & 1;
-          if (j + 1 >= 2 && !mbar_wait(&s.dp_loaded[nb], (((j + 1) >> 1) - 1) & 1, a.err, kErrBwdMma)) break;
-          if (!mbar_wait(&s.k_full[(j + 1) % 3], ((j + 1) / 3) & 1, a.err, kErrBwdMma)) break;
-          tc_fence_after_sync();
-          issue_s(j + 1);
-        }
+        issue_dp(0);
+      }
+      for (int j = 0; ok && j + 1 < n_kv; ++j) {
+        const int n = j + 1;
+        if (!mbar_wait(&s.s_loaded, j & 1, a.err, kErrBwdMma)) break;
+        if (!mbar_wait(&s.k_full[n % 3], (n / 3) & 1, a.err, kErrBwdMma)) break;
+        tc_fence_after_sync();
+        issue_s(n);
+        if (!mbar_wait(&s.dp_loaded, j & 1, a.err, kErrBwdMma)) break;
+        if (!mbar_wait(&s.v_full[n & 1], (n >> 1) & 1, a.err, kErrBwdMma)) break;
+        tc_fence_after_sync();
+        issue_dp(n);
       }
       umma_commit(&s.drain_sdp);
       mbar_wait_drain(&s.drain_sdp, 0);
@@ -254,17 +259,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool full = tile_fully_visible(g, sq, q0, jb);
 
       // ---- S -> P (kept in registers)
-      if (!compute_wait(&s.s_full[b], u, a.err)) { ok = false; break; }
+      if (!compute_wait(&s.s_full, j & 1, a.err)) { ok = false; break; }
       tc_fence_after_sync();
       float p[64];
       {
         uint32_t s0[32], s1[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + b * 128 + cbase, s0);
-        tmem_ld_32x32b_x32(tmem + lane_off + b * 128 + cbase + 32, s1);
+        tmem_ld_32x32b_x32(tmem + lane_off + kColS + cbase, s0);
+        tmem_ld_32x32b_x32(tmem + lane_off + kColS + cbase + 32, s1);
         tmem_ld_wait(s0);
         tmem_ld_wait(s1);
         tc_fence_before_sync();
-        mbar_arrive(&s.s_loaded[b]);
+        mbar_arrive(&s.s_loaded);
         // Two copies of the loop: tiles entirely inside the window (nearly
         // all of them) need no per-element mask.  In the masked copy the
         // exp2 is unconditional and the comparisons use non-short-circuit
@@ -283,17 +288,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // ---- dP -> dS (packed bf16)
-      if (!compute_wait(&s.dp_full[b], u, a.err)) { ok = false; break; }
+      if (!compute_wait(&s.dp_full, j & 1, a.err)) { ok = false; break; }
       tc_fence_after_sync();
       uint32_t dk[32];
       {
         uint32_t d0[32], d1[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + b * 128 + cbase, d0);
-        tmem_ld_32x32b_x32(tmem + lane_off + b * 128 + cbase + 32, d1);
+        tmem_ld_32x32b_x32(tmem + lane_off + kColDP + cbase, d0);
+        tmem_ld_32x32b_x32(tmem + lane_off + kColDP + cbase + 32, d1);
         tmem_ld_wait(d0);
         tmem_ld_wait(d1);
         tc_fence_before_sync();
-        mbar_arrive(&s.dp_loaded[b]);
+        mbar_arrive(&s.dp_loaded);
 #pragma unroll
         for (int t2 = 0; t2 < 32; ++t2) {
           float dv[2];

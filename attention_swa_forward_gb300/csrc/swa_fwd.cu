@@ -33,7 +33,7 @@ struct FwdSmem {
   alignas(1024) uint8_t k[kStages][kTileBytes];
   alignas(1024) uint8_t v[kStages][kTileBytes];
   uint64_t q_full, k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
-  uint64_t s_full[2], s_free[2], p_full[2], o_done, drain_s, drain_pv;
+  uint64_t s_full[2], s_free[2], p_full[2], o_done[2], drain_s, drain_pv;  // o_done[b]: PV of P buffer b
   uint32_t tmem_base;
 };
 static_assert(sizeof(FwdSmem<128>) + 1024 <= 232448, "shared memory budget");
@@ -84,7 +84,8 @@ __global__ void __launch_bounds__(224, 1)
       mbar_init(&s.s_free[i], kTileM);
       mbar_init(&s.p_full[i], kTileM);
     }
-    mbar_init(&s.o_done, 1);
+    mbar_init(&s.o_done[0], 1);
+    mbar_init(&s.o_done[1], 1);
     mbar_init(&s.drain_s, 1);
     mbar_init(&s.drain_pv, 1);
     fence_mbar_init();
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(224, 1)
         for (int kk = 0; kk < kTileN / 16; ++kk)  // O += P V  (A = P in TMEM)
           umma_bf16_ts(tmem + kColO, tmem + kColP + pb * 64 + kk * 8, sdesc_sw128(v_addr + kk * 2048, kAtomBytes, 1024),
                        kIdO, (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&s.o_done);
+        umma_commit(&s.o_done[pb]);
         umma_commit(&s.v_empty[st]);
       }
       umma_commit(&s.drain_pv);
@@ -192,51 +193,52 @@ __global__ void __launch_bounds__(224, 1)
         break;
       }
       tc_fence_after_sync();
-      float x[kTileN];
+      // the row's 128 scores, loaded in place (xr holds fp32 bits, later the bf16 P pairs)
+      uint32_t xr[kTileN];
       {
-        // all four loads in flight before the one wait
-        uint32_t t0[32], t1[32], t2[32], t3[32];
+        uint32_t(&x0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&xr[0]);
+        uint32_t(&x1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&xr[32]);
+        uint32_t(&x2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&xr[64]);
+        uint32_t(&x3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&xr[96]);
         const uint32_t base = tmem + lane_off + sb * kTileN;
-        tmem_ld_32x32b_x32(base + 0, t0);
-        tmem_ld_32x32b_x32(base + 32, t1);
-        tmem_ld_32x32b_x32(base + 64, t2);
-        tmem_ld_32x32b_x32(base + 96, t3);
-        tmem_ld_wait(t0);
-        tmem_ld_wait(t1);
-        tmem_ld_wait(t2);
-        tmem_ld_wait(t3);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          x[t] = __uint_as_float(t0[t]);
-          x[32 + t] = __uint_as_float(t1[t]);
-          x[64 + t] = __uint_as_float(t2[t]);
-          x[96 + t] = __uint_as_float(t3[t]);
-        }
+        tmem_ld_32x32b_x32(base + 0, x0);  // all four loads in flight before the one wait
+        tmem_ld_32x32b_x32(base + 32, x1);
+        tmem_ld_32x32b_x32(base + 64, x2);
+        tmem_ld_32x32b_x32(base + 96, x3);
+        tmem_ld_wait(x0);
+        tmem_ld_wait(x1);
+        tmem_ld_wait(x2);
+        tmem_ld_wait(x3);
       }
       tc_fence_before_sync();
       mbar_arrive(&s.s_free[sb]);
+      auto X = [&](int t) -> float { return __uint_as_float(xr[t]); };
 
       const int j0 = (kv_t0 + it) * kTileN;
-      // eight independent partial maxima: no 128-long dependency chain
-      float m8[8];
+      // Fast path (tiles inside the window, positive scale): the maximum is
+      // taken on the raw scores and the scale folds into one packed FMA per
+      // pair, p = exp2(x*c - m).  Otherwise scale, mask, then exp2(x - m).
+      const bool fast = tile_fully_visible(g, sq, q0, j0) && c > 0.f;
+      float mx;
+      {
+        float m8[8];  // eight independent partial maxima: no long dependency chain
 #pragma unroll
-      for (int u = 0; u < 8; ++u) m8[u] = -INFINITY;
-      if (tile_fully_visible(g, sq, q0, j0)) {
+        for (int u = 0; u < 8; ++u) m8[u] = -INFINITY;
+        if (fast) {
 #pragma unroll
-        for (int t = 0; t < kTileN; ++t) {
-          x[t] *= c;
-          m8[t & 7] = fmaxf(m8[t & 7], x[t]);
+          for (int t = 0; t < kTileN; t += 2) m8[(t >> 1) & 7] = fmax3(m8[(t >> 1) & 7], X(t), X(t + 1));
+        } else {
+          const int lo_t = wlo - j0, hi_t = whi - j0;  // visible t in [lo_t, hi_t]
+#pragma unroll
+          for (int t = 0; t < kTileN; ++t) {
+            const float v = ((t >= lo_t) & (t <= hi_t)) ? X(t) * c : -INFINITY;  // selects, not branches
+            xr[t] = __float_as_uint(v);
+            m8[t & 7] = fmaxf(m8[t & 7], v);
+          }
         }
-      } else {
-#pragma unroll
-        for (int t = 0; t < kTileN; ++t) {
-          const int j = j0 + t;
-          x[t] = ((j >= wlo) & (j <= whi)) ? x[t] * c : -INFINITY;  // selects, not branches
-          m8[t & 7] = fmaxf(m8[t & 7], x[t]);
-        }
+        mx = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], fmax3(m8[5], m8[6], m8[7])));
+        if (fast) mx *= c;
       }
-      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       const float m_new = fmaxf(m_true, mx);
       m_true = m_new;
       const bool need = m_new > m_use + kRescaleThreshold;
@@ -247,38 +249,52 @@ __global__ void __launch_bounds__(224, 1)
         m_use = m_new;
       }
       const float msub = (m_use == -INFINITY) ? 0.f : m_use;
+      uint32_t bits[4] = {~0u, ~0u, ~0u, ~0u};
+      if (DROP) {
+        bits[0] = bits[1] = bits[2] = bits[3] = 0u;
+        if (row_valid) load_keep_bits(a.mask, sq, w.n, i, j0, bits);
+      }
+      // p = exp2(.), the row sum of p (before dropout), then P = p*z packed
+      // to bf16 pairs in place: xr[t/2] receives the pair (t, t+1)
       float r8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) r8[u] = 0.f;
 #pragma unroll
-      for (int t = 0; t < kTileN; ++t) {
-        x[t] = ex2_approx(x[t] - msub);
-        r8[t & 7] += x[t];
+      for (int t = 0; t < kTileN; t += 2) {
+        float p0, p1;
+        if (fast) {
+          ffma2_bcast(p0, p1, X(t), X(t + 1), c, -msub);
+        } else {
+          p0 = X(t) - msub;
+          p1 = X(t + 1) - msub;
+        }
+        p0 = ex2_approx(p0);
+        p1 = ex2_approx(p1);
+        fadd2_acc(r8[(t >> 1) & 3], r8[4 + ((t >> 1) & 3)], p0, p1);
+        if (DROP) {
+          p0 = ((bits[t >> 5] >> (t & 31)) & 1u) ? p0 : 0.f;
+          p1 = ((bits[(t + 1) >> 5] >> ((t + 1) & 31)) & 1u) ? p1 : 0.f;
+        }
+        xr[t >> 1] = pack_bf16x2(p0, p1);
       }
       const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
       l = l * alpha + rs;
-      if (DROP) {
-        uint32_t bits[4] = {0u, 0u, 0u, 0u};
-        if (row_valid) load_keep_bits(a.mask, sq, w.n, i, j0, bits);
-#pragma unroll
-        for (int t = 0; t < kTileN; ++t)
-          if (!((bits[t >> 5] >> (t & 31)) & 1u)) x[t] = 0.f;
+      // P buffer (it & 1) was last read by PV(it-2).  Only a warp that must
+      // rescale its rows of O also waits for PV(it-1); the others write P(it)
+      // while PV(it-1) may still run, so the tensor pipe never waits for the
+      // softmax's hand-off in the common case.
+      if (it >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait(&s.o_done[sb], ((it >> 1) - 1) & 1, a.err, kErrFwdSoftmax))) {
+        ok = false;
+        break;
       }
-      uint32_t pk0[32], pk1[32];
-#pragma unroll
-      for (int t = 0; t < 32; ++t) {
-        pk0[t] = pack_bf16x2(x[2 * t], x[2 * t + 1]);
-        pk1[t] = pack_bf16x2(x[64 + 2 * t], x[64 + 2 * t + 1]);
-      }
-      // PV(it-1) must be done before O is rescaled; it also frees P buffer
-      // (it & 1), last read by PV(it-2).
-      if (it >= 1) {
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&s.o_done, (it - 1) & 1, a.err, kErrFwdSoftmax))) {
+      tc_fence_after_sync();
+      if (it >= 1 && warp_need) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&s.o_done[sb ^ 1], ((it - 1) >> 1) & 1, a.err, kErrFwdSoftmax))) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        if (warp_need) {
+        {
 #pragma unroll
           for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t t32[32];
@@ -291,14 +307,14 @@ __global__ void __launch_bounds__(224, 1)
           }
         }
       }
-      tmem_st_32x32b_x32(tmem + lane_off + kColP + sb * 64, pk0);
-      tmem_st_32x32b_x32(tmem + lane_off + kColP + sb * 64 + 32, pk1);
+      tmem_st_32x32b_x32(tmem + lane_off + kColP + sb * 64, *reinterpret_cast<const uint32_t(*)[32]>(&xr[0]));
+      tmem_st_32x32b_x32(tmem + lane_off + kColP + sb * 64 + 32, *reinterpret_cast<const uint32_t(*)[32]>(&xr[32]));
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(&s.p_full[sb]);
     }
     if (ok && n_kv > 0) {
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s.o_done, (n_kv - 1) & 1, a.err, kErrFwdSoftmax));
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s.o_done[(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1, a.err, kErrFwdSoftmax));
       tc_fence_after_sync();
     }
     if (ok) {
