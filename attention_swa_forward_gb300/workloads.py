@@ -39,9 +39,14 @@ class Geometry:
     next_tokens: int = INT32_MAX
     sparse_mode: int = 0
     keep_prob: float = 1.0
+    N_kv: int = 0  # key/value heads (grouped-query attention); 0 means N
 
     def as_dict(self) -> dict:
         return asdict(self)
+
+    @property
+    def n_kv(self) -> int:
+        return self.N_kv or self.N
 
     @property
     def T_q(self) -> int:
@@ -55,7 +60,7 @@ class Geometry:
         return (self.B, self.N, self.S_q, self.D) if self.layout == "BNSD" else (self.T_q, self.N, self.D)
 
     def kv_shape(self):
-        return (self.B, self.N, self.S_kv, self.D) if self.layout == "BNSD" else (self.T_kv, self.N, self.D)
+        return (self.B, self.n_kv, self.S_kv, self.D) if self.layout == "BNSD" else (self.T_kv, self.n_kv, self.D)
 
     def stat_shape(self):
         return (self.B, self.N, self.S_q) if self.layout == "BNSD" else (self.T_q, self.N)

@@ -55,6 +55,7 @@ class _Params(ctypes.Structure):
         ("pre_tokens", ctypes.c_int64),
         ("next_tokens", ctypes.c_int64),
         ("keep_prob", ctypes.c_double),
+        ("N_kv", ctypes.c_int64),
     ]
 
 
@@ -93,6 +94,11 @@ class Problem:
     next_tokens: int = 2147483647
     sparse_mode: int = 0
     keep_prob: float = 1.0
+    N_kv: int = 0  # key/value heads (GQA / MQA); 0 means N
+
+    @property
+    def n_kv(self) -> int:
+        return self.N_kv or self.N
 
     @property
     def T_q(self) -> int:
@@ -152,7 +158,10 @@ class _Call:
             pr.pre_tokens,
             pr.next_tokens,
             pr.keep_prob,
+            pr.n_kv,
         )
+        if pr.n_kv < 1 or pr.N % pr.n_kv:
+            raise ValueError(f"N={pr.N} is not a multiple of N_kv={pr.n_kv}")
 
     def ref(self):
         return ctypes.byref(self.p)
@@ -167,7 +176,7 @@ def _q_shape(pr: Problem):
 
 
 def _kv_shape(pr: Problem):
-    return (pr.B, pr.N, pr.S_kv, pr.D) if pr.layout == "BNSD" else (pr.T_kv, pr.N, pr.D)
+    return (pr.B, pr.n_kv, pr.S_kv, pr.D) if pr.layout == "BNSD" else (pr.T_kv, pr.n_kv, pr.D)
 
 
 def forward(pr: Problem, q, k, v, drop_mask=None):
@@ -224,7 +233,7 @@ def backward_dq_rows(pr: Problem, q, k, v, dy, drop_mask, rows):
 
 
 def backward_dkv_cols(pr: Problem, q, k, v, dy, drop_mask, cols):
-    """dK and dV for selected key rows (flat ids (b*N+n)*S_kv+j or t*N+n)."""
+    """dK and dV for selected key rows (flat ids (b*N_kv+h)*S_kv+j or t*N_kv+h)."""
     lib = _load()
     c = _Call(pr)
     q, k, v, dy, m = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dy), _as_u8(drop_mask)

@@ -26,6 +26,12 @@
  *       dK_j  = scale * sum_i dS_ij * q_i
  * Empty rows (V_i empty): O_i = 0, m_i = -inf, l_i = 0, no gradient flows.
  *
+ * Grouped key/value heads (aclnnFlashAttentionUnpaddingScoreGradV2 article
+ * §6.2: the query head count must be a non-zero integer multiple of the
+ * key/value head count): query head n reads key/value head n / (N / N_kv),
+ * and since that head is shared, its dK_j / dV_j are the sums of the
+ * expressions above over the N / N_kv query heads that read it.
+ *
  * Inputs are fp64 arrays (the bf16 values of the problem, converted exactly
  * by the caller); all arithmetic is double.  The
  * sequences of a TND problem use cumulative end offsets (no leading 0); a
@@ -49,6 +55,7 @@ typedef struct {
   double scale;
   int64_t pre_tokens, next_tokens;
   double keep_prob;
+  int64_t N_kv; /* key/value heads; N is a multiple of N_kv */
 } orc_params;
 
 /* ------------------------------------------------------------ geometry -- */
@@ -92,10 +99,13 @@ static int64_t row_q(const orc_params *p, const orc_seq *s, int64_t b, int64_t n
   if (p->layout == 0) return ((b * p->N + n) * p->S_q + i) * p->D;
   return ((s->q_start + i) * p->N + n) * p->D;
 }
-static int64_t row_kv(const orc_params *p, const orc_seq *s, int64_t b, int64_t n, int64_t j) {
-  if (p->layout == 0) return ((b * p->N + n) * p->S_kv + j) * p->D;
-  return ((s->kv_start + j) * p->N + n) * p->D;
+/* Element offset of key row j of key/value head h, batch b. */
+static int64_t row_kv(const orc_params *p, const orc_seq *s, int64_t b, int64_t h, int64_t j) {
+  if (p->layout == 0) return ((b * p->N_kv + h) * p->S_kv + j) * p->D;
+  return ((s->kv_start + j) * p->N_kv + h) * p->D;
 }
+/* The key/value head query head n reads. */
+static int64_t kv_head(const orc_params *p, int64_t n) { return n / (p->N / p->N_kv); }
 /* Index of the softmax statistics of query row i: [B,N,S] or [T,N]. */
 static int64_t stat_q(const orc_params *p, const orc_seq *s, int64_t b, int64_t n, int64_t i) {
   if (p->layout == 0) return (b * p->N + n) * p->S_q + i;
@@ -162,17 +172,18 @@ static void forward_row(const orc_params *p, const orc_seq *s, int64_t b, int64_
     return;
   }
   const double *qi = q + row_q(p, s, b, n, i);
+  const int64_t h = kv_head(p, n);
   double m = -INFINITY;
   for (int64_t j = lo; j <= hi; ++j) {
-    double sij = p->scale * dot(qi, k + row_kv(p, s, b, n, j), D);
+    double sij = p->scale * dot(qi, k + row_kv(p, s, b, h, j), D);
     if (sij > m) m = sij;
   }
   double l = 0.0;
-  for (int64_t j = lo; j <= hi; ++j) l += exp(p->scale * dot(qi, k + row_kv(p, s, b, n, j), D) - m);
+  for (int64_t j = lo; j <= hi; ++j) l += exp(p->scale * dot(qi, k + row_kv(p, s, b, h, j), D) - m);
   for (int64_t j = lo; j <= hi; ++j) {
-    double pij = exp(p->scale * dot(qi, k + row_kv(p, s, b, n, j), D) - m) / l;
+    double pij = exp(p->scale * dot(qi, k + row_kv(p, s, b, h, j), D) - m) / l;
     double w = pij * keep_bit(s, mask, n, i, j) / p->keep_prob;
-    const double *vj = v + row_kv(p, s, b, n, j);
+    const double *vj = v + row_kv(p, s, b, h, j);
     for (int64_t d = 0; d < D; ++d) o[d] += w * vj[d];
   }
   *m_out = m; *l_out = l;
@@ -219,36 +230,41 @@ static void dq_row(const orc_params *p, const orc_seq *s, int64_t b, int64_t n, 
   if (!key_range(p, s, i, &lo, &hi)) return;
   const double *qi = q + row_q(p, s, b, n, i);
   const double *dyi = dy + row_q(p, s, b, n, i);
+  const int64_t h = kv_head(p, n);
   for (int64_t j = lo; j <= hi; ++j) {
-    const double *kj = k + row_kv(p, s, b, n, j);
+    const double *kj = k + row_kv(p, s, b, h, j);
     double pij = prob(r, p->scale * dot(qi, kj, D));
-    double dpij = dot(dyi, v + row_kv(p, s, b, n, j), D) * keep_bit(s, mask, n, i, j) / p->keep_prob;
+    double dpij = dot(dyi, v + row_kv(p, s, b, h, j), D) * keep_bit(s, mask, n, i, j) / p->keep_prob;
     double dsij = pij * (dpij - r->Di);
     for (int64_t d = 0; d < D; ++d) dq[d] += p->scale * dsij * kj[d];
   }
 }
 
-/* dK_j and dV_j, gathering over the queries that see key j.  `rows` holds
- * the row data of every query row of this (b, n), indexed by local i. */
-static void dkv_col(const orc_params *p, const orc_seq *s, int64_t b, int64_t n, int64_t j, const row_data *rows,
+/* dK_j and dV_j of key/value head h, gathering over the queries that see
+ * key j in each of the query heads that read head h.  `rows` holds the row
+ * data of those heads: rows[g * q_len + i] for the g-th head of the group. */
+static void dkv_col(const orc_params *p, const orc_seq *s, int64_t b, int64_t h, int64_t j, const row_data *rows,
                     const double *q, const double *k, const double *v, const double *dy,
                     const uint8_t *mask, double *dk, double *dv) {
-  const int64_t D = p->D;
+  const int64_t D = p->D, G = p->N / p->N_kv;
   int64_t lo, hi;
   for (int64_t d = 0; d < D; ++d) { dk[d] = 0.0; dv[d] = 0.0; }
   if (!query_range(p, s, j, &lo, &hi)) return;
-  const double *kj = k + row_kv(p, s, b, n, j);
-  const double *vj = v + row_kv(p, s, b, n, j);
-  for (int64_t i = lo; i <= hi; ++i) {
-    const double *qi = q + row_q(p, s, b, n, i);
-    const double *dyi = dy + row_q(p, s, b, n, i);
-    const row_data *r = &rows[i];
-    double pij = prob(r, p->scale * dot(qi, kj, D));
-    double z = keep_bit(s, mask, n, i, j) / p->keep_prob;
-    double dsij = pij * (dot(dyi, vj, D) * z - r->Di);
-    for (int64_t d = 0; d < D; ++d) {
-      dv[d] += pij * z * dyi[d];
-      dk[d] += p->scale * dsij * qi[d];
+  const double *kj = k + row_kv(p, s, b, h, j);
+  const double *vj = v + row_kv(p, s, b, h, j);
+  for (int64_t gi = 0; gi < G; ++gi) {
+    const int64_t n = h * G + gi;
+    for (int64_t i = lo; i <= hi; ++i) {
+      const double *qi = q + row_q(p, s, b, n, i);
+      const double *dyi = dy + row_q(p, s, b, n, i);
+      const row_data *r = &rows[gi * s->q_len + i];
+      double pij = prob(r, p->scale * dot(qi, kj, D));
+      double z = keep_bit(s, mask, n, i, j) / p->keep_prob;
+      double dsij = pij * (dot(dyi, vj, D) * z - r->Di);
+      for (int64_t d = 0; d < D; ++d) {
+        dv[d] += pij * z * dyi[d];
+        dk[d] += p->scale * dsij * qi[d];
+      }
     }
   }
 }
@@ -270,13 +286,15 @@ static int locate_q(const orc_params *p, int64_t id, int64_t *b, int64_t *n, int
   }
   return 0;
 }
+/* Map a flat key-row id ((b*N_kv+h)*S_kv+j for BNSD, t*N_kv+h for TND) to
+ * (b, key/value head h, local j). */
 static int locate_kv(const orc_params *p, int64_t id, int64_t *b, int64_t *n, int64_t *j) {
   if (p->layout == 0) {
-    *j = id % p->S_kv; *n = (id / p->S_kv) % p->N; *b = id / (p->S_kv * p->N);
+    *j = id % p->S_kv; *n = (id / p->S_kv) % p->N_kv; *b = id / (p->S_kv * p->N_kv);
     return 1;
   }
-  int64_t t = id / p->N;
-  *n = id % p->N;
+  int64_t t = id / p->N_kv;
+  *n = id % p->N_kv;
   for (int64_t bb = 0; bb < p->B; ++bb) {
     int64_t st, len;
     seq_span(p->cu_kv, bb, &st, &len);
@@ -327,30 +345,34 @@ int orc_forward_rows(const orc_params *p, const double *q, const double *k, cons
 int orc_backward(const orc_params *p, const double *q, const double *k, const double *v, const double *dy,
                  const uint8_t *mask, const double *given_out, const double *given_max, const double *given_sum,
                  double *dq, double *dk, double *dv) {
-  const int64_t N = p->N, D = p->D;
+  const int64_t D = p->D, G = p->N / p->N_kv;
   int64_t max_sq = 0;
   for (int64_t b = 0; b < p->B; ++b) { orc_seq s = seq_of(p, b); if (s.q_len > max_sq) max_sq = s.q_len; }
-  row_data *rows = (row_data *)malloc(sizeof(row_data) * (max_sq > 0 ? max_sq : 1));
+  row_data *rows = (row_data *)malloc(sizeof(row_data) * (size_t)(G * (max_sq > 0 ? max_sq : 1)));
   for (int64_t b = 0; b < p->B; ++b) {
     orc_seq s = seq_of(p, b);
-    for (int64_t n = 0; n < N; ++n) {
-      /* 1) row statistics and D_i for every query of this (b, n) */
+    for (int64_t h = 0; h < p->N_kv; ++h) {
+      for (int64_t gi = 0; gi < G; ++gi) {
+        const int64_t n = h * G + gi;
+        row_data *rg = rows + gi * s.q_len;
+        /* 1) row statistics and D_i for every query of this (b, n) */
 #pragma omp parallel
-      {
-        double *o = (double *)malloc(sizeof(double) * D);
+        {
+          double *o = (double *)malloc(sizeof(double) * D);
 #pragma omp for schedule(dynamic, 8)
-        for (int64_t i = 0; i < s.q_len; ++i)
-          rows[i] = backward_row_data(p, &s, b, n, i, q, k, v, dy, mask, given_out, given_max, given_sum, o);
-        free(o);
-      }
-      /* 2) dQ rows */
+          for (int64_t i = 0; i < s.q_len; ++i)
+            rg[i] = backward_row_data(p, &s, b, n, i, q, k, v, dy, mask, given_out, given_max, given_sum, o);
+          free(o);
+        }
+        /* 2) dQ rows */
 #pragma omp parallel for schedule(dynamic, 8)
-      for (int64_t i = 0; i < s.q_len; ++i)
-        dq_row(p, &s, b, n, i, &rows[i], q, k, v, dy, mask, dq + row_q(p, &s, b, n, i));
-      /* 3) dK / dV columns */
+        for (int64_t i = 0; i < s.q_len; ++i)
+          dq_row(p, &s, b, n, i, &rg[i], q, k, v, dy, mask, dq + row_q(p, &s, b, n, i));
+      }
+      /* 3) dK / dV columns of key/value head h, over its query heads */
 #pragma omp parallel for schedule(dynamic, 8)
       for (int64_t j = 0; j < s.kv_len; ++j)
-        dkv_col(p, &s, b, n, j, rows, q, k, v, dy, mask, dk + row_kv(p, &s, b, n, j), dv + row_kv(p, &s, b, n, j));
+        dkv_col(p, &s, b, h, j, rows, q, k, v, dy, mask, dk + row_kv(p, &s, b, h, j), dv + row_kv(p, &s, b, h, j));
     }
   }
   free(rows);
@@ -377,27 +399,32 @@ int orc_backward_dq_rows(const orc_params *p, const double *q, const double *k, 
   return 0;
 }
 
-/* dK / dV for a list of key rows (flat ids (b*N+n)*S_kv+j or t*N+n), exact
- * mode.  Computes the row data of exactly the queries that see each key. */
+/* dK / dV for a list of key rows (flat ids (b*N_kv+h)*S_kv+j or t*N_kv+h),
+ * exact mode.  Computes the row data of exactly the queries that see each
+ * key, in every query head of the key's group. */
 int orc_backward_dkv_cols(const orc_params *p, const double *q, const double *k, const double *v,
                           const double *dy, const uint8_t *mask, int64_t nsel, const int64_t *sel, double *dk,
                           double *dv) {
+  const int64_t G = p->N / p->N_kv;
   for (int64_t t = 0; t < nsel; ++t) {
-    int64_t b, n, j, lo, hi;
+    int64_t b, h, j, lo, hi;
     for (int64_t d = 0; d < p->D; ++d) { dk[t * p->D + d] = 0.0; dv[t * p->D + d] = 0.0; }
-    if (!locate_kv(p, sel[t], &b, &n, &j)) continue;
+    if (!locate_kv(p, sel[t], &b, &h, &j)) continue;
     orc_seq s = seq_of(p, b);
     if (!query_range(p, &s, j, &lo, &hi)) continue;
-    row_data *rows = (row_data *)calloc((size_t)(s.q_len > 0 ? s.q_len : 1), sizeof(row_data));
+    row_data *rows = (row_data *)calloc((size_t)(G * (s.q_len > 0 ? s.q_len : 1)), sizeof(row_data));
+    for (int64_t gi = 0; gi < G; ++gi) {
+      const int64_t n = h * G + gi;
 #pragma omp parallel
-    {
-      double *o = (double *)malloc(sizeof(double) * p->D);
+      {
+        double *o = (double *)malloc(sizeof(double) * p->D);
 #pragma omp for schedule(dynamic, 8)
-      for (int64_t i = lo; i <= hi; ++i)
-        rows[i] = backward_row_data(p, &s, b, n, i, q, k, v, dy, mask, NULL, NULL, NULL, o);
-      free(o);
+        for (int64_t i = lo; i <= hi; ++i)
+          rows[gi * s.q_len + i] = backward_row_data(p, &s, b, n, i, q, k, v, dy, mask, NULL, NULL, NULL, o);
+        free(o);
+      }
     }
-    dkv_col(p, &s, b, n, j, rows, q, k, v, dy, mask, dk + t * p->D, dv + t * p->D);
+    dkv_col(p, &s, b, h, j, rows, q, k, v, dy, mask, dk + t * p->D, dv + t * p->D);
     free(rows);
   }
   return 0;

@@ -359,3 +359,117 @@ def test_visible_pair_count_matches_dense_mask():
         pr = to_problem(Geometry(**case))
         dense = _dense_mask(pr, pr.S_q, pr.S_kv).sum() * pr.B * pr.N
         assert orc.visible_pairs(pr) == dense
+
+
+# ------------------------------------------- grouped key/value heads (GQA) --
+# The rule (aclnnFlashAttentionUnpaddingScoreGradV2 article §6.2): N is a
+# non-zero integer multiple of N_kv; query head n reads key/value head
+# n // (N / N_kv).  Pinned three ways: against the oracle's own per-head path
+# on explicitly repeated K / V (dK, dV summed over each group), against torch
+# SDPA with repeated K / V and autograd, and by finite differences.
+GQA_CASES = {
+    "bnsd_g2_band": dict(layout="BNSD", B=2, N=4, N_kv=2, D=8, S_q=19, S_kv=19, scale=0.4, sparse_mode=4,
+                         pre_tokens=5, next_tokens=2),
+    "bnsd_mqa_nomask": dict(layout="BNSD", B=1, N=3, N_kv=1, D=8, S_q=17, S_kv=23, scale=0.3, sparse_mode=0),
+    "bnsd_g3_dropout": dict(layout="BNSD", B=1, N=6, N_kv=2, D=4, S_q=12, S_kv=12, scale=0.5, sparse_mode=4,
+                            pre_tokens=3, next_tokens=3, keep_prob=0.75),
+    "tnd_g2_band": dict(layout="TND", B=3, N=4, N_kv=2, D=8, cu_seqlens_q=[7, 7, 20], cu_seqlens_kv=[7, 7, 20],
+                        scale=0.45, sparse_mode=4, pre_tokens=4, next_tokens=0),
+}
+
+
+def _repeat_heads(x, geom, G):
+    """Repeat each key/value head G times along the head axis (BNSD axis 1, TND axis 1)."""
+    return np.repeat(np.asarray(x), G, axis=1)
+
+
+def _sum_groups(x, geom, G):
+    """Sum each run of G consecutive heads (the inverse bookkeeping of _repeat_heads)."""
+    x = np.asarray(x)
+    shp = list(x.shape)
+    shp[1:2] = [shp[1] // G, G]
+    return x.reshape(shp).sum(axis=2)
+
+
+@pytest.mark.parametrize("name", sorted(GQA_CASES))
+def test_gqa_equals_per_head_on_repeated_kv(name):
+    case = GQA_CASES[name]
+    geom = Geometry(**case)
+    G = geom.N // geom.N_kv
+    inp = draw(geom, 3000 + len(name))
+    pr = to_problem(geom)
+    mha = to_problem(Geometry(**{**case, "N_kv": 0}))
+    q, k, v, dy = (t.double().numpy() for t in (inp.q, inp.k, inp.v, inp.dy))
+    kr, vr = _repeat_heads(k, geom, G), _repeat_heads(v, geom, G)
+    out, smax, ssum = orc.forward(pr, q, k, v, inp.drop_mask)
+    out_r, smax_r, ssum_r = orc.forward(mha, q, kr, vr, inp.drop_mask)
+    assert np.array_equal(out, out_r) and np.array_equal(smax, smax_r) and np.array_equal(ssum, ssum_r)
+    dq, dk, dv = orc.backward(pr, q, k, v, dy, inp.drop_mask)
+    dq_r, dk_r, dv_r = orc.backward(mha, q, kr, vr, dy, inp.drop_mask)
+    assert dk.shape == k.shape and dv.shape == v.shape
+    assert np.array_equal(dq, dq_r)
+    assert np.allclose(dk, _sum_groups(dk_r, geom, G), rtol=1e-12, atol=1e-14)
+    assert np.allclose(dv, _sum_groups(dv_r, geom, G), rtol=1e-12, atol=1e-14)
+    # the key-column entry point agrees with the full backward
+    cols = np.arange(geom.B * geom.n_kv * geom.S_kv if geom.layout == "BNSD" else geom.T_kv * geom.n_kv)
+    ck, cv = orc.backward_dkv_cols(pr, q, k, v, dy, inp.drop_mask, cols)
+    assert np.allclose(ck, dk.reshape(-1, geom.D), rtol=1e-12, atol=1e-14)
+    assert np.allclose(cv, dv.reshape(-1, geom.D), rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("name", ["bnsd_g2_band", "bnsd_mqa_nomask"])
+def test_gqa_against_sdpa_float64(name):
+    case = GQA_CASES[name]
+    geom = Geometry(**case)
+    G = geom.N // geom.N_kv
+    inp = draw(geom, 4000 + len(name))
+    pr = to_problem(geom)
+    out, _, _ = orc.forward(pr, inp.q, inp.k, inp.v)
+    dq, dk, dv = orc.backward(pr, inp.q, inp.k, inp.v, inp.dy)
+    q = inp.q.double().requires_grad_(True)
+    k = inp.k.double().requires_grad_(True)
+    v = inp.v.double().requires_grad_(True)
+    m = torch.from_numpy(_dense_mask(pr, geom.S_q, geom.S_kv))
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k.repeat_interleave(G, dim=1),
+                                                           v.repeat_interleave(G, dim=1), attn_mask=m,
+                                                           scale=geom.scale)
+    ref.backward(inp.dy.double())
+    assert np.allclose(out, ref.detach().numpy(), rtol=1e-10, atol=1e-12)
+    assert np.allclose(dq, q.grad.numpy(), rtol=1e-9, atol=1e-11)
+    assert np.allclose(dk, k.grad.numpy(), rtol=1e-9, atol=1e-11)
+    assert np.allclose(dv, v.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+def test_gqa_finite_differences():
+    case = dict(layout="BNSD", B=1, N=4, N_kv=2, D=3, S_q=6, S_kv=6, scale=0.8, sparse_mode=4, pre_tokens=2,
+                next_tokens=1, keep_prob=0.7)
+    geom, inp = _fd_inputs(case, 5001)
+    pr = to_problem(geom)
+    q, k, v, dy = (t.double().numpy() for t in (inp.q, inp.k, inp.v, inp.dy))
+    mask = inp.drop_mask
+    dq, dk, dv = orc.backward(pr, q, k, v, dy, mask)
+
+    def loss(qq, kk, vv):
+        out, _, _ = orc.forward(pr, qq, kk, vv, mask)
+        return float(np.sum(out * dy))
+
+    h = 1e-6
+    for which, base, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(base)
+        flat = base.reshape(-1)
+        for idx in range(flat.size):
+            save = flat[idx]
+            flat[idx] = save + h
+            lp = loss(q, k, v)
+            flat[idx] = save - h
+            lm = loss(q, k, v)
+            flat[idx] = save
+            num.reshape(-1)[idx] = (lp - lm) / (2 * h)
+        err = np.linalg.norm((num - grad).ravel()) / max(np.linalg.norm(num.ravel()), 1e-30)
+        assert err <= 1e-6, (which, err)
+
+
+def test_gqa_rejects_non_multiple():
+    geom = Geometry("BNSD", 1, 4, 8, S_q=8, S_kv=8, N_kv=3)
+    with pytest.raises(ValueError):
+        orc.forward(to_problem(geom), np.zeros((1, 4, 8, 8)), np.zeros((1, 3, 8, 8)), np.zeros((1, 3, 8, 8)))
