@@ -95,6 +95,10 @@ swa_status_t make_plan(const swa_params_t* p, Plan& plan) {
   if (!(p->keep_prob > 0.0 && p->keep_prob <= 1.0))
     return fail(SWA_ERR_PARAM_INVALID, "keep_prob must be in (0, 1], got %g", p->keep_prob);
   if (p->N < 1 || p->N > 256) return fail(SWA_ERR_PARAM_INVALID, "N must be in [1, 256], got %lld", (long long)p->N);
+  const int64_t n_kv = p->N_kv == 0 ? p->N : p->N_kv;
+  if (n_kv < 1 || n_kv > p->N || p->N % n_kv != 0)
+    return fail(SWA_ERR_PARAM_INVALID, "N = %lld must be a multiple of N_kv = %lld", (long long)p->N,
+                (long long)p->N_kv);
   if (p->B < 1) return fail(SWA_ERR_PARAM_INVALID, "B must be >= 1, got %lld", (long long)p->B);
   if (p->D < 1 || p->D > 768) return fail(SWA_ERR_PARAM_INVALID, "D must be in [1, 768], got %lld", (long long)p->D);
   if (p->D != 64 && p->D != 128) return fail(SWA_ERR_UNSUPPORTED, "D = %lld is not built (64 or 128)", (long long)p->D);
@@ -110,6 +114,8 @@ swa_status_t make_plan(const swa_params_t* p, Plan& plan) {
   Geometry& g = plan.g;
   g.layout = p->layout;
   g.N = static_cast<int32_t>(p->N);
+  g.N_kv = static_cast<int32_t>(n_kv);
+  g.group = static_cast<int32_t>(p->N / n_kv);
   g.D = static_cast<int32_t>(p->D);
   g.sparse_mode = p->sparse_mode;
   g.scale = static_cast<float>(p->scale);
@@ -211,10 +217,13 @@ std::vector<SeqDesc> build_descs(const Plan& plan, bool forward) {
     d.descending = c1 >= c0 ? 1 : 0;
     entries.push_back(Entry{d, wmax});
   };
+  // the query-side passes run one CTA per query head, the key-side pass one
+  // per key/value head (it walks the query heads of its group)
+  const int32_t nh = forward ? g.N : g.N_kv;
   if (g.layout == 0) {
-    fill(plan.seqs[0], -1, static_cast<int32_t>(plan.B * g.N));
+    fill(plan.seqs[0], -1, static_cast<int32_t>(plan.B * nh));
   } else {
-    for (int64_t b = 0; b < plan.B; ++b) fill(plan.seqs[b], static_cast<int32_t>(b), g.N);
+    for (int64_t b = 0; b < plan.B; ++b) fill(plan.seqs[b], static_cast<int32_t>(b), nh);
     std::stable_sort(entries.begin(), entries.end(),
                      [](const Entry& x, const Entry& y) { return x.weight > y.weight; });
   }
@@ -276,7 +285,7 @@ swa_status_t make_map(CUtensorMap* m, const void* ptr, const Plan& plan, bool q_
   auto fn = encode_fn();
   if (!fn) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const Geometry& g = plan.g;
-  const cuuint64_t D = g.D, N = g.N;
+  const cuuint64_t D = g.D, N = q_side ? g.N : g.N_kv;
   const cuuint64_t es_bytes = 2;
   const cuuint32_t box_x = 64;  // 128 bytes, one swizzle row
   cuuint64_t dims[4], strides[3];

@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kColDK = kColDV + D;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Geometry& g = a.g;
-  const Item w = resolve_item(tab, a.g, static_cast<int>(blockIdx.x));
+  const Item w = resolve_item(tab, a.g, static_cast<int>(blockIdx.x), a.g.N_kv);  // w.n: key/value head
   const SeqInfo sq = w.s;
   const int j0 = w.tile * kTileN;
   const int j_last = min(j0 + kTileN - 1, sq.kv_len - 1);
@@ -112,6 +112,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     q_t0 = lo / kTileM;
     n_q = hi / kTileM - q_t0 + 1;
   }
+  // The CTA walks those query tiles for each query head that reads this
+  // key/value head (one head without grouping): step it is query tile
+  // q_t0 + it % n_q of query head w.n * group + it / n_q, and dK / dV sum
+  // over all of them in TMEM.
+  const int n_it = g.group * n_q;
 
   if (threadIdx.x == 0) {
     mbar_init(&s.kv_full, 1);
@@ -158,8 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_rows<D>(s.v, &mv, &s.kv_full, g, w.b, w.n, sq.kv_start, j0);
       }
       int q_issued = 0, dy_issued = 0;
-      for (int it = 0; it < n_q; ++it) {
-        const int i0 = (q_t0 + it) * kTileM;
+      for (int it = 0; it < n_it; ++it) {
+        const int i0 = (q_t0 + it % n_q) * kTileM;
+        const int qn = w.n * g.group + it / n_q;  // query head of this step
         const int qs = it % kQS;
         // Q(it) reuses the stage of Q(it - kQS), free once dK of that tile is done
         if (it >= kQS &&
@@ -167,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         if (lane == 0) {
           mbar_arrive_expect_tx(&s.q_full[qs], kTileBytes);
-          tma_rows<D>(s.q[qs], &mq, &s.q_full[qs], g, w.b, w.n, sq.q_start, i0);
+          tma_rows<D>(s.q[qs], &mq, &s.q_full[qs], g, w.b, qn, sq.q_start, i0);
         }
         ++q_issued;
         // dY and the statistics reuse stage (it & 1) once dV(it - 2) is done,
@@ -178,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         if (lane == 0) {
           mbar_arrive_expect_tx(&s.dy_full[st], kTileBytes);
-          tma_rows<D>(s.dy[st], &mdy, &s.dy_full[st], g, w.b, w.n, sq.q_start, i0);
+          tma_rows<D>(s.dy[st], &mdy, &s.dy_full[st], g, w.b, qn, sq.q_start, i0);
         }
         ++dy_issued;
         // per-query statistics (and keep bits) of this tile: 4 rows per lane
@@ -189,10 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           float l2 = INFINITY, dd = 0.f;
           uint32_t bits[4] = {0u, 0u, 0u, 0u};
           if (i < sq.q_len) {
-            const int64_t si = stat_index(g, sq, w.b, w.n, i);
+            const int64_t si = stat_index(g, sq, w.b, qn, i);
             l2 = a.lse2[si];
             dd = a.dsum[si];
-            if constexpr (DROP) load_keep_bits(a.mask, sq, w.n, i, j0, bits);
+            if constexpr (DROP) load_keep_bits(a.mask, sq, qn, i, j0, bits);
           }
           s.lse2[st][c] = l2;
           s.dsum[st][c] = dd;
@@ -235,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_ss(region(0), k_addr, smem_u32(s.q[0]));  // S^T(0) = K Q(0)^T
         umma_commit(&s.s_full[0]);
       }
-      for (int it = 0; ok && it < n_q; ++it) {
+      for (int it = 0; ok && it < n_it; ++it) {
         const int st = it & 1;
         // dP^T(it) over S^T(it), once every compute thread has read S^T(it)
         if (!mbar_wait(&s.s_loaded, it & 1, a.err, kErrBwdMma)) break;
@@ -243,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         issue_ss(region(it), v_addr, smem_u32(s.dy[st]));  // dP^T = V dY^T
         umma_commit(&s.dp_full);
-        if (it + 1 < n_q) {
+        if (it + 1 < n_it) {
           // S^T(it+1) into the other region, once dK(it-1) has read it
           if (it >= 1 && !mbar_wait(&s.region_free[(it - 1) & 1], ((it - 1) >> 1) & 1, a.err, kErrBwdMma)) break;
           const int nq = (it + 1) % kQS;
@@ -260,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------- dV / dK issuer --
     if (lane == 0 && n_q > 0) {
       constexpr uint32_t kIdKV = idesc_bf16_f32(kTileN, D, false, true);  // A = P^T / dS^T in TMEM
-      for (int it = 0; it < n_q; ++it) {
+      for (int it = 0; it < n_it; ++it) {
         const int st = it & 1, qs = it % kQS;
         // dV, dK from the P^T / dS^T the compute warps stored in region(it):
         // query columns [64h, 64h+64) of the tile hold P^T in columns
@@ -280,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        sdesc_sw128(q_addr + kk * 2048, kAtomBytes, 1024), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&s.q_empty[qs]);  // likewise S^T(it) for Q(it)
         umma_commit(&s.region_free[st]);
-        if (it == n_q - 1) umma_commit(&s.mma_done);
+        if (it == n_it - 1) umma_commit(&s.mma_done);
       }
       umma_commit(&s.drain_kv);
       mbar_wait_drain(&s.drain_kv, 0);
@@ -304,9 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       qhi = 0;
     }
     bool ok = true;
-    for (int it = 0; it < n_q; ++it) {
+    for (int it = 0; it < n_it; ++it) {
       const int st = it & 1;
-      const int i0 = (q_t0 + it) * kTileM;
+      const int i0 = (q_t0 + it % n_q) * kTileM;
       const bool full = tile_fully_visible(g, sq, i0, j0);
       const uint32_t col = tmem + lane_off + region(it) + cbase;
       if (!compute_wait(&s.s_full[st], (it >> 1) & 1, a.err)) { ok = false; break; }

@@ -65,7 +65,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kTileBytes = DqSmem<D>::kTileBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Geometry& g = a.g;
-  const Item w = resolve_item(tab, a.g, static_cast<int>(blockIdx.x));
+  const Item w = resolve_item(tab, a.g, static_cast<int>(blockIdx.x), a.g.N);
+  const int hk = w.n / a.g.group;  // the key/value head this query head reads
   const SeqInfo sq = w.s;
   const int q0 = w.tile * kTileM;
   const int q_last = min(q0 + kTileM - 1, sq.q_len - 1);
@@ -130,12 +131,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // K(j) reuses the stage of K(j-3), free once dQ(j-3) is done
         if (j >= 3 && !mbar_wait(&s.k_empty[kb], ((j / 3) - 1) & 1, a.err, kErrBwdLoad)) break;
         mbar_arrive_expect_tx(&s.k_full[kb], kTileBytes);
-        tma_rows<D>(s.k[kb], &mk, &s.k_full[kb], g, w.b, w.n, sq.kv_start, jr);
+        tma_rows<D>(s.k[kb], &mk, &s.k_full[kb], g, w.b, hk, sq.kv_start, jr);
         ++k_issued;
         // V(j) reuses the stage of V(j-2), free once dP(j-2) is done
         if (j >= 2 && !mbar_wait(&s.v_empty[vb], ((j >> 1) - 1) & 1, a.err, kErrBwdLoad)) break;
         mbar_arrive_expect_tx(&s.v_full[vb], kTileBytes);
-        tma_rows<D>(s.v[vb], &mv, &s.v_full[vb], g, w.b, w.n, sq.kv_start, jr);
+        tma_rows<D>(s.v[vb], &mv, &s.v_full[vb], g, w.b, hk, sq.kv_start, jr);
         ++v_issued;
       }
       // every copy issued has landed before the CTA may exit

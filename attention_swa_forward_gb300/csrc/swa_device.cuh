@@ -20,8 +20,10 @@ struct Item {
   SeqInfo s;
 };
 
+// `nh` is the number of heads per batch the table enumerates: query heads
+// for the query-major kernels, key/value heads for the key-major one.
 template <int CAP>
-__device__ __forceinline__ Item resolve_item(const SeqTable<CAP>& tab, const Geometry& g, int k) {
+__device__ __forceinline__ Item resolve_item(const SeqTable<CAP>& tab, const Geometry& g, int k, int nh) {
   int lo = 0, hi = tab.count - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -34,8 +36,8 @@ __device__ __forceinline__ Item resolve_item(const SeqTable<CAP>& tab, const Geo
   Item it;
   it.tile = d.descending ? d.tiles - 1 - rank : rank;
   if (d.b < 0) {
-    it.b = h / g.N;
-    it.n = h - it.b * g.N;
+    it.b = h / nh;
+    it.n = h - it.b * nh;
     it.s.mask_base = static_cast<int64_t>(it.b) * g.N * g.S_q * static_cast<int64_t>(g.S_kv);
   } else {
     it.b = d.b;
@@ -54,9 +56,10 @@ __device__ __forceinline__ int64_t q_elem(const Geometry& g, const SeqInfo& s, i
   return g.layout == 0 ? ((static_cast<int64_t>(b) * g.N + n) * g.S_q + i) * g.D
                        : (static_cast<int64_t>(s.q_start + i) * g.N + n) * g.D;
 }
-__device__ __forceinline__ int64_t kv_elem(const Geometry& g, const SeqInfo& s, int b, int n, int j) {
-  return g.layout == 0 ? ((static_cast<int64_t>(b) * g.N + n) * g.S_kv + j) * g.D
-                       : (static_cast<int64_t>(s.kv_start + j) * g.N + n) * g.D;
+// Element offset of local key row j of key/value head h: BNSD [B,N_kv,S,D] or TND [T,N_kv,D].
+__device__ __forceinline__ int64_t kv_elem(const Geometry& g, const SeqInfo& s, int b, int h, int j) {
+  return g.layout == 0 ? ((static_cast<int64_t>(b) * g.N_kv + h) * g.S_kv + j) * g.D
+                       : (static_cast<int64_t>(s.kv_start + j) * g.N_kv + h) * g.D;
 }
 // Index of the softmax statistics of local query row i: [B,N,S] or [T,N].
 __device__ __forceinline__ int64_t stat_index(const Geometry& g, const SeqInfo& s, int b, int n, int i) {

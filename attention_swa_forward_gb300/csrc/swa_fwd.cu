@@ -54,7 +54,8 @@ __global__ void __launch_bounds__(224, 1)
   constexpr int kTileBytes = FwdSmem<D>::kTileBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Geometry& g = a.g;
-  const Item w = resolve_item(tab, a.g, static_cast<int>(blockIdx.x));
+  const Item w = resolve_item(tab, a.g, static_cast<int>(blockIdx.x), a.g.N);
+  const int hk = w.n / a.g.group;  // the key/value head this query head reads
   const SeqInfo sq = w.s;
   const int q0 = w.tile * kTileM;
   const int q_last = min(q0 + kTileM - 1, sq.q_len - 1);
@@ -114,11 +115,11 @@ __global__ void __launch_bounds__(224, 1)
         const int j0 = (kv_t0 + it) * kTileN;
         if (it >= kStages && !mbar_wait(&s.k_empty[st], (use - 1) & 1, a.err, kErrFwdLoad)) break;
         mbar_arrive_expect_tx(&s.k_full[st], kTileBytes);
-        tma_rows<D>(s.k[st], &mk, &s.k_full[st], g, w.b, w.n, sq.kv_start, j0);
+        tma_rows<D>(s.k[st], &mk, &s.k_full[st], g, w.b, hk, sq.kv_start, j0);
         ++k_issued;
         if (it >= kStages && !mbar_wait(&s.v_empty[st], (use - 1) & 1, a.err, kErrFwdLoad)) break;
         mbar_arrive_expect_tx(&s.v_full[st], kTileBytes);
-        tma_rows<D>(s.v[st], &mv, &s.v_full[st], g, w.b, w.n, sq.kv_start, j0);
+        tma_rows<D>(s.v[st], &mv, &s.v_full[st], g, w.b, hk, sq.kv_start, j0);
         ++v_issued;
       }
       // every copy issued has landed before the CTA may exit

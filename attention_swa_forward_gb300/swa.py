@@ -50,6 +50,7 @@ class SwaParams(ctypes.Structure):
         ("next_tokens", ctypes.c_int64),
         ("sparse_mode", ctypes.c_int32),
         ("keep_prob", ctypes.c_double),
+        ("N_kv", ctypes.c_int64),
     ]
 
 
@@ -126,6 +127,7 @@ class Params:
         c.next_tokens = int(geom.next_tokens)
         c.sparse_mode = int(geom.sparse_mode)
         c.keep_prob = float(geom.keep_prob)
+        c.N_kv = int(getattr(geom, "N_kv", 0) or 0)
 
     def ref(self):
         return ctypes.byref(self.c)

@@ -95,6 +95,12 @@ typedef struct {
   int64_t next_tokens;          /* BAND right extent, default 2147483647 */
   int32_t sparse_mode;          /* 0 or 4 */
   double keep_prob;             /* dropout keep probability in (0, 1], default 1.0 */
+  int64_t N_kv;                 /* key/value heads for grouped-query attention: N must be a
+                                   multiple of N_kv (aclnnFlashAttentionUnpaddingScoreGradV2
+                                   article, shape constraints: Nq/Nkv a non-zero integer);
+                                   query head n reads key/value head n / (N / N_kv).
+                                   k, v, dk, dv then have N_kv heads ([B,N_kv,S_kv,D] or
+                                   [T_kv,N_kv,D]).  0 (the default) means N_kv = N. */
 } swa_params_t;
 
 /* Fill `p` with the documented defaults (FlashAttentionScore REG_OP

@@ -44,13 +44,14 @@ def test_ctypes_struct_matches_c_layout(tmp_path):
         '#include <stdio.h>\n#include <stddef.h>\n#include "swa.h"\n'
         "int main(void){printf(\"%zu %zu %zu %zu %zu %zu\\n\", sizeof(swa_params_t),"
         " offsetof(swa_params_t, B), offsetof(swa_params_t, cu_seqlens_q), offsetof(swa_params_t, scale),"
-        " offsetof(swa_params_t, sparse_mode), offsetof(swa_params_t, keep_prob));return 0;}\n")
+        " offsetof(swa_params_t, sparse_mode), offsetof(swa_params_t, keep_prob));"
+        "printf(\"%zu\\n\", offsetof(swa_params_t, N_kv));return 0;}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
     got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
     P = swa.SwaParams
     want = [ctypes.sizeof(P), P.B.offset, P.cu_seqlens_q.offset, P.scale.offset, P.sparse_mode.offset,
-            P.keep_prob.offset]
+            P.keep_prob.offset, P.N_kv.offset]
     assert got == want
 
 
@@ -60,6 +61,7 @@ def test_defaults_match_documented_attributes(lib):
     assert p.scale == 1.0 and p.keep_prob == 1.0
     assert p.pre_tokens == 2147483647 and p.next_tokens == 2147483647
     assert p.sparse_mode == 0
+    assert p.N_kv == 0  # N_kv = N
 
 
 def _size(geom, backward=False):
@@ -91,6 +93,13 @@ BASE = dict(layout="BNSD", B=1, N=2, D=128, S_q=256, S_kv=256, scale=0.1, sparse
     ({"pre_tokens": -1, "next_tokens": 2}, swa.SWA_OK),
     ({"scale": float("inf")}, swa.SWA_ERR_PARAM_INVALID),
     ({"D": 64}, swa.SWA_OK),
+    # grouped key/value heads: N must be a multiple of N_kv
+    ({"N": 8, "N_kv": 2}, swa.SWA_OK),
+    ({"N": 8, "N_kv": 1}, swa.SWA_OK),
+    ({"N": 8, "N_kv": 8}, swa.SWA_OK),
+    ({"N": 8, "N_kv": 3}, swa.SWA_ERR_PARAM_INVALID),
+    ({"N": 4, "N_kv": 8}, swa.SWA_ERR_PARAM_INVALID),
+    ({"N": 4, "N_kv": -2}, swa.SWA_ERR_PARAM_INVALID),
 ])
 def test_parameter_checks(lib, change, status):
     st, _ = _size(Geometry(**{**BASE, **change}))

@@ -122,6 +122,18 @@ SMALL = {
                                         pre_tokens=100, next_tokens=17, keep_prob=0.85),
     "tnd_rect": dict(layout="TND", B=3, N=2, D=128, cu_seqlens_q=[50, 300, 310], cu_seqlens_kv=[170, 180, 420],
                      scale=0.09, sparse_mode=4, pre_tokens=64, next_tokens=64),
+    # grouped key/value heads (query head n reads key/value head n // (N / N_kv))
+    "bnsd_gqa4_band_d128_ragged": dict(layout="BNSD", B=1, N=8, N_kv=2, D=128, S_q=517, S_kv=517,
+                                       scale=128 ** -0.5, sparse_mode=4, pre_tokens=200, next_tokens=0),
+    "bnsd_mqa_nomask_d64": dict(layout="BNSD", B=2, N=4, N_kv=1, D=64, S_q=300, S_kv=300, scale=0.125,
+                                sparse_mode=0),
+    "bnsd_gqa2_band_dropout_d64": dict(layout="BNSD", B=1, N=4, N_kv=2, D=64, S_q=333, S_kv=333, scale=0.125,
+                                       sparse_mode=4, pre_tokens=150, next_tokens=40, keep_prob=0.8),
+    "bnsd_gqa2_band_dropout_d128": dict(layout="BNSD", B=1, N=4, N_kv=2, D=128, S_q=290, S_kv=290, scale=0.09,
+                                        sparse_mode=4, pre_tokens=100, next_tokens=30, keep_prob=0.75),
+    "tnd_gqa2_varlen_band_d128": dict(layout="TND", B=3, N=4, N_kv=2, D=128, cu_seqlens_q=[200, 200, 520],
+                                      cu_seqlens_kv=[200, 200, 520], scale=0.09, sparse_mode=4, pre_tokens=100,
+                                      next_tokens=20),
 }
 
 
@@ -154,6 +166,17 @@ def test_repeat_calls_are_deterministic_forward():
     b = as_np(run_gpu(inp, backward=False))
     for k_ in a:
         assert np.array_equal(a[k_], b[k_])
+
+
+def test_repeat_calls_are_deterministic_backward():
+    # dQ, dK and dV accumulate in TMEM in a fixed order: no atomics, so two
+    # runs agree bit for bit (grouped heads included)
+    geom = Geometry(**SMALL["bnsd_gqa4_band_d128_ragged"])
+    inp = draw(geom, 78)
+    a = as_np(run_gpu(inp))
+    b = as_np(run_gpu(inp))
+    for k_ in a:
+        assert np.array_equal(a[k_], b[k_]), k_
 
 
 # ------------------------------------------------------ masked set, exact --
