@@ -73,6 +73,9 @@ def _load():
             lib.orc_backward_dq_rows.argtypes = [P, vp, vp, vp, vp, vp, i64, vp, vp]
             lib.orc_backward_dkv_cols.argtypes = [P, vp, vp, vp, vp, vp, i64, vp, vp, vp]
             lib.orc_key_ranges.argtypes = [P, i64, vp, vp, vp]
+            lib.orc_philox4x32_10.argtypes = [vp, vp, vp]
+            lib.orc_philox4x32_10.restype = None
+            lib.orc_generate_keep_mask.argtypes = [P, ctypes.c_uint64, ctypes.c_uint64, vp]
             _lib = lib
     return _lib
 
@@ -254,6 +257,33 @@ def key_ranges(pr: Problem, rows):
     hi = np.zeros(len(sel), dtype=np.int64)
     lib.orc_key_ranges(c.ref(), len(sel), _ptr(sel), _ptr(lo), _ptr(hi))
     return lo, hi
+
+
+def philox4x32_10(counter, key):
+    """Philox4x32-10 of a 4-word counter under a 2-word key -> 4 uint32 words."""
+    lib = _load()
+    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint32))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32))
+    out = np.zeros(4, dtype=np.uint32)
+    lib.orc_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def generate_keep_mask(pr: Problem, seed: int, offset: int) -> np.ndarray:
+    """The packed keep mask (uint8, drop_mask order) a dropout seed / offset pair stands for."""
+    lib = _load()
+    c = _Call(pr)
+    nbits = 0
+    if pr.layout == "BNSD":
+        nbits = pr.B * pr.N * pr.S_q * pr.S_kv
+    else:
+        pq = pk = 0
+        for eq, ek in zip(pr.cu_seqlens_q, pr.cu_seqlens_kv):
+            nbits += pr.N * max(0, eq - pq) * max(0, ek - pk)
+            pq, pk = eq, ek
+    mask = np.zeros((nbits + 7) // 8, dtype=np.uint8)
+    lib.orc_generate_keep_mask(c.ref(), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(mask))
+    return mask
 
 
 def flops(pr: Problem) -> float:

@@ -430,6 +430,57 @@ int orc_backward_dkv_cols(const orc_params *p, const double *q, const double *k,
   return 0;
 }
 
+/* ------------------------------------------------ generated dropout -- */
+
+/* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+ * easy as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplications by
+ * 0xD2511F53 and 0xCD9E8D57 on counter words 0 and 2; the new counter is
+ * (hi(c2*M1) ^ c1 ^ k0, lo(c2*M1), hi(c0*M0) ^ c3 ^ k1, lo(c0*M0)); the key is
+ * bumped by (0x9E3779B9, 0xBB67AE85) after every round. */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3], k0 = key[0], k1 = key[1];
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c0, p1 = (uint64_t)0xCD9E8D57u * c2;
+    const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0, n1 = (uint32_t)p1;
+    const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1, n3 = (uint32_t)p0;
+    c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The keep mask a seed / offset pair stands for, written in the packed
+ * element order of the drop_mask input (bit e of byte e>>3, LSB first).
+ * Element (query row r = statistics id, local key j) keeps iff
+ *   byte (j mod 16) of Philox4x32-10(counter = (j/16, lo32 r, hi32 r,
+ *   lo32 offset), key = (lo32 seed, hi32 seed)) < threshold,
+ * bytes taken little-endian across the four output words, threshold =
+ * round(keep_prob * 256) in [0, 256]. */
+int orc_generate_keep_mask(const orc_params *p, uint64_t seed, uint64_t offset, uint8_t *mask) {
+  const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  long thr = lround(p->keep_prob * 256.0);
+  if (thr < 0) thr = 0;
+  if (thr > 256) thr = 256;
+  for (int64_t b = 0; b < p->B; ++b) {
+    orc_seq s = seq_of(p, b);
+    for (int64_t n = 0; n < p->N; ++n)
+      for (int64_t i = 0; i < s.q_len; ++i) {
+        const int64_t r = stat_q(p, &s, b, n, i);
+        for (int64_t j = 0; j < s.kv_len; ++j) {
+          const uint32_t ctr[4] = {(uint32_t)(j >> 4), (uint32_t)r, (uint32_t)((uint64_t)r >> 32), (uint32_t)offset};
+          uint32_t o[4];
+          orc_philox4x32_10(ctr, key, o);
+          const uint32_t byte = (o[(j & 15) >> 2] >> (8 * (j & 3))) & 0xFFu;
+          const int64_t e = s.mask_base + (n * s.q_len + i) * s.kv_len + j;
+          if ((long)byte < thr) mask[e >> 3] |= (uint8_t)(1u << (e & 7));
+          else mask[e >> 3] &= (uint8_t)~(1u << (e & 7));
+        }
+      }
+  }
+  return 0;
+}
+
 /* Visible key range [lo, hi] of each query row (flat statistics ids); lo > hi
  * for an empty row.  Used to compare masked sets exactly. */
 int orc_key_ranges(const orc_params *p, int64_t nsel, const int64_t *sel, int64_t *lo, int64_t *hi) {

@@ -473,3 +473,52 @@ def test_gqa_rejects_non_multiple():
     geom = Geometry("BNSD", 1, 4, 8, S_q=8, S_kv=8, N_kv=3)
     with pytest.raises(ValueError):
         orc.forward(to_problem(geom), np.zeros((1, 4, 8, 8)), np.zeros((1, 3, 8, 8)), np.zeros((1, 3, 8, 8)))
+
+
+# ------------------------------------------------------ generated dropout --
+# Philox4x32-10 (Salmon et al., SC'11) is pinned by the known-answer vectors
+# published with its reference implementation (Random123): counter / key
+# all zeros, all ones, and the hex digits of pi.
+PHILOX_KAT = [
+    ([0, 0, 0, 0], [0, 0], [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]),
+    ([0xFFFFFFFF] * 4, [0xFFFFFFFF] * 2, [0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD]),
+    ([0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344], [0xA4093822, 0x299F31D0],
+     [0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1]),
+]
+
+
+@pytest.mark.parametrize("ctr,key,want", PHILOX_KAT)
+def test_philox_known_answers(ctr, key, want):
+    assert list(orc.philox4x32_10(ctr, key)) == want
+
+
+def _mask_bits(mask, nbits):
+    return np.unpackbits(mask, bitorder="little")[:nbits].astype(bool)
+
+
+@pytest.mark.parametrize("keep", [0.5, 0.9, 0.25])
+def test_generated_mask_keep_fraction(keep):
+    geom = Geometry("BNSD", 2, 3, 8, S_q=160, S_kv=200, keep_prob=keep)
+    pr = to_problem(geom)
+    bits = _mask_bits(orc.generate_keep_mask(pr, seed=1234, offset=7), geom.mask_bits())
+    p = round(keep * 256) / 256  # the generator's probability (an 8-bit threshold)
+    n = bits.size
+    # within 5 standard deviations of the binomial mean
+    assert abs(bits.sum() - p * n) <= 5 * math.sqrt(n * p * (1 - p))
+    # and no structure along keys: the 16 key positions of a block keep alike
+    by_pos = bits.reshape(-1, 200)[:, :192].reshape(-1, 16).mean(axis=0)
+    assert np.all(np.abs(by_pos - p) < 0.05)
+
+
+def test_generated_mask_seed_offset_and_bounds():
+    geom = Geometry("TND", 3, 2, 8, cu_seqlens_q=[40, 40, 97], cu_seqlens_kv=[35, 50, 120], keep_prob=0.8)
+    pr = to_problem(geom)
+    m0 = orc.generate_keep_mask(pr, 5, 0)
+    assert np.array_equal(m0, orc.generate_keep_mask(pr, 5, 0))
+    assert not np.array_equal(m0, orc.generate_keep_mask(pr, 6, 0))
+    assert not np.array_equal(m0, orc.generate_keep_mask(pr, 5, 1))
+    # keep_prob 1 keeps everything, a threshold of 0 nothing
+    one = to_problem(Geometry(**{**geom.as_dict(), "keep_prob": 1.0}))
+    assert _mask_bits(orc.generate_keep_mask(one, 5, 0), geom.mask_bits()).all()
+    zero = to_problem(Geometry(**{**geom.as_dict(), "keep_prob": 1e-4}))
+    assert not _mask_bits(orc.generate_keep_mask(zero, 5, 0), geom.mask_bits()).any()
