@@ -121,6 +121,14 @@ swa_status_t make_plan(const swa_params_t* p, Plan& plan) {
   g.scale = static_cast<float>(p->scale);
   g.scale_log2 = static_cast<float>(p->scale * kLog2e);
   g.inv_keep = static_cast<float>(1.0 / p->keep_prob);
+  if (p->dropout_gen != 0 && p->dropout_gen != 1)
+    return fail(SWA_ERR_PARAM_INVALID, "dropout_gen should be 0 or 1, got %d", p->dropout_gen);
+  g.has_mask = p->keep_prob < 1.0;
+  g.drop_gen = (p->dropout_gen == 1 && p->keep_prob < 1.0) ? 1 : 0;
+  g.seed_lo = static_cast<uint32_t>(p->dropout_seed);
+  g.seed_hi = static_cast<uint32_t>(p->dropout_seed >> 32);
+  g.off_lo = static_cast<uint32_t>(p->dropout_offset);
+  g.keep_thr = static_cast<uint32_t>(std::min(256L, std::max(0L, std::lround(p->keep_prob * 256.0))));
 
   int64_t max_len = 0;
   if (p->layout == SWA_LAYOUT_BNSD) {
@@ -381,8 +389,10 @@ swa_status_t swa_forward(const swa_params_t* p, const void* q, const void* k, co
   if (st != SWA_OK) return st;
   if (!q || !k || !v || !out || !softmax_max || !softmax_sum)
     return fail(SWA_ERR_PARAM_NULLPTR, "a required tensor pointer is NULL");
-  if ((p->keep_prob < 1.0) != (drop_mask != nullptr))
-    return fail(SWA_ERR_PARAM_INVALID, "drop_mask must be given iff keep_prob < 1 (keep_prob = %g)", p->keep_prob);
+  if ((p->keep_prob < 1.0 && p->dropout_gen == 0) != (drop_mask != nullptr))
+    return fail(SWA_ERR_PARAM_INVALID,
+                "drop_mask must be given iff keep_prob < 1 and dropout_gen == 0 (keep_prob = %g, dropout_gen = %d)",
+                p->keep_prob, p->dropout_gen);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(softmax_max) ||
       !aligned16(softmax_sum) || !aligned16(drop_mask))
     return fail(SWA_ERR_PARAM_INVALID, "tensor pointers (and drop_mask) must be 16-byte aligned");
@@ -397,7 +407,6 @@ swa_status_t swa_forward(const swa_params_t* p, const void* q, const void* k, co
 
   FwdArgs a{};
   a.g = plan.g;
-  a.g.has_mask = drop_mask != nullptr;
   a.mask = drop_mask;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.smax = softmax_max;
@@ -425,8 +434,10 @@ swa_status_t swa_backward(const swa_params_t* p, const void* q, const void* k, c
   if (st != SWA_OK) return st;
   if (!q || !k || !v || !dy || !out || !softmax_max || !softmax_sum || !dq || !dk || !dv)
     return fail(SWA_ERR_PARAM_NULLPTR, "a required tensor pointer is NULL");
-  if ((p->keep_prob < 1.0) != (drop_mask != nullptr))
-    return fail(SWA_ERR_PARAM_INVALID, "drop_mask must be given iff keep_prob < 1 (keep_prob = %g)", p->keep_prob);
+  if ((p->keep_prob < 1.0 && p->dropout_gen == 0) != (drop_mask != nullptr))
+    return fail(SWA_ERR_PARAM_INVALID,
+                "drop_mask must be given iff keep_prob < 1 and dropout_gen == 0 (keep_prob = %g, dropout_gen = %d)",
+                p->keep_prob, p->dropout_gen);
   for (const void* ptr : {q, k, v, dy, out, static_cast<const void*>(drop_mask), static_cast<const void*>(softmax_max),
                           static_cast<const void*>(softmax_sum), static_cast<const void*>(dq),
                           static_cast<const void*>(dk), static_cast<const void*>(dv)})
@@ -463,7 +474,6 @@ swa_status_t swa_backward(const swa_params_t* p, const void* q, const void* k, c
 
   BwdArgs a{};
   a.g = plan.g;
-  a.g.has_mask = drop_mask != nullptr;
   a.mask = drop_mask;
   a.lse2 = lse2;
   a.dsum = dsum;
@@ -487,6 +497,30 @@ swa_status_t swa_backward(const swa_params_t* p, const void* q, const void* k, c
       [&](const SeqTable<kLargeTable>& t) { return launch_backward_dq(a, t, mq, mk, mv, mdy, s); });
   if (t_ev[5]) cudaEventRecord(t_ev[5], s);
   if (e != cudaSuccess) return cuda_fail(e, "backward dQ launch");
+  return SWA_OK;
+}
+
+swa_status_t swa_dropout_mask(const swa_params_t* p, uint8_t* mask, size_t mask_bytes, swa_stream_t stream) {
+  Plan plan;
+  swa_status_t st = make_plan(p, plan);
+  if (st != SWA_OK) return st;
+  if (!mask) return fail(SWA_ERR_PARAM_NULLPTR, "mask is NULL");
+  const size_t need = static_cast<size_t>((plan.mask_bits + 127) / 128) * 16;
+  if (mask_bytes < need)
+    return fail(SWA_ERR_WORKSPACE, "mask needs %zu bytes (16-byte multiple of the packed bits), got %zu", need,
+                mask_bytes);
+  if (!aligned16(mask)) return fail(SWA_ERR_PARAM_INVALID, "mask must be 16-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(mask, 0, mask_bytes, s);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the mask");
+  MaskGenArgs a{};
+  a.g = plan.g;
+  a.mask = reinterpret_cast<uint32_t*>(mask);
+  const std::vector<SeqDesc> descs = build_descs(plan, true);
+  e = run_tables(
+      descs, [&](const SeqTable<kSmallTable>& t) { return launch_dropout_mask(a, t, s); },
+      [&](const SeqTable<kLargeTable>& t) { return launch_dropout_mask(a, t, s); });
+  if (e != cudaSuccess) return cuda_fail(e, "dropout mask launch");
   return SWA_OK;
 }
 

@@ -7,7 +7,7 @@
 // Both layouts address a query row (b, n, i) / (t, n) the same way once
 // flattened: row id r -> elements [r*D, r*D + D), statistics index r.
 #include "swa_internal.h"
-#include "sm103.cuh"
+#include "swa_device.cuh"
 
 namespace swa {
 namespace {
@@ -53,7 +53,42 @@ __global__ void __launch_bounds__(256) swa_prep_kernel(const PrepArgs a) {
   }
 }
 
+// The keep mask a seed / offset pair stands for, in the packed drop_mask
+// layout: thread = one query row of a 128-row tile; it generates its row's
+// keep bits 16 keys at a time and ORs them into the zeroed 32-bit words (a
+// 16-bit group may straddle two words).
+template <int CAP>
+__global__ void __launch_bounds__(128) swa_dropmask_kernel(const MaskGenArgs a, const __grid_constant__ SeqTable<CAP> tab) {
+  const Geometry& g = a.g;
+  const Item w = resolve_item(tab, g, static_cast<int>(blockIdx.x), g.N);
+  const SeqInfo sq = w.s;
+  const int i = w.tile * kTileM + static_cast<int>(threadIdx.x);
+  if (i >= sq.q_len) return;
+  const int64_t row = stat_index(g, sq, w.b, w.n, i);
+  const int64_t e_row = sq.mask_base + (static_cast<int64_t>(w.n) * sq.q_len + i) * sq.kv_len;
+  const int nblk = (sq.kv_len + 15) / 16;
+  for (int kb = 0; kb < nblk; ++kb) {
+    uint32_t bits = gen_keep16(g, row, kb);
+    const int cnt = min(16, sq.kv_len - kb * 16);
+    if (cnt < 16) bits &= (1u << cnt) - 1u;
+    if (!bits) continue;
+    const int64_t e = e_row + kb * 16;
+    const int sh = static_cast<int>(e & 31);
+    atomicOr(&a.mask[e >> 5], bits << sh);
+    if (sh > 16) atomicOr(&a.mask[(e >> 5) + 1], bits >> (32 - sh));
+  }
+}
+
 }  // namespace
+
+template <int CAP>
+cudaError_t launch_dropout_mask(const MaskGenArgs& a, const SeqTable<CAP>& tab, cudaStream_t stream) {
+  if (tab.n_items == 0) return cudaSuccess;
+  swa_dropmask_kernel<CAP><<<tab.n_items, 128, 0, stream>>>(a, tab);
+  return cudaGetLastError();
+}
+template cudaError_t launch_dropout_mask<kSmallTable>(const MaskGenArgs&, const SeqTable<kSmallTable>&, cudaStream_t);
+template cudaError_t launch_dropout_mask<kLargeTable>(const MaskGenArgs&, const SeqTable<kLargeTable>&, cudaStream_t);
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream) {
   if (a.rows == 0) return cudaSuccess;

@@ -56,6 +56,7 @@ struct DkvSmem {
   // per-region barriers where the two issuers hand off, so that no waiter
   // can be a full phase behind
   uint64_t s_full[2], s_loaded, dp_full, pds_full[2], region_free[2], mma_done, drain_sdp, drain_kv;
+  uint64_t gen_full[2];  // generated keep bits of the tile in that stage written (compute threads)
   uint32_t tmem_base;
 };
 constexpr size_t kMaxSmem = 232448;
@@ -79,11 +80,12 @@ __device__ __forceinline__ bool compute_wait(uint64_t* bar, uint32_t parity, int
 }
 __device__ __forceinline__ uint32_t region(int it) { return (it & 1) * 128u; }
 
-template <int D, bool DROP, int CAP>
+template <int D, int DM, int CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_bwd_dkv_kernel(const BwdArgs a, const __grid_constant__ SeqTable<CAP> tab,
                        const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                        const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdy) {
+  constexpr bool DROP = DM != 0;
   using Smem = DkvSmem<D, DROP>;
   constexpr int kQS = Smem::kQStages;
   extern __shared__ uint8_t smem_raw[];
@@ -128,6 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.dy_full[st], 1);
       mbar_init(&s.dy_empty[st], 1);
       mbar_init(&s.stat_full[st], 32);
+      mbar_init(&s.gen_full[st], kComputeThreads);
       mbar_init(&s.s_full[st], 1);
     }
     mbar_init(&s.s_loaded, kComputeThreads);
@@ -198,11 +201,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t si = stat_index(g, sq, w.b, qn, i);
             l2 = a.lse2[si];
             dd = a.dsum[si];
-            if constexpr (DROP) load_keep_bits(a.mask, sq, qn, i, j0, bits);
+            if constexpr (DM == 1) load_keep_bits(a.mask, sq, qn, i, j0, bits);
           }
           s.lse2[st][c] = l2;
           s.dsum[st][c] = dd;
-          if constexpr (DROP) {
+          if constexpr (DM == 1) {
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) s.keep.w[st][c][q4] = bits[q4];
           }
@@ -310,6 +313,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       qhi = 0;
     }
     bool ok = true;
+    // Generated keep bits (DM == 2): thread (r, h) writes the words for keys
+    // [64h, 64h + 64) of query row r of a tile into the stage the consumers
+    // read (row r's four words, as the producer fills them from a mask).
+    auto gen_tile_bits = [&](int it2) {
+      const int stage = it2 & 1;
+      const int qn = w.n * g.group + it2 / n_q;
+      const int row_i = (q_t0 + it2 % n_q) * kTileM + r;
+      uint32_t words[2];
+      gen_keep_words<2>(g, stat_index(g, sq, w.b, qn, row_i), (j0 + cbase) >> 4, words);
+      if constexpr (DROP) {
+        s.keep.w[stage][r][2 * h] = words[0];
+        s.keep.w[stage][r][2 * h + 1] = words[1];
+      }
+      mbar_arrive(&s.gen_full[stage]);
+    };
+    if (DM == 2 && n_it > 0) gen_tile_bits(0);
     for (int it = 0; it < n_it; ++it) {
       const int st = it & 1;
       const int i0 = (q_t0 + it % n_q) * kTileM;
@@ -358,7 +377,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // ---- next tile's generated keep bits, into the stage tile it-1 used
+      // once every thread is through with tile it-1 (its pds_full)
+      if (DM == 2 && it + 1 < n_it) {
+        if (it >= 1 && !compute_wait(&s.pds_full[(it - 1) & 1], ((it - 1) >> 1) & 1, a.err)) { ok = false; break; }
+        gen_tile_bits(it + 1);
+      }
       // ---- dP^T -> dS^T; P^T*z/keep and dS^T packed bf16 into the same columns
+      if (DM == 2 && !compute_wait(&s.gen_full[st], (it >> 1) & 1, a.err)) { ok = false; break; }
       if (!compute_wait(&s.dp_full, it & 1, a.err)) { ok = false; break; }
       tc_fence_after_sync();
       uint32_t pk[32], dk[32];
@@ -434,18 +460,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool DROP, int CAP>
+template <int D, int DM, int CAP>
 cudaError_t launch_dkv_t(const BwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, const CUtensorMap& mdy, cudaStream_t stream) {
+  constexpr bool DROP = DM != 0;
   const size_t smem = sizeof(DkvSmem<D, DROP>) + (kDkvSlack<D, DROP> ? 1024 : 0);
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(swa_bwd_dkv_kernel<D, DROP, CAP>,
+    cudaError_t e = cudaFuncSetAttribute(swa_bwd_dkv_kernel<D, DM, CAP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  swa_bwd_dkv_kernel<D, DROP, CAP><<<tab.n_items, kThreads, smem, stream>>>(a, tab, mq, mk, mv, mdy);
+  swa_bwd_dkv_kernel<D, DM, CAP><<<tab.n_items, kThreads, smem, stream>>>(a, tab, mq, mk, mv, mdy);
   return cudaGetLastError();
 }
 
@@ -456,11 +483,14 @@ cudaError_t launch_backward_dkv(const BwdArgs& a, const SeqTable<CAP>& tab, cons
                                 const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdy,
                                 cudaStream_t stream) {
   if (tab.n_items == 0) return cudaSuccess;
-  const bool drop = a.g.has_mask != 0;
-  if (a.g.D == 64) return drop ? launch_dkv_t<64, true>(a, tab, mq, mk, mv, mdy, stream)
-                               : launch_dkv_t<64, false>(a, tab, mq, mk, mv, mdy, stream);
-  return drop ? launch_dkv_t<128, true>(a, tab, mq, mk, mv, mdy, stream)
-              : launch_dkv_t<128, false>(a, tab, mq, mk, mv, mdy, stream);
+  switch (drop_mode_of(a.g.has_mask, a.g.drop_gen) * 2 + (a.g.D == 64 ? 0 : 1)) {
+    case 0: return launch_dkv_t<64, 0>(a, tab, mq, mk, mv, mdy, stream);
+    case 1: return launch_dkv_t<128, 0>(a, tab, mq, mk, mv, mdy, stream);
+    case 2: return launch_dkv_t<64, 1>(a, tab, mq, mk, mv, mdy, stream);
+    case 3: return launch_dkv_t<128, 1>(a, tab, mq, mk, mv, mdy, stream);
+    case 4: return launch_dkv_t<64, 2>(a, tab, mq, mk, mv, mdy, stream);
+    default: return launch_dkv_t<128, 2>(a, tab, mq, mk, mv, mdy, stream);
+  }
 }
 
 template cudaError_t launch_backward_dkv<kSmallTable>(const BwdArgs&, const SeqTable<kSmallTable>&,

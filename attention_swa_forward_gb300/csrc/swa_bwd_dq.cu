@@ -55,7 +55,7 @@ __device__ __forceinline__ bool compute_wait(uint64_t* bar, uint32_t parity, int
   return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, err, kErrBwdCompute));
 }
 
-template <int D, bool DROP, int CAP>
+template <int D, int DM, int CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_bwd_dq_kernel(const BwdArgs a, const __grid_constant__ SeqTable<CAP> tab, const __grid_constant__ CUtensorMap mq,
                       const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
@@ -239,23 +239,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       lse2 = a.lse2[si];
       drow = a.dsum[si];
     }
+    // keep bits of this thread's 64 key columns of key tile j (two words)
     auto fetch_bits = [&](int j, uint32_t& kb0, uint32_t& kb1) {
       kb0 = kb1 = 0xFFFFFFFFu;
-      if (DROP && row_valid) {
+      if (DM == 1 && row_valid) {
         uint32_t bits[4];
         load_keep_bits(a.mask, sq, w.n, i, (kv_t0 + j) * kTileN, bits);
         kb0 = h ? bits[2] : bits[0];
         kb1 = h ? bits[3] : bits[1];
+      } else if (DM == 2) {
+        uint32_t bits[2];
+        gen_keep_words<2>(g, stat_index(g, sq, w.b, w.n, i), ((kv_t0 + j) * kTileN + cbase) >> 4, bits);
+        kb0 = bits[0];
+        kb1 = bits[1];
       }
     };
     uint32_t n_kb0 = 0xFFFFFFFFu, n_kb1 = 0xFFFFFFFFu;
-    if (DROP && n_kv > 0) fetch_bits(0, n_kb0, n_kb1);
+    if (DM != 0 && n_kv > 0) fetch_bits(0, n_kb0, n_kb1);
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const int b = j & 1;
       const uint32_t u = (j >> 1) & 1;
       const uint32_t kb0 = n_kb0, kb1 = n_kb1;
-      if (DROP && j + 1 < n_kv) fetch_bits(j + 1, n_kb0, n_kb1);
+      if (DM != 0 && j + 1 < n_kv) fetch_bits(j + 1, n_kb0, n_kb1);
       const int jb = (kv_t0 + j) * kTileN;
       const bool full = tile_fully_visible(g, sq, q0, jb);
 
@@ -307,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int uu = 0; uu < 2; ++uu) {
             const int t = 2 * t2 + uu;
             float dp = __uint_as_float(t < 32 ? d0[t] : d1[t - 32]);
-            if (DROP) {
+            if (DM != 0) {
               const bool keep = ((t < 32 ? kb0 : kb1) >> (t & 31)) & 1u;
               dp = keep ? dp * g.inv_keep : 0.f;
             }
@@ -357,18 +363,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool DROP, int CAP>
+template <int D, int DM, int CAP>
 cudaError_t launch_dq_t(const BwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdy, cudaStream_t stream) {
   const size_t smem = sizeof(DqSmem<D>) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(swa_bwd_dq_kernel<D, DROP, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(swa_bwd_dq_kernel<D, DM, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  swa_bwd_dq_kernel<D, DROP, CAP><<<tab.n_items, kThreads, smem, stream>>>(a, tab, mq, mk, mv, mdy);
+  swa_bwd_dq_kernel<D, DM, CAP><<<tab.n_items, kThreads, smem, stream>>>(a, tab, mq, mk, mv, mdy);
   return cudaGetLastError();
 }
 
@@ -379,11 +385,14 @@ cudaError_t launch_backward_dq(const BwdArgs& a, const SeqTable<CAP>& tab, const
                                const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdy,
                                cudaStream_t stream) {
   if (tab.n_items == 0) return cudaSuccess;
-  const bool drop = a.g.has_mask != 0;
-  if (a.g.D == 64) return drop ? launch_dq_t<64, true>(a, tab, mq, mk, mv, mdy, stream)
-                               : launch_dq_t<64, false>(a, tab, mq, mk, mv, mdy, stream);
-  return drop ? launch_dq_t<128, true>(a, tab, mq, mk, mv, mdy, stream)
-              : launch_dq_t<128, false>(a, tab, mq, mk, mv, mdy, stream);
+  switch (drop_mode_of(a.g.has_mask, a.g.drop_gen) * 2 + (a.g.D == 64 ? 0 : 1)) {
+    case 0: return launch_dq_t<64, 0>(a, tab, mq, mk, mv, mdy, stream);
+    case 1: return launch_dq_t<128, 0>(a, tab, mq, mk, mv, mdy, stream);
+    case 2: return launch_dq_t<64, 1>(a, tab, mq, mk, mv, mdy, stream);
+    case 3: return launch_dq_t<128, 1>(a, tab, mq, mk, mv, mdy, stream);
+    case 4: return launch_dq_t<64, 2>(a, tab, mq, mk, mv, mdy, stream);
+    default: return launch_dq_t<128, 2>(a, tab, mq, mk, mv, mdy, stream);
+  }
 }
 
 template cudaError_t launch_backward_dq<kSmallTable>(const BwdArgs&, const SeqTable<kSmallTable>&, const CUtensorMap&,

@@ -135,6 +135,57 @@ __device__ __forceinline__ void load_keep_bits(const uint8_t* __restrict__ mask,
   }
 }
 
+// ------------------------------------------------- generated keep bits --
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC'11): ten rounds; each multiplies counter words 0 and 2
+// by 0xD2511F53 and 0xCD9E8D57 (32x32 -> 64 bits) and forms the new counter
+// (hi(c2*M1) ^ c1 ^ k0, lo(c2*M1), hi(c0*M0) ^ c3 ^ k1, lo(c0*M0)); the key
+// is bumped by (0x9E3779B9, 0xBB67AE85) after every round.
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                               uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+    const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return make_uint4(c0, c1, c2, c3);
+}
+
+// Bit m (0..3) set iff byte m of w is below thr (thr in 0..256).
+__device__ __forceinline__ uint32_t keep4(uint32_t w, uint32_t thr) {
+  if (thr >= 256u) return 0xFu;
+  const uint32_t m = __vcmpltu4(w, thr * 0x01010101u) & 0x01010101u;  // 1 per kept byte
+  return (m * 0x10204080u) >> 28;  // gathers the four byte flags into bits 28..31
+}
+
+// Keep bits of query row `row` (its statistics id) for local keys
+// [16*kb, 16*kb + 16): bit m is key 16*kb + m.  The element is kept iff byte
+// (j mod 16) of Philox4x32-10(counter = (j/16, lo32 row, hi32 row, lo32
+// offset), key = seed) is below keep_thr, bytes little-endian across the
+// four output words.
+__device__ __forceinline__ uint32_t gen_keep16(const Geometry& g, int64_t row, int kb) {
+  const uint4 r = philox4x32_10(static_cast<uint32_t>(kb), static_cast<uint32_t>(row),
+                                static_cast<uint32_t>(static_cast<uint64_t>(row) >> 32), g.off_lo, g.seed_lo,
+                                g.seed_hi);
+  return keep4(r.x, g.keep_thr) | (keep4(r.y, g.keep_thr) << 4) | (keep4(r.z, g.keep_thr) << 8) |
+         (keep4(r.w, g.keep_thr) << 12);
+}
+
+// NW 32-bit keep words of row `row` for local keys [16*kb0, 16*kb0 + 32*NW):
+// bit t of word t>>5 is key 16*kb0 + t (the layout load_keep_bits returns).
+template <int NW>
+__device__ __forceinline__ void gen_keep_words(const Geometry& g, int64_t row, int kb0, uint32_t* words) {
+#pragma unroll
+  for (int q = 0; q < NW; ++q) words[q] = gen_keep16(g, row, kb0 + 2 * q) | (gen_keep16(g, row, kb0 + 2 * q + 1) << 16);
+}
+
 // Write 8 bf16 (one 16-byte chunk) of row r, chunk index c (0..15 over a
 // 128-wide row spanning two atom columns) into a swizzled tile.
 __device__ __forceinline__ void st_chunk_sw128(uint8_t* tile, int r, int c, uint4 v) {

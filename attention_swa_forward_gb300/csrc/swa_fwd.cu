@@ -45,7 +45,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 // until then the stale max is kept and p may reach 256, far from overflow.
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D, bool DROP, int CAP>
+template <int D, int DM, int CAP>
 __global__ void __launch_bounds__(224, 1)
     swa_fwd_kernel(const FwdArgs a, const __grid_constant__ SeqTable<CAP> tab, const __grid_constant__ CUtensorMap mq,
                    const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
@@ -251,9 +251,11 @@ __global__ void __launch_bounds__(224, 1)
       }
       const float msub = (m_use == -INFINITY) ? 0.f : m_use;
       uint32_t bits[4] = {~0u, ~0u, ~0u, ~0u};
-      if (DROP) {
+      if (DM == 1) {
         bits[0] = bits[1] = bits[2] = bits[3] = 0u;
         if (row_valid) load_keep_bits(a.mask, sq, w.n, i, j0, bits);
+      } else if (DM == 2) {
+        gen_keep_words<4>(g, stat_index(g, sq, w.b, w.n, i), j0 >> 4, bits);
       }
       // p = exp2(.), the row sum of p (before dropout), then P = p*z packed
       // to bf16 pairs in place: xr[t/2] receives the pair (t, t+1)
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__(224, 1)
         p0 = ex2_approx(p0);
         p1 = ex2_approx(p1);
         fadd2_acc(r8[(t >> 1) & 3], r8[4 + ((t >> 1) & 3)], p0, p1);
-        if (DROP) {
+        if (DM != 0) {
           p0 = ((bits[t >> 5] >> (t & 31)) & 1u) ? p0 : 0.f;
           p1 = ((bits[(t + 1) >> 5] >> ((t + 1) & 31)) & 1u) ? p1 : 0.f;
         }
@@ -356,18 +358,18 @@ __global__ void __launch_bounds__(224, 1)
   }
 }
 
-template <int D, bool DROP, int CAP>
+template <int D, int DM, int CAP>
 cudaError_t launch_fwd_t(const FwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, cudaStream_t stream) {
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(swa_fwd_kernel<D, DROP, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(swa_fwd_kernel<D, DM, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  swa_fwd_kernel<D, DROP, CAP><<<tab.n_items, 224, smem, stream>>>(a, tab, mq, mk, mv);
+  swa_fwd_kernel<D, DM, CAP><<<tab.n_items, 224, smem, stream>>>(a, tab, mq, mk, mv);
   return cudaGetLastError();
 }
 
@@ -377,11 +379,14 @@ template <int CAP>
 cudaError_t launch_forward(const FwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, cudaStream_t stream) {
   if (tab.n_items == 0) return cudaSuccess;
-  const bool drop = a.g.has_mask != 0;
-  if (a.g.D == 64) return drop ? launch_fwd_t<64, true>(a, tab, mq, mk, mv, stream)
-                               : launch_fwd_t<64, false>(a, tab, mq, mk, mv, stream);
-  return drop ? launch_fwd_t<128, true>(a, tab, mq, mk, mv, stream)
-              : launch_fwd_t<128, false>(a, tab, mq, mk, mv, stream);
+  switch (drop_mode_of(a.g.has_mask, a.g.drop_gen) * 2 + (a.g.D == 64 ? 0 : 1)) {
+    case 0: return launch_fwd_t<64, 0>(a, tab, mq, mk, mv, stream);
+    case 1: return launch_fwd_t<128, 0>(a, tab, mq, mk, mv, stream);
+    case 2: return launch_fwd_t<64, 1>(a, tab, mq, mk, mv, stream);
+    case 3: return launch_fwd_t<128, 1>(a, tab, mq, mk, mv, stream);
+    case 4: return launch_fwd_t<64, 2>(a, tab, mq, mk, mv, stream);
+    default: return launch_fwd_t<128, 2>(a, tab, mq, mk, mv, stream);
+  }
 }
 
 template cudaError_t launch_forward<kSmallTable>(const FwdArgs&, const SeqTable<kSmallTable>&, const CUtensorMap&,

@@ -78,7 +78,10 @@ struct Geometry {
   float scale;        // score scale
   float scale_log2;   // scale * log2(e)
   float inv_keep;     // 1 / keep_prob
-  int32_t has_mask;   // drop_mask given
+  int32_t has_mask;   // dropout active (a drop_mask, or generated from seed / offset)
+  int32_t drop_gen;   // 1: keep bits generated from (seed, offset) instead of read
+  uint32_t seed_lo, seed_hi, off_lo;
+  uint32_t keep_thr;  // element kept iff its Philox byte < keep_thr (0..256)
 };
 
 struct FwdArgs {
@@ -113,6 +116,10 @@ struct PrepArgs {
   float* dsum;
 };
 
+// Dropout mode DM: 0 none, 1 keep bits read from the caller's mask, 2 keep
+// bits generated from (seed, offset).
+__host__ __device__ constexpr int drop_mode_of(int has_mask, int gen) { return has_mask ? (gen ? 2 : 1) : 0; }
+
 // Record `fmt` as the text of swa_last_error() on this thread; returns st.
 swa_status_t set_error(swa_status_t st, const char* fmt, ...);
 
@@ -130,5 +137,15 @@ cudaError_t launch_backward_dq(const BwdArgs& a, const SeqTable<CAP>& tab, const
                                const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdy,
                                cudaStream_t stream);
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream);
+
+// The packed keep mask a seed / offset pair stands for: one CTA per query
+// tile of a (batch, head) from the forward's work table, one thread per
+// query row; bits are OR-ed into the zeroed mask.
+struct MaskGenArgs {
+  Geometry g;
+  uint32_t* mask;  // 32-bit words of the packed mask, zeroed beforehand
+};
+template <int CAP>
+cudaError_t launch_dropout_mask(const MaskGenArgs& a, const SeqTable<CAP>& tab, cudaStream_t stream);
 
 }  // namespace swa

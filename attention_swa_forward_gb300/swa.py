@@ -51,6 +51,9 @@ class SwaParams(ctypes.Structure):
         ("sparse_mode", ctypes.c_int32),
         ("keep_prob", ctypes.c_double),
         ("N_kv", ctypes.c_int64),
+        ("dropout_gen", ctypes.c_int32),
+        ("dropout_seed", ctypes.c_uint64),
+        ("dropout_offset", ctypes.c_uint64),
     ]
 
 
@@ -83,6 +86,8 @@ def lib() -> ctypes.CDLL:
             L.swa_backward_noalloc.restype = st
             L.swa_workspace_status.argtypes = [vp, vp]
             L.swa_workspace_status.restype = st
+            L.swa_dropout_mask.argtypes = [P, vp, sz, vp]
+            L.swa_dropout_mask.restype = st
             L.swa_set_timing_events.argtypes = [vp]
             L.swa_set_timing_events.restype = None
             L.swa_last_error.argtypes = []
@@ -94,7 +99,7 @@ def lib() -> ctypes.CDLL:
 def exported_symbols():
     return ["swa_params_default", "swa_forward_workspace_size", "swa_forward", "swa_backward_workspace_size",
             "swa_backward", "swa_backward_noalloc", "swa_workspace_status", "swa_set_timing_events",
-            "swa_last_error"]
+            "swa_last_error", "swa_dropout_mask"]
 
 
 def _check(status: int):
@@ -128,6 +133,9 @@ class Params:
         c.sparse_mode = int(geom.sparse_mode)
         c.keep_prob = float(geom.keep_prob)
         c.N_kv = int(getattr(geom, "N_kv", 0) or 0)
+        c.dropout_gen = int(getattr(geom, "dropout_gen", 0) or 0)
+        c.dropout_seed = int(getattr(geom, "dropout_seed", 0) or 0) & (2**64 - 1)
+        c.dropout_offset = int(getattr(geom, "dropout_offset", 0) or 0) & (2**64 - 1)
 
     def ref(self):
         return ctypes.byref(self.c)
@@ -168,6 +176,11 @@ def swa_backward_noalloc(params: Params, q, k, v, dy, out, softmax_max, softmax_
 
 def swa_workspace_status(workspace, stream) -> int:
     return lib().swa_workspace_status(workspace, stream)
+
+
+def swa_dropout_mask(params: "Params", mask, mask_bytes: int, stream) -> int:
+    """Raw call: write the keep mask params' dropout seed / offset stand for."""
+    return lib().swa_dropout_mask(params.ref(), mask, mask_bytes, stream)
 
 
 _timing_handles = None
@@ -232,6 +245,15 @@ def backward(geom, q, k, v, dy, out, softmax_max, softmax_sum, drop_mask=None, d
                         _ptr(drop_mask), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
                         _stream_handle(stream)))
     return dq, dk, dv
+
+
+def dropout_mask(geom, device="cuda:0", stream=None):
+    """The packed keep mask (uint8 device tensor, drop_mask layout, padded to
+    a 16-byte multiple) that geom's dropout_seed / dropout_offset stand for."""
+    nbytes = (geom.mask_bits() + 127) // 128 * 16
+    mask = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+    _check(swa_dropout_mask(Params(geom), _ptr(mask), mask.numel(), _stream_handle(stream)))
+    return mask
 
 
 def check_workspace(workspace, stream=None):

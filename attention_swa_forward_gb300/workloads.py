@@ -40,6 +40,9 @@ class Geometry:
     sparse_mode: int = 0
     keep_prob: float = 1.0
     N_kv: int = 0  # key/value heads (grouped-query attention); 0 means N
+    dropout_gen: int = 0  # 1: the keep mask is the one dropout_seed / dropout_offset stand for
+    dropout_seed: int = 0
+    dropout_offset: int = 0
 
     def as_dict(self) -> dict:
         return asdict(self)
@@ -150,7 +153,7 @@ def draw(geom: Geometry, seed: int, lengths: tuple | None = None, with_dy: bool 
     dy = torch.randn(geom.q_shape(), generator=g).to(torch.bfloat16) if with_dy else None
     p_keep = geom.keep_prob if mask_keep is None else mask_keep
     mask = None
-    if geom.keep_prob < 1.0 or mask_keep is not None:
+    if (geom.keep_prob < 1.0 and not geom.dropout_gen) or mask_keep is not None:
         chunks = []
         for (lq, lk) in geom.seq_lens():
             for _ in range(geom.N):

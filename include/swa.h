@@ -28,6 +28,14 @@
  * 1 = keep.  Element order: BNSD e = ((b*N + n)*Sq + i)*Skv + j; TND
  * e = sum_{b'<b} N*Sq_b'*Skv_b' + (n*Sq_b + i)*Skv_b + j (no padding).
  * softmax_sum excludes dropout; kept probabilities are scaled by 1/keep_prob.
+ * Instead of a mask, a seed and an offset may stand for it (dropout_gen = 1;
+ * the pages' high-level backward regenerates the mask from seed / offset,
+ * SWA article §1.1): element (query row r, local key j) is kept iff byte
+ * (j mod 16) of Philox4x32-10(counter = (j/16, lo32 r, hi32 r,
+ * lo32 dropout_offset), key = (lo32 dropout_seed, hi32 dropout_seed)),
+ * bytes little-endian across the four output words, is below
+ * round(keep_prob * 256); r is the statistics index of the row (BNSD
+ * (b*N + n)*S_q + i, TND t*N + n).  swa_dropout_mask writes that mask out.
  *
  * Layouts (doc parameter list, inputLayout; PyPTO-Gym article, I/O table):
  *   BNSD  q, dy, out, dq: [B, N, S_q, D];  k, v, dk, dv: [B, N, S_kv, D]
@@ -101,6 +109,11 @@ typedef struct {
                                    query head n reads key/value head n / (N / N_kv).
                                    k, v, dk, dv then have N_kv heads ([B,N_kv,S_kv,D] or
                                    [T_kv,N_kv,D]).  0 (the default) means N_kv = N. */
+  int32_t dropout_gen;          /* 1: keep_prob < 1 with drop_mask NULL, the mask being the one
+                                   dropout_seed / dropout_offset stand for (see above); 0: the
+                                   caller's drop_mask.  Default 0. */
+  uint64_t dropout_seed;
+  uint64_t dropout_offset;
 } swa_params_t;
 
 /* Fill `p` with the documented defaults (FlashAttentionScore REG_OP
@@ -115,6 +128,7 @@ SWA_API swa_status_t swa_forward_workspace_size(const swa_params_t *p, size_t *b
 /* Forward (doc formula; PyPTO-Gym "前向公式").
  *   q, k, v       device, bf16, layout per p->layout
  *   drop_mask     device, packed keep bits, 16-byte aligned; NULL iff keep_prob == 1
+ *                 or dropout_gen == 1
  *   out           device, bf16, q's shape
  *   softmax_max   device, fp32, [B,N,S_q] or [T_q,N]
  *   softmax_sum   device, fp32, same shape
@@ -168,6 +182,17 @@ SWA_API swa_status_t swa_backward_noalloc(const swa_params_t *p, const void *q, 
 /* Wait for `stream`, then report whether any kernel of the last call that
  * used `workspace` gave up a bounded wait: SWA_OK or SWA_ERR_TIMEOUT
  * (SWA_ERR_CUDA if the stream itself failed). */
+/* Write the keep mask that p->dropout_seed / p->dropout_offset stand for
+ * (see "Dropout" above) in the drop_mask layout: ceil(bits / 8) bytes, bits =
+ * sum over sequences of N * Sq_b * Skv_b.  mask is device memory of
+ * mask_bytes bytes; bytes past the last element are zero.  It lets a caller
+ * keep or inspect the mask a seed-driven call used; the pages' low-level
+ * backward takes it as drop_mask.  Errors: the size query's,
+ * SWA_ERR_PARAM_NULLPTR, SWA_ERR_WORKSPACE (mask_bytes too small),
+ * SWA_ERR_CUDA. */
+SWA_API swa_status_t swa_dropout_mask(const swa_params_t *p, uint8_t *mask, size_t mask_bytes,
+                                      swa_stream_t stream);
+
 SWA_API swa_status_t swa_workspace_status(const void *workspace, swa_stream_t stream);
 
 /* Measurement support.  `events` is NULL (stop recording) or an array of six

@@ -98,6 +98,11 @@ class Problem:
     sparse_mode: int = 0
     keep_prob: float = 1.0
     N_kv: int = 0  # key/value heads (GQA / MQA); 0 means N
+    # A seed / offset standing for the dropout mask: the oracle does not use
+    # them directly; generate_keep_mask turns them into the mask it takes.
+    dropout_gen: int = 0
+    dropout_seed: int = 0
+    dropout_offset: int = 0
 
     @property
     def n_kv(self) -> int:
