@@ -244,9 +244,16 @@ def run_reference(args, g: Geometry, name: str):
 
 
 def workload_config(g: Geometry, name: str) -> dict:
+    q_bytes = 2 * int(np.prod(g.q_shape()))
+    l2 = ("inputs larger than L2 (q/k/v/dy each > 129 MB), no flush" if q_bytes > 129e6 else
+          "inputs smaller than L2, not flushed between steps")
     cfg = {"workload": name, "layout": g.layout, "B": g.B, "N": g.N, "D": g.D, "sparse_mode": g.sparse_mode,
            "pre_tokens": g.pre_tokens, "next_tokens": g.next_tokens, "keep_prob": g.keep_prob,
-           "scale": g.scale, "l2": "inputs larger than L2 (q/k/v/dy each > 129 MB), no flush"}
+           "scale": g.scale, "l2": l2}
+    if g.N_kv:
+        cfg["N_kv"] = g.N_kv
+    if g.keep_prob < 1.0:
+        cfg["dropout"] = "keep bits generated from seed / offset" if g.dropout_gen else "packed keep mask input"
     if g.layout == "BNSD":
         cfg.update(S_q=g.S_q, S_kv=g.S_kv)
     else:
@@ -273,6 +280,10 @@ def run_swa(args, name: str):
 
     w = WORKLOADS[name]
     geom = w.geom if args.heads is None else Geometry(**{**w.geom.as_dict(), "N": args.heads})
+    if args.keep_prob is not None:
+        geom = Geometry(**{**geom.as_dict(), "keep_prob": args.keep_prob})
+    if args.dropout_gen and geom.keep_prob < 1.0:  # keep bits from (seed, offset) instead of a mask
+        geom = Geometry(**{**geom.as_dict(), "dropout_gen": 1, "dropout_seed": w.seed, "dropout_offset": 0})
     inp = draw(geom, w.seed, w.lengths)
     g = inp.geom
     fl = flops(g)
@@ -420,6 +431,9 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=8192, help="positions per oracle sample (reference arm)")
+    ap.add_argument("--keep-prob", type=float, default=None, help="override the workload's keep_prob")
+    ap.add_argument("--dropout-gen", action="store_true",
+                    help="dropout workloads: generate the keep mask in the kernels from a seed / offset")
     ap.add_argument("--heads", type=int, default=None,
                     help="override the workload's head count N (smaller profiling captures)")
     args = ap.parse_args(argv)
