@@ -121,6 +121,11 @@ swa_status_t make_plan(const swa_params_t* p, Plan& plan) {
   g.scale = static_cast<float>(p->scale);
   g.scale_log2 = static_cast<float>(p->scale * kLog2e);
   g.inv_keep = static_cast<float>(1.0 / p->keep_prob);
+  if (p->dtype == SWA_DTYPE_FP32)
+    return fail(SWA_ERR_UNSUPPORTED, "FLOAT32 inputs are not built (bf16 and fp16 are)");
+  if (p->dtype != SWA_DTYPE_BF16 && p->dtype != SWA_DTYPE_FP16)
+    return fail(SWA_ERR_PARAM_INVALID, "dtype should be 0 (bf16), 1 (fp16) or 2 (fp32), got %d", p->dtype);
+  g.f16 = p->dtype == SWA_DTYPE_FP16 ? 1 : 0;
   if (p->dropout_gen != 0 && p->dropout_gen != 1)
     return fail(SWA_ERR_PARAM_INVALID, "dropout_gen should be 0 or 1, got %d", p->dropout_gen);
   g.has_mask = p->keep_prob < 1.0;
@@ -310,7 +315,7 @@ swa_status_t make_map(CUtensorMap* m, const void* ptr, const Plan& plan, bool q_
     strides[0] = D * es_bytes; strides[1] = N * D * es_bytes; strides[2] = T * N * D * es_bytes;
     box[0] = box_x; box[1] = 1; box[2] = kTileM; box[3] = 1;
   }
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+  CUresult r = fn(m, g.f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);

@@ -14,8 +14,15 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Two packed elements (bf16 or fp16) to floats.
+template <bool F16>
+__device__ __forceinline__ float2 unpack2(uint32_t v) {
+  if constexpr (F16) return __half22float2(*reinterpret_cast<const __half2*>(&v));
+  else return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+}
+
 // One warp per row; each lane handles D/32 consecutive elements.
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(256) swa_prep_kernel(const PrepArgs a) {
   constexpr int kPer = D / 32;  // 2 or 4 bf16 per lane
   const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -27,20 +34,19 @@ __global__ void __launch_bounds__(256) swa_prep_kernel(const PrepArgs a) {
   if (kPer == 4) {
     const uint2 dy = __ldg(reinterpret_cast<const uint2*>(a.dy + base));
     const uint2 o = __ldg(reinterpret_cast<const uint2*>(a.out + base));
-    const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dy);
-    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
+    const uint32_t d2[2] = {dy.x, dy.y}, o2[2] = {o.x, o.y};
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      const float2 df = __bfloat1622float2(d2[t]);
-      const float2 of = __bfloat1622float2(o2[t]);
+      const float2 df = unpack2<F16>(d2[t]);
+      const float2 of = unpack2<F16>(o2[t]);
       acc = fmaf(df.x, of.x, acc);
       acc = fmaf(df.y, of.y, acc);
     }
   } else {
     const uint32_t dy = __ldg(reinterpret_cast<const uint32_t*>(a.dy + base));
     const uint32_t o = __ldg(reinterpret_cast<const uint32_t*>(a.out + base));
-    const float2 df = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dy));
-    const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o));
+    const float2 df = unpack2<F16>(dy);
+    const float2 of = unpack2<F16>(o);
     acc = fmaf(df.x, of.x, acc);
     acc = fmaf(df.y, of.y, acc);
   }
@@ -95,10 +101,14 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream) {
   const int64_t threads = a.rows * 32;
   const int block = 256;
   const int64_t grid = (threads + block - 1) / block;
-  if (a.g.D == 64)
-    swa_prep_kernel<64><<<static_cast<unsigned>(grid), block, 0, stream>>>(a);
-  else
-    swa_prep_kernel<128><<<static_cast<unsigned>(grid), block, 0, stream>>>(a);
+  const unsigned gr = static_cast<unsigned>(grid);
+  if (a.g.D == 64) {
+    if (a.g.f16) swa_prep_kernel<64, true><<<gr, block, 0, stream>>>(a);
+    else swa_prep_kernel<64, false><<<gr, block, 0, stream>>>(a);
+  } else {
+    if (a.g.f16) swa_prep_kernel<128, true><<<gr, block, 0, stream>>>(a);
+    else swa_prep_kernel<128, false><<<gr, block, 0, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -80,7 +80,7 @@ __device__ __forceinline__ bool compute_wait(uint64_t* bar, uint32_t parity, int
 }
 __device__ __forceinline__ uint32_t region(int it) { return (it & 1) * 128u; }
 
-template <int D, int DM, int CAP>
+template <int D, int DM, bool F16, int CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_bwd_dkv_kernel(const BwdArgs a, const __grid_constant__ SeqTable<CAP> tab,
                        const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     // ----------------------------------------------------- tcgen05 issuer --
     if (lane == 0 && n_q > 0) {
-      constexpr uint32_t kIdT = idesc_bf16_f32(kTileN, kTileM, false, false);  // S^T, dP^T
+      constexpr uint32_t kIdT = idesc_f16_f32(kTileN, kTileM, false, false, F16);  // S^T, dP^T
       const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
       auto issue_ss = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {  // 128 x 128 x D, both K-major
 #pragma unroll
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 10) {
     // ------------------------------------------------- dV / dK issuer --
     if (lane == 0 && n_q > 0) {
-      constexpr uint32_t kIdKV = idesc_bf16_f32(kTileN, D, false, true);  // A = P^T / dS^T in TMEM
+      constexpr uint32_t kIdKV = idesc_f16_f32(kTileN, D, false, true, F16);  // A = P^T / dS^T in TMEM
       for (int it = 0; it < n_it; ++it) {
         const int st = it & 1, qs = it % kQS;
         // dV, dK from the P^T / dS^T the compute warps stored in region(it):
@@ -412,10 +412,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             pv[u] = pt;
             dsv[u] = p[t] * (dp - dv4[u]);
           }
-          pk[t4 * 2] = pack_bf16x2(pv[0], pv[1]);
-          pk[t4 * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-          dk[t4 * 2] = pack_bf16x2(dsv[0], dsv[1]);
-          dk[t4 * 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+          pk[t4 * 2] = pack2<F16>(pv[0], pv[1]);
+          pk[t4 * 2 + 1] = pack2<F16>(pv[2], pv[3]);
+          dk[t4 * 2] = pack2<F16>(dsv[0], dsv[1]);
+          dk[t4 * 2 + 1] = pack2<F16>(dsv[2], dsv[3]);
         }
       }
       tmem_st_32x32b_x32(col, pk);
@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (kv_valid) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(dst + ch * 32)[q4] = pack8(&o[q4 * 8]);
+          for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(dst + ch * 32)[q4] = pack8<F16>(&o[q4 * 8]);
         }
       }
     }
@@ -460,19 +460,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int DM, int CAP>
+template <int D, int DM, bool F16, int CAP>
 cudaError_t launch_dkv_t(const BwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, const CUtensorMap& mdy, cudaStream_t stream) {
   constexpr bool DROP = DM != 0;
   const size_t smem = sizeof(DkvSmem<D, DROP>) + (kDkvSlack<D, DROP> ? 1024 : 0);
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(swa_bwd_dkv_kernel<D, DM, CAP>,
+    cudaError_t e = cudaFuncSetAttribute(swa_bwd_dkv_kernel<D, DM, F16, CAP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  swa_bwd_dkv_kernel<D, DM, CAP><<<tab.n_items, kThreads, smem, stream>>>(a, tab, mq, mk, mv, mdy);
+  swa_bwd_dkv_kernel<D, DM, F16, CAP><<<tab.n_items, kThreads, smem, stream>>>(a, tab, mq, mk, mv, mdy);
   return cudaGetLastError();
 }
 
@@ -483,13 +483,20 @@ cudaError_t launch_backward_dkv(const BwdArgs& a, const SeqTable<CAP>& tab, cons
                                 const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdy,
                                 cudaStream_t stream) {
   if (tab.n_items == 0) return cudaSuccess;
-  switch (drop_mode_of(a.g.has_mask, a.g.drop_gen) * 2 + (a.g.D == 64 ? 0 : 1)) {
-    case 0: return launch_dkv_t<64, 0>(a, tab, mq, mk, mv, mdy, stream);
-    case 1: return launch_dkv_t<128, 0>(a, tab, mq, mk, mv, mdy, stream);
-    case 2: return launch_dkv_t<64, 1>(a, tab, mq, mk, mv, mdy, stream);
-    case 3: return launch_dkv_t<128, 1>(a, tab, mq, mk, mv, mdy, stream);
-    case 4: return launch_dkv_t<64, 2>(a, tab, mq, mk, mv, mdy, stream);
-    default: return launch_dkv_t<128, 2>(a, tab, mq, mk, mv, mdy, stream);
+  // (drop mode, D, element type) -> one of the twelve instantiations
+  switch ((drop_mode_of(a.g.has_mask, a.g.drop_gen) * 2 + (a.g.D == 64 ? 0 : 1)) * 2 + (a.g.f16 ? 1 : 0)) {
+    case 0: return launch_dkv_t<64, 0, false>(a, tab, mq, mk, mv, mdy, stream);
+    case 1: return launch_dkv_t<64, 0, true>(a, tab, mq, mk, mv, mdy, stream);
+    case 2: return launch_dkv_t<128, 0, false>(a, tab, mq, mk, mv, mdy, stream);
+    case 3: return launch_dkv_t<128, 0, true>(a, tab, mq, mk, mv, mdy, stream);
+    case 4: return launch_dkv_t<64, 1, false>(a, tab, mq, mk, mv, mdy, stream);
+    case 5: return launch_dkv_t<64, 1, true>(a, tab, mq, mk, mv, mdy, stream);
+    case 6: return launch_dkv_t<128, 1, false>(a, tab, mq, mk, mv, mdy, stream);
+    case 7: return launch_dkv_t<128, 1, true>(a, tab, mq, mk, mv, mdy, stream);
+    case 8: return launch_dkv_t<64, 2, false>(a, tab, mq, mk, mv, mdy, stream);
+    case 9: return launch_dkv_t<64, 2, true>(a, tab, mq, mk, mv, mdy, stream);
+    case 10: return launch_dkv_t<128, 2, false>(a, tab, mq, mk, mv, mdy, stream);
+    default: return launch_dkv_t<128, 2, true>(a, tab, mq, mk, mv, mdy, stream);
   }
 }
 

@@ -55,7 +55,7 @@ __device__ __forceinline__ bool compute_wait(uint64_t* bar, uint32_t parity, int
   return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, err, kErrBwdCompute));
 }
 
-template <int D, int DM, int CAP>
+template <int D, int DM, bool F16, int CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_bwd_dq_kernel(const BwdArgs a, const __grid_constant__ SeqTable<CAP> tab, const __grid_constant__ CUtensorMap mq,
                       const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     // ----------------------------------------------------- tcgen05 issuer --
     if (lane == 0 && n_kv > 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(kTileM, kTileN, false, false);  // S, dP
+      constexpr uint32_t kIdS = idesc_f16_f32(kTileM, kTileN, false, false, F16);  // S, dP
       const uint32_t q_addr = smem_u32(s.q), dy_addr = smem_u32(s.dy);
       auto issue_s = [&](int j) {  // S(j) = Q K_j^T
         const uint32_t k_addr = smem_u32(s.k[j % 3]);
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 10) {
     // ------------------------------------------------ dQ += dS K issuer --
     if (lane == 0 && n_kv > 0) {
-      constexpr uint32_t kIdQ = idesc_bf16_f32(kTileM, D, false, true);
+      constexpr uint32_t kIdQ = idesc_f16_f32(kTileM, D, false, true, F16);
       for (int j = 0; j < n_kv; ++j) {
         const int b = j & 1;
         if (!mbar_wait(&s.ds_full[b], (j >> 1) & 1, a.err, kErrBwdMma)) break;
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             dv[uu] = p[t] * (dp - drow);
           }
-          dk[t2] = pack_bf16x2(dv[0], dv[1]);
+          dk[t2] = pack2<F16>(dv[0], dv[1]);
         }
       }
       // ---- dS -> TMEM buffer b (after dQ(j-2) has read it)
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (row_valid) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(dst + ch * 32)[q4] = pack8(&o[q4 * 8]);
+          for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(dst + ch * 32)[q4] = pack8<F16>(&o[q4 * 8]);
         }
       }
     }
@@ -363,18 +363,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int DM, int CAP>
+template <int D, int DM, bool F16, int CAP>
 cudaError_t launch_dq_t(const BwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdy, cudaStream_t stream) {
   const size_t smem = sizeof(DqSmem<D>) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(swa_bwd_dq_kernel<D, DM, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(swa_bwd_dq_kernel<D, DM, F16, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  swa_bwd_dq_kernel<D, DM, CAP><<<tab.n_items, kThreads, smem, stream>>>(a, tab, mq, mk, mv, mdy);
+  swa_bwd_dq_kernel<D, DM, F16, CAP><<<tab.n_items, kThreads, smem, stream>>>(a, tab, mq, mk, mv, mdy);
   return cudaGetLastError();
 }
 
@@ -385,13 +385,20 @@ cudaError_t launch_backward_dq(const BwdArgs& a, const SeqTable<CAP>& tab, const
                                const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdy,
                                cudaStream_t stream) {
   if (tab.n_items == 0) return cudaSuccess;
-  switch (drop_mode_of(a.g.has_mask, a.g.drop_gen) * 2 + (a.g.D == 64 ? 0 : 1)) {
-    case 0: return launch_dq_t<64, 0>(a, tab, mq, mk, mv, mdy, stream);
-    case 1: return launch_dq_t<128, 0>(a, tab, mq, mk, mv, mdy, stream);
-    case 2: return launch_dq_t<64, 1>(a, tab, mq, mk, mv, mdy, stream);
-    case 3: return launch_dq_t<128, 1>(a, tab, mq, mk, mv, mdy, stream);
-    case 4: return launch_dq_t<64, 2>(a, tab, mq, mk, mv, mdy, stream);
-    default: return launch_dq_t<128, 2>(a, tab, mq, mk, mv, mdy, stream);
+  // (drop mode, D, element type) -> one of the twelve instantiations
+  switch ((drop_mode_of(a.g.has_mask, a.g.drop_gen) * 2 + (a.g.D == 64 ? 0 : 1)) * 2 + (a.g.f16 ? 1 : 0)) {
+    case 0: return launch_dq_t<64, 0, false>(a, tab, mq, mk, mv, mdy, stream);
+    case 1: return launch_dq_t<64, 0, true>(a, tab, mq, mk, mv, mdy, stream);
+    case 2: return launch_dq_t<128, 0, false>(a, tab, mq, mk, mv, mdy, stream);
+    case 3: return launch_dq_t<128, 0, true>(a, tab, mq, mk, mv, mdy, stream);
+    case 4: return launch_dq_t<64, 1, false>(a, tab, mq, mk, mv, mdy, stream);
+    case 5: return launch_dq_t<64, 1, true>(a, tab, mq, mk, mv, mdy, stream);
+    case 6: return launch_dq_t<128, 1, false>(a, tab, mq, mk, mv, mdy, stream);
+    case 7: return launch_dq_t<128, 1, true>(a, tab, mq, mk, mv, mdy, stream);
+    case 8: return launch_dq_t<64, 2, false>(a, tab, mq, mk, mv, mdy, stream);
+    case 9: return launch_dq_t<64, 2, true>(a, tab, mq, mk, mv, mdy, stream);
+    case 10: return launch_dq_t<128, 2, false>(a, tab, mq, mk, mv, mdy, stream);
+    default: return launch_dq_t<128, 2, true>(a, tab, mq, mk, mv, mdy, stream);
   }
 }
 

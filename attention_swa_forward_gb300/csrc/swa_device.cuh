@@ -193,12 +193,13 @@ __device__ __forceinline__ void st_chunk_sw128(uint8_t* tile, int r, int c, uint
   *reinterpret_cast<uint4*>(dst) = v;
 }
 
+template <bool F16>
 __device__ __forceinline__ uint4 pack8(const float* x) {
   uint4 v;
-  v.x = pack_bf16x2(x[0], x[1]);
-  v.y = pack_bf16x2(x[2], x[3]);
-  v.z = pack_bf16x2(x[4], x[5]);
-  v.w = pack_bf16x2(x[6], x[7]);
+  v.x = pack2<F16>(x[0], x[1]);
+  v.y = pack2<F16>(x[2], x[3]);
+  v.z = pack2<F16>(x[4], x[5]);
+  v.w = pack2<F16>(x[6], x[7]);
   return v;
 }
 

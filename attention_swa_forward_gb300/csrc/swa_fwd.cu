@@ -45,7 +45,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 // until then the stale max is kept and p may reach 256, far from overflow.
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D, int DM, int CAP>
+template <int D, int DM, bool F16, int CAP>
 __global__ void __launch_bounds__(224, 1)
     swa_fwd_kernel(const FwdArgs a, const __grid_constant__ SeqTable<CAP> tab, const __grid_constant__ CUtensorMap mq,
                    const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(224, 1)
   } else if (warp == 5) {
     // ------------------------------------------------ S = Q K^T issuer --
     if (lane == 0 && n_kv > 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(kTileM, kTileN, false, false);
+      constexpr uint32_t kIdS = idesc_f16_f32(kTileM, kTileN, false, false, F16);
       const uint32_t q_addr = smem_u32(s.q);
       bool ok = mbar_wait(&s.q_full, 0, a.err, kErrFwdMma);
       for (int it = 0; ok && it < n_kv; ++it) {
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(224, 1)
   } else if (warp == 6) {
     // ------------------------------------------------- O += P V issuer --
     if (lane == 0 && n_kv > 0) {
-      constexpr uint32_t kIdO = idesc_bf16_f32(kTileM, D, false, true);
+      constexpr uint32_t kIdO = idesc_f16_f32(kTileM, D, false, true, F16);
       for (int it = 0; it < n_kv; ++it) {
         const int pb = it & 1, st = it % kStages;
         if (!mbar_wait(&s.p_full[pb], (it >> 1) & 1, a.err, kErrFwdMma)) break;
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(224, 1)
           p0 = ((bits[t >> 5] >> (t & 31)) & 1u) ? p0 : 0.f;
           p1 = ((bits[(t + 1) >> 5] >> ((t + 1) & 31)) & 1u) ? p1 : 0.f;
         }
-        xr[t >> 1] = pack_bf16x2(p0, p1);
+        xr[t >> 1] = pack2<F16>(p0, p1);
       }
       const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
       l = l * alpha + rs;
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(224, 1)
         }
         if (row_valid) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(orow + ch * 32)[q4] = pack8(&o[q4 * 8]);
+          for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(orow + ch * 32)[q4] = pack8<F16>(&o[q4 * 8]);
         }
       }
       if (row_valid) {
@@ -358,18 +358,18 @@ __global__ void __launch_bounds__(224, 1)
   }
 }
 
-template <int D, int DM, int CAP>
+template <int D, int DM, bool F16, int CAP>
 cudaError_t launch_fwd_t(const FwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, cudaStream_t stream) {
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(swa_fwd_kernel<D, DM, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(swa_fwd_kernel<D, DM, F16, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  swa_fwd_kernel<D, DM, CAP><<<tab.n_items, 224, smem, stream>>>(a, tab, mq, mk, mv);
+  swa_fwd_kernel<D, DM, F16, CAP><<<tab.n_items, 224, smem, stream>>>(a, tab, mq, mk, mv);
   return cudaGetLastError();
 }
 
@@ -379,13 +379,20 @@ template <int CAP>
 cudaError_t launch_forward(const FwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, cudaStream_t stream) {
   if (tab.n_items == 0) return cudaSuccess;
-  switch (drop_mode_of(a.g.has_mask, a.g.drop_gen) * 2 + (a.g.D == 64 ? 0 : 1)) {
-    case 0: return launch_fwd_t<64, 0>(a, tab, mq, mk, mv, stream);
-    case 1: return launch_fwd_t<128, 0>(a, tab, mq, mk, mv, stream);
-    case 2: return launch_fwd_t<64, 1>(a, tab, mq, mk, mv, stream);
-    case 3: return launch_fwd_t<128, 1>(a, tab, mq, mk, mv, stream);
-    case 4: return launch_fwd_t<64, 2>(a, tab, mq, mk, mv, stream);
-    default: return launch_fwd_t<128, 2>(a, tab, mq, mk, mv, stream);
+  // (drop mode, D, element type) -> one of the twelve instantiations
+  switch ((drop_mode_of(a.g.has_mask, a.g.drop_gen) * 2 + (a.g.D == 64 ? 0 : 1)) * 2 + (a.g.f16 ? 1 : 0)) {
+    case 0: return launch_fwd_t<64, 0, false>(a, tab, mq, mk, mv, stream);
+    case 1: return launch_fwd_t<64, 0, true>(a, tab, mq, mk, mv, stream);
+    case 2: return launch_fwd_t<128, 0, false>(a, tab, mq, mk, mv, stream);
+    case 3: return launch_fwd_t<128, 0, true>(a, tab, mq, mk, mv, stream);
+    case 4: return launch_fwd_t<64, 1, false>(a, tab, mq, mk, mv, stream);
+    case 5: return launch_fwd_t<64, 1, true>(a, tab, mq, mk, mv, stream);
+    case 6: return launch_fwd_t<128, 1, false>(a, tab, mq, mk, mv, stream);
+    case 7: return launch_fwd_t<128, 1, true>(a, tab, mq, mk, mv, stream);
+    case 8: return launch_fwd_t<64, 2, false>(a, tab, mq, mk, mv, stream);
+    case 9: return launch_fwd_t<64, 2, true>(a, tab, mq, mk, mv, stream);
+    case 10: return launch_fwd_t<128, 2, false>(a, tab, mq, mk, mv, stream);
+    default: return launch_fwd_t<128, 2, true>(a, tab, mq, mk, mv, stream);
   }
 }
 

@@ -72,6 +72,7 @@ struct Geometry {
   int32_t N, D;
   int32_t N_kv;    // key/value heads; query head n reads key/value head n / group
   int32_t group;   // N / N_kv
+  int32_t f16;     // element type of q, k, v, dy, out, dq, dk, dv: 0 bf16, 1 fp16
   int32_t S_q, S_kv;  // BNSD (per-batch lengths)
   int32_t sparse_mode;
   int32_t pre, next;  // clamped into +-(max sequence length + 1)

@@ -23,6 +23,7 @@ SWA_ERR_WORKSPACE = 161101
 SWA_ERR_CUDA = 161102
 SWA_ERR_TIMEOUT = 161103
 LAYOUTS = {"BNSD": 0, "TND": 1}
+DTYPES = {"bf16": 0, "fp16": 1, "fp32": 2}
 
 
 class SwaError(RuntimeError):
@@ -54,6 +55,7 @@ class SwaParams(ctypes.Structure):
         ("dropout_gen", ctypes.c_int32),
         ("dropout_seed", ctypes.c_uint64),
         ("dropout_offset", ctypes.c_uint64),
+        ("dtype", ctypes.c_int32),
     ]
 
 
@@ -136,6 +138,7 @@ class Params:
         c.dropout_gen = int(getattr(geom, "dropout_gen", 0) or 0)
         c.dropout_seed = int(getattr(geom, "dropout_seed", 0) or 0) & (2**64 - 1)
         c.dropout_offset = int(getattr(geom, "dropout_offset", 0) or 0) & (2**64 - 1)
+        c.dtype = DTYPES[getattr(geom, "dtype", "bf16") or "bf16"]
 
     def ref(self):
         return ctypes.byref(self.c)

@@ -8,7 +8,7 @@ Recipe (every workload): ``g = torch.Generator('cpu').manual_seed(seed)``;
 for a TND workload the sequence lengths are drawn first
 (``torch.randint(lo, hi + 1, (B,), generator=g)``); then q, k, v, dy are drawn
 in that order as ``torch.randn(shape, generator=g)`` (fp32) and rounded to
-bf16; finally, when ``keep_prob < 1``, the keep mask is drawn head by head as
+bf16 (fp16 for a geometry whose dtype is "fp16"); finally, when ``keep_prob < 1``, the keep mask is drawn head by head as
 ``torch.rand(Sq*Skv, generator=g) < keep_prob`` in (b, n) order and packed
 8 per byte, least significant bit first (element e is bit e & 7 of byte
 e >> 3, 1 = keep), matching the UINT8 = 8 x 1-bit layout of the dropout mask
@@ -43,6 +43,7 @@ class Geometry:
     dropout_gen: int = 0  # 1: the keep mask is the one dropout_seed / dropout_offset stand for
     dropout_seed: int = 0
     dropout_offset: int = 0
+    dtype: str = "bf16"  # element type of q, k, v, dy (and of out and the gradients): "bf16" or "fp16"
 
     def as_dict(self) -> dict:
         return asdict(self)
@@ -147,10 +148,11 @@ def draw(geom: Geometry, seed: int, lengths: tuple | None = None, with_dy: bool 
         lens = torch.randint(lo, hi + 1, (count,), generator=g).tolist()
         cu = np.cumsum(lens).tolist()
         geom = Geometry(**{**geom.as_dict(), "B": count, "cu_seqlens_q": cu, "cu_seqlens_kv": list(cu)})
-    q = torch.randn(geom.q_shape(), generator=g).to(torch.bfloat16)
-    k = torch.randn(geom.kv_shape(), generator=g).to(torch.bfloat16)
-    v = torch.randn(geom.kv_shape(), generator=g).to(torch.bfloat16)
-    dy = torch.randn(geom.q_shape(), generator=g).to(torch.bfloat16) if with_dy else None
+    dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[geom.dtype]
+    q = torch.randn(geom.q_shape(), generator=g).to(dt)
+    k = torch.randn(geom.kv_shape(), generator=g).to(dt)
+    v = torch.randn(geom.kv_shape(), generator=g).to(dt)
+    dy = torch.randn(geom.q_shape(), generator=g).to(dt) if with_dy else None
     p_keep = geom.keep_prob if mask_keep is None else mask_keep
     mask = None
     if (geom.keep_prob < 1.0 and not geom.dropout_gen) or mask_keep is not None:

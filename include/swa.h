@@ -42,7 +42,8 @@
  *         softmax_max / softmax_sum: [B, N, S_q] fp32
  *   TND   q, dy, out, dq: [T_q, N, D];     k, v, dk, dv: [T_kv, N, D]
  *         softmax_max / softmax_sum: [T_q, N] fp32
- *   All tensors are dense, row-major, bf16 unless stated, device memory,
+ *   All tensors are dense, row-major, of p->dtype (bf16 by default) unless
+ *   stated (statistics are fp32), device memory,
  *   16-byte aligned.  D must be 64 or 128.
  *
  * Variable length (TND): cu_seqlens_q / cu_seqlens_kv are HOST arrays of
@@ -114,7 +115,12 @@ typedef struct {
                                    caller's drop_mask.  Default 0. */
   uint64_t dropout_seed;
   uint64_t dropout_offset;
+  int32_t dtype;                /* element type of q, k, v, dy, out, dq, dk, dv (doc: FLOAT16 /
+                                   BFLOAT16 / FLOAT32): SWA_DTYPE_BF16 (0, default) or
+                                   SWA_DTYPE_FP16 (1); FLOAT32 returns SWA_ERR_UNSUPPORTED */
 } swa_params_t;
+
+typedef enum { SWA_DTYPE_BF16 = 0, SWA_DTYPE_FP16 = 1, SWA_DTYPE_FP32 = 2 } swa_dtype_t;
 
 /* Fill `p` with the documented defaults (FlashAttentionScore REG_OP
  * attribute defaults): scale 1.0, keep_prob 1.0, pre/next 2147483647,
@@ -126,10 +132,10 @@ SWA_API void swa_params_default(swa_params_t *p);
 SWA_API swa_status_t swa_forward_workspace_size(const swa_params_t *p, size_t *bytes);
 
 /* Forward (doc formula; PyPTO-Gym "前向公式").
- *   q, k, v       device, bf16, layout per p->layout
+ *   q, k, v       device, p->dtype (bf16 / fp16), layout per p->layout
  *   drop_mask     device, packed keep bits, 16-byte aligned; NULL iff keep_prob == 1
  *                 or dropout_gen == 1
- *   out           device, bf16, q's shape
+ *   out           device, p->dtype, q's shape
  *   softmax_max   device, fp32, [B,N,S_q] or [T_q,N]
  *   softmax_sum   device, fp32, same shape
  *   workspace     device, >= swa_forward_workspace_size bytes, 256-byte aligned
@@ -147,8 +153,8 @@ SWA_API swa_status_t swa_backward_workspace_size(const swa_params_t *p, size_t *
 /* Backward (PyPTO-Gym "反向公式"; aclnnFlashAttentionUnpaddingScoreGradV2
  * article §2.3).  out / softmax_max / softmax_sum are this library's forward
  * results for the same q, k, v, drop_mask and parameters.
- *   dy            device, bf16, q's shape (gradient of out)
- *   dq, dk, dv    device, bf16, shapes of q, k, v; fully overwritten
+ *   dy            device, p->dtype, q's shape (gradient of out)
+ *   dq, dk, dv    device, p->dtype, shapes of q, k, v; fully overwritten
  * Errors: as swa_forward. */
 SWA_API swa_status_t swa_backward(const swa_params_t *p, const void *q, const void *k, const void *v, const void *dy,
                           const void *out, const float *softmax_max, const float *softmax_sum,

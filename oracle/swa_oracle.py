@@ -103,6 +103,7 @@ class Problem:
     dropout_gen: int = 0
     dropout_seed: int = 0
     dropout_offset: int = 0
+    dtype: str = "bf16"  # the inputs' element type; the oracle reads their exact values in fp64
 
     @property
     def n_kv(self) -> int:

@@ -45,13 +45,14 @@ def test_ctypes_struct_matches_c_layout(tmp_path):
         "int main(void){printf(\"%zu %zu %zu %zu %zu %zu\\n\", sizeof(swa_params_t),"
         " offsetof(swa_params_t, B), offsetof(swa_params_t, cu_seqlens_q), offsetof(swa_params_t, scale),"
         " offsetof(swa_params_t, sparse_mode), offsetof(swa_params_t, keep_prob));"
-        "printf(\"%zu\\n\", offsetof(swa_params_t, N_kv));return 0;}\n")
+        "printf(\"%zu %zu %zu\\n\", offsetof(swa_params_t, N_kv), offsetof(swa_params_t, dropout_seed),"
+        " offsetof(swa_params_t, dtype));return 0;}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
     got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
     P = swa.SwaParams
     want = [ctypes.sizeof(P), P.B.offset, P.cu_seqlens_q.offset, P.scale.offset, P.sparse_mode.offset,
-            P.keep_prob.offset, P.N_kv.offset]
+            P.keep_prob.offset, P.N_kv.offset, P.dropout_seed.offset, P.dtype.offset]
     assert got == want
 
 
@@ -100,6 +101,9 @@ BASE = dict(layout="BNSD", B=1, N=2, D=128, S_q=256, S_kv=256, scale=0.1, sparse
     ({"N": 8, "N_kv": 3}, swa.SWA_ERR_PARAM_INVALID),
     ({"N": 4, "N_kv": 8}, swa.SWA_ERR_PARAM_INVALID),
     ({"N": 4, "N_kv": -2}, swa.SWA_ERR_PARAM_INVALID),
+    # element types: bf16 and fp16 built, fp32 not
+    ({"dtype": "fp16"}, swa.SWA_OK),
+    ({"dtype": "fp32"}, swa.SWA_ERR_UNSUPPORTED),
 ])
 def test_parameter_checks(lib, change, status):
     st, _ = _size(Geometry(**{**BASE, **change}))

@@ -72,6 +72,9 @@ CASES = {
     "bnsd_gqa_d128": dict(layout="BNSD", B=1, N=4, N_kv=2, D=128, S_q=290, S_kv=290, scale=0.09, sparse_mode=4,
                           pre_tokens=100, next_tokens=30, keep_prob=0.75, dropout_gen=1, dropout_seed=5,
                           dropout_offset=1),
+    "bnsd_band_d64_fp16": dict(layout="BNSD", B=1, N=3, D=64, S_q=270, S_kv=270, scale=0.125, sparse_mode=4,
+                               pre_tokens=90, next_tokens=10, keep_prob=0.9, dropout_gen=1, dropout_seed=3,
+                               dropout_offset=2, dtype="fp16"),
 }
 
 

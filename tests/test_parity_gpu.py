@@ -131,6 +131,17 @@ SMALL = {
                                        sparse_mode=4, pre_tokens=150, next_tokens=40, keep_prob=0.8),
     "bnsd_gqa2_band_dropout_d128": dict(layout="BNSD", B=1, N=4, N_kv=2, D=128, S_q=290, S_kv=290, scale=0.09,
                                         sparse_mode=4, pre_tokens=100, next_tokens=30, keep_prob=0.75),
+    # fp16 inputs (the MMAs run on fp16 operands, P and dS are rounded to fp16)
+    "bnsd_band_d128_ragged_fp16": dict(layout="BNSD", B=1, N=3, D=128, S_q=517, S_kv=517, scale=128 ** -0.5,
+                                       sparse_mode=4, pre_tokens=200, next_tokens=0, dtype="fp16"),
+    "bnsd_nomask_d64_ragged_fp16": dict(layout="BNSD", B=2, N=2, D=64, S_q=300, S_kv=300, scale=0.125,
+                                        sparse_mode=0, dtype="fp16"),
+    "tnd_varlen_band_dropout_d64_fp16": dict(layout="TND", B=4, N=3, D=64, cu_seqlens_q=[200, 201, 460, 0],
+                                             cu_seqlens_kv=[200, 201, 460, 0], scale=0.125, sparse_mode=4,
+                                             pre_tokens=100, next_tokens=17, keep_prob=0.85, dtype="fp16"),
+    "bnsd_gqa2_band_dropout_d128_fp16": dict(layout="BNSD", B=1, N=4, N_kv=2, D=128, S_q=290, S_kv=290, scale=0.09,
+                                             sparse_mode=4, pre_tokens=100, next_tokens=30, keep_prob=0.75,
+                                             dtype="fp16"),
     "tnd_gqa2_varlen_band_d128": dict(layout="TND", B=3, N=4, N_kv=2, D=128, cu_seqlens_q=[200, 200, 520],
                                       cu_seqlens_kv=[200, 200, 520], scale=0.09, sparse_mode=4, pre_tokens=100,
                                       next_tokens=20),
