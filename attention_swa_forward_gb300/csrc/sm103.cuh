@@ -307,6 +307,30 @@ __device__ __forceinline__ void fadd2_acc(float& s0, float& s1, float a0, float 
       : "+f"(s0), "+f"(s1)
       : "f"(a0), "f"(a1));
 }
+// (d0, d1) = (a0, a1) * b + (c0, c1)  with b broadcast
+__device__ __forceinline__ void ffma2_bv(float& d0, float& d1, float a0, float a1, float b, float c0, float c1) {
+  asm("{\n\t.reg .b64 x, bb, cc, r;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 bb, {%4, %4};\n\t"
+      "mov.b64 cc, {%5, %6};\n\t"
+      "fma.rn.f32x2 r, x, bb, cc;\n\t"
+      "mov.b64 {%0, %1}, r;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c0), "f"(c1));
+}
+// (d0, d1) = (p0, p1) * ((x0, x1) - (y0, y1))
+__device__ __forceinline__ void fmulsub2(float& d0, float& d1, float p0, float p1, float x0, float x1, float y0,
+                                         float y1) {
+  asm("{\n\t.reg .b64 p, x, y, r;\n\t"
+      "mov.b64 p, {%2, %3};\n\t"
+      "mov.b64 x, {%4, %5};\n\t"
+      "mov.b64 y, {%6, %7};\n\t"
+      "sub.rn.f32x2 r, x, y;\n\t"
+      "mul.rn.f32x2 r, p, r;\n\t"
+      "mov.b64 {%0, %1}, r;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(p0), "f"(p1), "f"(x0), "f"(x1), "f"(y0), "f"(y1));
+}
 // three-input maximum
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;

@@ -357,9 +357,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[st][cbase + t4 * 4]);
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 4; u += 2) {  // packed pairs: (s*c - lse2) in one f32x2 FMA
               const int t = t4 * 4 + u;
-              p[t] = ex2_approx(__uint_as_float(t < 32 ? s0[t] : s1[t - 32]) * c - lv[u]);
+              float x0, x1;
+              ffma2_bv(x0, x1, __uint_as_float(t < 32 ? s0[t] : s1[t - 32]),
+                       __uint_as_float(t + 1 < 32 ? s0[t + 1] : s1[t - 31]), c, -lv[u], -lv[u + 1]);
+              p[t] = ex2_approx(x0);
+              p[t + 1] = ex2_approx(x1);
             }
           }
         } else {
@@ -399,18 +403,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float4 d4 = *reinterpret_cast<const float4*>(&s.dsum[st][cbase + t4 * 4]);
           const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
           float pv[4], dsv[4];
+          if constexpr (DROP) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int t = t4 * 4 + u;
-            float dp = __uint_as_float(t < 32 ? d0[t] : d1[t - 32]);
-            float pt = p[t];
-            if constexpr (DROP) {
+            for (int u = 0; u < 4; ++u) {
+              const int t = t4 * 4 + u;
+              float dp = __uint_as_float(t < 32 ? d0[t] : d1[t - 32]);
               const bool keep = (s.keep.w[st][cbase + t][wq] >> lane) & 1u;  // bit (query, key r)
-              pt = keep ? p[t] * g.inv_keep : 0.f;
+              pv[u] = keep ? p[t] * g.inv_keep : 0.f;
               dp = keep ? dp * g.inv_keep : 0.f;
+              dsv[u] = p[t] * (dp - dv4[u]);
             }
-            pv[u] = pt;
-            dsv[u] = p[t] * (dp - dv4[u]);
+          } else {
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {  // dS = P * (dP - D), packed pairs
+              const int t = t4 * 4 + u;
+              pv[u] = p[t];
+              pv[u + 1] = p[t + 1];
+              fmulsub2(dsv[u], dsv[u + 1], p[t], p[t + 1], __uint_as_float(t < 32 ? d0[t] : d1[t - 32]),
+                       __uint_as_float(t + 1 < 32 ? d0[t + 1] : d1[t - 31]), dv4[u], dv4[u + 1]);
+            }
           }
           pk[t4 * 2] = pack2<F16>(pv[0], pv[1]);
           pk[t4 * 2 + 1] = pack2<F16>(pv[2], pv[3]);

@@ -283,8 +283,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // operators, so the mask compiles to selects, not branches.
         if (full) {
 #pragma unroll
-          for (int t = 0; t < 64; ++t)
-            p[t] = ex2_approx(__uint_as_float(t < 32 ? s0[t] : s1[t - 32]) * c - lse2);
+          for (int t = 0; t < 64; t += 2) {  // packed pairs: (s*c - lse2) in one f32x2 FMA
+            float x0, x1;
+            ffma2_bcast(x0, x1, __uint_as_float(t < 32 ? s0[t] : s1[t - 32]),
+                        __uint_as_float(t + 1 < 32 ? s0[t + 1] : s1[t - 31]), c, -lse2);
+            p[t] = ex2_approx(x0);
+            p[t + 1] = ex2_approx(x1);
+          }
         } else {
           const int lo_t = wlo - (jb + cbase), hi_t = whi - (jb + cbase);  // visible t in [lo_t, hi_t]
 #pragma unroll
@@ -309,15 +314,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t2 = 0; t2 < 32; ++t2) {
           float dv[2];
+          if (DM != 0) {
 #pragma unroll
-          for (int uu = 0; uu < 2; ++uu) {
-            const int t = 2 * t2 + uu;
-            float dp = __uint_as_float(t < 32 ? d0[t] : d1[t - 32]);
-            if (DM != 0) {
+            for (int uu = 0; uu < 2; ++uu) {
+              const int t = 2 * t2 + uu;
+              float dp = __uint_as_float(t < 32 ? d0[t] : d1[t - 32]);
               const bool keep = ((t < 32 ? kb0 : kb1) >> (t & 31)) & 1u;
               dp = keep ? dp * g.inv_keep : 0.f;
+              dv[uu] = p[t] * (dp - drow);
             }
-            dv[uu] = p[t] * (dp - drow);
+          } else {  // dS = P * (dP - D), packed pair
+            const int t = 2 * t2;
+            fmulsub2(dv[0], dv[1], p[t], p[t + 1], __uint_as_float(t < 32 ? d0[t] : d1[t - 32]),
+                     __uint_as_float(t + 1 < 32 ? d0[t + 1] : d1[t - 31]), drow, drow);
           }
           dk[t2] = pack2<F16>(dv[0], dv[1]);
         }
