@@ -55,7 +55,7 @@ struct DkvSmem {
   uint64_t kv_full, q_full[kQStages], q_empty[kQStages], dy_full[2], dy_empty[2], stat_full[2];
   // per-region barriers where the two issuers hand off, so that no waiter
   // can be a full phase behind
-  uint64_t s_full[2], s_loaded, dp_full, pds_full[2], region_free[2], mma_done, drain_sdp, drain_kv;
+  uint64_t s_full[2], s_loaded, dp_full, pt_full[2], ds_full[2], region_free[2], mma_done, drain_sdp, drain_kv;
   uint64_t gen_full[2];  // generated keep bits of the tile in that stage written (compute threads)
   uint32_t tmem_base;
 };
@@ -136,7 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.s_loaded, kComputeThreads);
     mbar_init(&s.dp_full, 1);
     for (int r = 0; r < 2; ++r) {
-      mbar_init(&s.pds_full[r], kComputeThreads);
+      mbar_init(&s.pt_full[r], kComputeThreads);
+      mbar_init(&s.ds_full[r], kComputeThreads);
       mbar_init(&s.region_free[r], 1);
     }
     mbar_init(&s.mma_done, 1);
@@ -273,8 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = it & 1, qs = it % kQS;
         // dV, dK from the P^T / dS^T the compute warps stored in region(it):
         // query columns [64h, 64h+64) of the tile hold P^T in columns
-        // [64h, 64h+32) and dS^T in [64h+32, 64h+64), two bf16 per column
-        if (!mbar_wait(&s.pds_full[st], (it >> 1) & 1, a.err, kErrBwdMma)) break;
+        // [64h, 64h+32) and dS^T in [64h+32, 64h+64), two bf16 per column.
+        // P^T is stored first, so dV(it) runs while dS^T is computed.
+        if (!mbar_wait(&s.pt_full[st], (it >> 1) & 1, a.err, kErrBwdMma)) break;
         tc_fence_after_sync();
         const uint32_t ra = tmem + region(it);
         const uint32_t dy_addr = smem_u32(s.dy[st]), q_addr = smem_u32(s.q[qs]);
@@ -283,6 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16_ts(tmem + kColDV, ra + (kk >> 2) * 64 + (kk & 3) * 8,
                        sdesc_sw128(dy_addr + kk * 2048, kAtomBytes, 1024), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&s.dy_empty[st]);  // dP^T(it) read dY(it) too; it finished before P^T(it) existed
+        if (!mbar_wait(&s.ds_full[st], (it >> 1) & 1, a.err, kErrBwdMma)) break;
+        tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk)  // dK += dS^T Q
           umma_bf16_ts(tmem + kColDK, ra + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
@@ -382,58 +386,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // ---- next tile's generated keep bits, into the stage tile it-1 used
-      // once every thread is through with tile it-1 (its pds_full)
+      // once every thread is through with tile it-1 (its ds_full)
       if (DM == 2 && it + 1 < n_it) {
-        if (it >= 1 && !compute_wait(&s.pds_full[(it - 1) & 1], ((it - 1) >> 1) & 1, a.err)) { ok = false; break; }
+        if (it >= 1 && !compute_wait(&s.ds_full[(it - 1) & 1], ((it - 1) >> 1) & 1, a.err)) { ok = false; break; }
         gen_tile_bits(it + 1);
       }
       // ---- dP^T -> dS^T; P^T*z/keep and dS^T packed bf16 into the same columns
       if (DM == 2 && !compute_wait(&s.gen_full[st], (it >> 1) & 1, a.err)) { ok = false; break; }
       if (!compute_wait(&s.dp_full, it & 1, a.err)) { ok = false; break; }
       tc_fence_after_sync();
-      uint32_t pk[32], dk[32];
       {
         uint32_t d0[32], d1[32];
         tmem_ld_32x32b_x32(col, d0);
         tmem_ld_32x32b_x32(col + 32, d1);
         tmem_ld_wait(d0);
         tmem_ld_wait(d1);
+        // this thread's keep bits of the tile: bit t = (query cbase + t, key r)
+        uint32_t km[2] = {~0u, ~0u};
+        if constexpr (DROP) {
+          km[0] = km[1] = 0u;
+#pragma unroll
+          for (int t = 0; t < 64; ++t) km[t >> 5] |= ((s.keep.w[st][cbase + t][wq] >> lane) & 1u) << (t & 31);
+        }
+        // P^T * z / keep first (over the dP^T columns just read), so dV can start
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int t2 = 0; t2 < 16; ++t2) {
+            const int t = half * 32 + 2 * t2;
+            float p0 = p[t], p1 = p[t + 1];
+            if constexpr (DROP) {
+              p0 = ((km[t >> 5] >> (t & 31)) & 1u) ? p0 * g.inv_keep : 0.f;
+              p1 = ((km[(t + 1) >> 5] >> ((t + 1) & 31)) & 1u) ? p1 * g.inv_keep : 0.f;
+            }
+            pk[t2] = pack2<F16>(p0, p1);
+          }
+          tmem_st_32x32b_x16(col + half * 16, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&s.pt_full[st]);
+        // dS^T = P^T * (dP^T * z / keep - D)
+        uint32_t dk[32];
 #pragma unroll
         for (int t4 = 0; t4 < 16; ++t4) {
           const float4 d4 = *reinterpret_cast<const float4*>(&s.dsum[st][cbase + t4 * 4]);
           const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pv[4], dsv[4];
+          float dsv[4];
           if constexpr (DROP) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int t = t4 * 4 + u;
               float dp = __uint_as_float(t < 32 ? d0[t] : d1[t - 32]);
-              const bool keep = (s.keep.w[st][cbase + t][wq] >> lane) & 1u;  // bit (query, key r)
-              pv[u] = keep ? p[t] * g.inv_keep : 0.f;
-              dp = keep ? dp * g.inv_keep : 0.f;
+              dp = ((km[t >> 5] >> (t & 31)) & 1u) ? dp * g.inv_keep : 0.f;
               dsv[u] = p[t] * (dp - dv4[u]);
             }
           } else {
 #pragma unroll
-            for (int u = 0; u < 4; u += 2) {  // dS = P * (dP - D), packed pairs
+            for (int u = 0; u < 4; u += 2) {  // packed pairs
               const int t = t4 * 4 + u;
-              pv[u] = p[t];
-              pv[u + 1] = p[t + 1];
               fmulsub2(dsv[u], dsv[u + 1], p[t], p[t + 1], __uint_as_float(t < 32 ? d0[t] : d1[t - 32]),
                        __uint_as_float(t + 1 < 32 ? d0[t + 1] : d1[t - 31]), dv4[u], dv4[u + 1]);
             }
           }
-          pk[t4 * 2] = pack2<F16>(pv[0], pv[1]);
-          pk[t4 * 2 + 1] = pack2<F16>(pv[2], pv[3]);
           dk[t4 * 2] = pack2<F16>(dsv[0], dsv[1]);
           dk[t4 * 2 + 1] = pack2<F16>(dsv[2], dsv[3]);
         }
+        tmem_st_32x32b_x32(col + 32, dk);
       }
-      tmem_st_32x32b_x32(col, pk);
-      tmem_st_32x32b_x32(col + 32, dk);
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&s.pds_full[st]);
+      mbar_arrive(&s.ds_full[st]);
     }
     if (ok && n_q > 0) ok = compute_wait(&s.mma_done, 0, a.err);  // every MMA done
     if (ok) {
