@@ -101,7 +101,11 @@ swa_status_t make_plan(const swa_params_t* p, Plan& plan) {
                 (long long)p->N_kv);
   if (p->B < 1) return fail(SWA_ERR_PARAM_INVALID, "B must be >= 1, got %lld", (long long)p->B);
   if (p->D < 1 || p->D > 768) return fail(SWA_ERR_PARAM_INVALID, "D must be in [1, 768], got %lld", (long long)p->D);
-  if (p->D != 64 && p->D != 128) return fail(SWA_ERR_UNSUPPORTED, "D = %lld is not built (64 or 128)", (long long)p->D);
+  // D up to 128 in steps of 8 (a row then starts on a 16-byte boundary, as a
+  // TMA copy needs); the kernels compute on 64 or 128 columns and the tensor
+  // maps fill the columns past D with zeros.
+  if (p->D % 8 != 0 || p->D > 128)
+    return fail(SWA_ERR_UNSUPPORTED, "D = %lld is not built (a multiple of 8 up to 128)", (long long)p->D);
   if (!std::isfinite(p->scale)) return fail(SWA_ERR_PARAM_INVALID, "scale is not finite");
   if (p->sparse_mode == 4) {
     // an everywhere-empty band is almost certainly a caller error

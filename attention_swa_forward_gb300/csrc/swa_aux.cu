@@ -21,17 +21,22 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
   else return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
 }
 
-// One warp per row; each lane handles D/32 consecutive elements.
-template <int D, bool F16>
+// One warp per row; each lane handles DP/32 consecutive elements of a row of
+// D <= DP elements (D a multiple of 8: a lane's elements lie all below D or
+// all past it).
+template <int DP, bool F16>
 __global__ void __launch_bounds__(256) swa_prep_kernel(const PrepArgs a) {
-  constexpr int kPer = D / 32;  // 2 or 4 bf16 per lane
+  constexpr int kPer = DP / 32;  // 2 or 4 elements per lane
   const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0;  // fresh error word for this backward call
   if (row >= a.rows) return;
+  const int D = a.g.D;
   const int64_t base = row * D + lane * kPer;
   float acc = 0.f;
-  if (kPer == 4) {
+  if (lane * kPer >= D) {
+    // past the row's last element
+  } else if (kPer == 4) {
     const uint2 dy = __ldg(reinterpret_cast<const uint2*>(a.dy + base));
     const uint2 o = __ldg(reinterpret_cast<const uint2*>(a.out + base));
     const uint32_t d2[2] = {dy.x, dy.y}, o2[2] = {o.x, o.y};
@@ -102,7 +107,7 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream) {
   const int block = 256;
   const int64_t grid = (threads + block - 1) / block;
   const unsigned gr = static_cast<unsigned>(grid);
-  if (a.g.D == 64) {
+  if (a.g.D <= 64) {
     if (a.g.f16) swa_prep_kernel<64, true><<<gr, block, 0, stream>>>(a);
     else swa_prep_kernel<64, false><<<gr, block, 0, stream>>>(a);
   } else {

@@ -231,9 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_q > 0) {
       constexpr uint32_t kIdT = idesc_f16_f32(kTileN, kTileM, false, false, F16);  // S^T, dP^T
       const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
+      const int nk = d_steps(g);
       auto issue_ss = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {  // 128 x 128 x D, both K-major
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
+          if (kk >= nk) break;
           const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
           umma_bf16_ss(tmem + d_col, sdesc_sw128(a_addr + off, 16, 1024), sdesc_sw128(b_addr + off, 16, 1024), kIdT,
                        kk > 0);
@@ -469,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16* dst = (h == 0 ? a.dv : a.dk) + kv_elem(g, sq, w.b, w.n, j);
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
+        if (ch * 32 >= g.D) break;  // columns past D are padding
         float o[32];
         if (n_q > 0) {
           uint32_t t32[32];
@@ -482,7 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (kv_valid) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(dst + ch * 32)[q4] = pack8<F16>(&o[q4 * 8]);
+          for (int q4 = 0; q4 < 4; ++q4)
+            if (ch * 32 + q4 * 8 < g.D) reinterpret_cast<uint4*>(dst + ch * 32)[q4] = pack8<F16>(&o[q4 * 8]);
         }
       }
     }
@@ -519,7 +523,7 @@ cudaError_t launch_backward_dkv(const BwdArgs& a, const SeqTable<CAP>& tab, cons
                                 cudaStream_t stream) {
   if (tab.n_items == 0) return cudaSuccess;
   // (drop mode, D, element type) -> one of the twelve instantiations
-  switch ((drop_mode_of(a.g.has_mask, a.g.drop_gen) * 2 + (a.g.D == 64 ? 0 : 1)) * 2 + (a.g.f16 ? 1 : 0)) {
+  switch ((drop_mode_of(a.g.has_mask, a.g.drop_gen) * 2 + (a.g.D <= 64 ? 0 : 1)) * 2 + (a.g.f16 ? 1 : 0)) {
     case 0: return launch_dkv_t<64, 0, false>(a, tab, mq, mk, mv, mdy, stream);
     case 1: return launch_dkv_t<64, 0, true>(a, tab, mq, mk, mv, mdy, stream);
     case 2: return launch_dkv_t<128, 0, false>(a, tab, mq, mk, mv, mdy, stream);

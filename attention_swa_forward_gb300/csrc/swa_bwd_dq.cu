@@ -155,10 +155,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_kv > 0) {
       constexpr uint32_t kIdS = idesc_f16_f32(kTileM, kTileN, false, false, F16);  // S, dP
       const uint32_t q_addr = smem_u32(s.q), dy_addr = smem_u32(s.dy);
+      const int nk = d_steps(g);
       auto issue_s = [&](int j) {  // S(j) = Q K_j^T
         const uint32_t k_addr = smem_u32(s.k[j % 3]);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
+          if (kk >= nk) break;
           const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
           umma_bf16_ss(tmem + kColS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), kIdS,
                        kk > 0);
@@ -169,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t v_addr = smem_u32(s.v[j & 1]);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
+          if (kk >= nk) break;
           const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
           umma_bf16_ss(tmem + kColDP, sdesc_sw128(dy_addr + off, 16, 1024), sdesc_sw128(v_addr + off, 16, 1024), kIdS,
                        kk > 0);
@@ -346,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16* dst = a.dq + q_elem(g, sq, w.b, w.n, i) + h * kCols;
 #pragma unroll
       for (int ch = 0; ch < kCols / 32; ++ch) {
+        if (h * kCols + ch * 32 >= g.D) break;  // columns past D are padding
         float o[32];
         if (n_kv > 0) {
           uint32_t t32[32];
@@ -359,7 +363,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (row_valid) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(dst + ch * 32)[q4] = pack8<F16>(&o[q4 * 8]);
+          for (int q4 = 0; q4 < 4; ++q4)
+            if (h * kCols + ch * 32 + q4 * 8 < g.D)
+              reinterpret_cast<uint4*>(dst + ch * 32)[q4] = pack8<F16>(&o[q4 * 8]);
         }
       }
     }
@@ -395,7 +401,7 @@ cudaError_t launch_backward_dq(const BwdArgs& a, const SeqTable<CAP>& tab, const
                                cudaStream_t stream) {
   if (tab.n_items == 0) return cudaSuccess;
   // (drop mode, D, element type) -> one of the twelve instantiations
-  switch ((drop_mode_of(a.g.has_mask, a.g.drop_gen) * 2 + (a.g.D == 64 ? 0 : 1)) * 2 + (a.g.f16 ? 1 : 0)) {
+  switch ((drop_mode_of(a.g.has_mask, a.g.drop_gen) * 2 + (a.g.D <= 64 ? 0 : 1)) * 2 + (a.g.f16 ? 1 : 0)) {
     case 0: return launch_dq_t<64, 0, false>(a, tab, mq, mk, mv, mdy, stream);
     case 1: return launch_dq_t<64, 0, true>(a, tab, mq, mk, mv, mdy, stream);
     case 2: return launch_dq_t<128, 0, false>(a, tab, mq, mk, mv, mdy, stream);

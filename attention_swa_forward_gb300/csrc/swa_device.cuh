@@ -82,6 +82,11 @@ __device__ __forceinline__ void key_window(const Geometry& g, const SeqInfo& s, 
   }
 }
 
+// 16-column steps of a contraction over the head dim: the kernels hold 64 or
+// 128 columns per row, and the columns past D (zero-filled by the tensor map)
+// add nothing, so the steps past them are skipped.
+__device__ __forceinline__ int d_steps(const Geometry& g) { return (g.D + 15) >> 4; }
+
 // Is every (i, j) of the query tile [q0, q0+128) x key tile [j0, j0+128) visible?
 __device__ __forceinline__ bool tile_fully_visible(const Geometry& g, const SeqInfo& s, int q0, int j0) {
   if (q0 + 127 >= s.q_len || j0 + 127 >= s.kv_len) return false;

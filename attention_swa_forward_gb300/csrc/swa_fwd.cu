@@ -135,6 +135,7 @@ __global__ void __launch_bounds__(224, 1)
     if (lane == 0 && n_kv > 0) {
       constexpr uint32_t kIdS = idesc_f16_f32(kTileM, kTileN, false, false, F16);
       const uint32_t q_addr = smem_u32(s.q);
+      const int nk = d_steps(g);
       bool ok = mbar_wait(&s.q_full, 0, a.err, kErrFwdMma);
       for (int it = 0; ok && it < n_kv; ++it) {
         const int st = it % kStages, sb = it & 1;
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(224, 1)
         const uint32_t k_addr = smem_u32(s.k[st]);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
+          if (kk >= nk) break;
           const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
           umma_bf16_ss(tmem + sb * kTileN, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
                        kIdS, kk > 0);
@@ -326,6 +328,7 @@ __global__ void __launch_bounds__(224, 1)
       __nv_bfloat16* orow = a.out + q_elem(g, sq, w.b, w.n, i);
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
+        if (ch * 32 >= g.D) break;  // columns past D are padding
         float o[32];
         if (n_kv > 0) {
           uint32_t t32[32];
@@ -339,7 +342,8 @@ __global__ void __launch_bounds__(224, 1)
         }
         if (row_valid) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(orow + ch * 32)[q4] = pack8<F16>(&o[q4 * 8]);
+          for (int q4 = 0; q4 < 4; ++q4)
+            if (ch * 32 + q4 * 8 < g.D) reinterpret_cast<uint4*>(orow + ch * 32)[q4] = pack8<F16>(&o[q4 * 8]);
         }
       }
       if (row_valid) {
@@ -380,7 +384,7 @@ cudaError_t launch_forward(const FwdArgs& a, const SeqTable<CAP>& tab, const CUt
                            const CUtensorMap& mv, cudaStream_t stream) {
   if (tab.n_items == 0) return cudaSuccess;
   // (drop mode, D, element type) -> one of the twelve instantiations
-  switch ((drop_mode_of(a.g.has_mask, a.g.drop_gen) * 2 + (a.g.D == 64 ? 0 : 1)) * 2 + (a.g.f16 ? 1 : 0)) {
+  switch ((drop_mode_of(a.g.has_mask, a.g.drop_gen) * 2 + (a.g.D <= 64 ? 0 : 1)) * 2 + (a.g.f16 ? 1 : 0)) {
     case 0: return launch_fwd_t<64, 0, false>(a, tab, mq, mk, mv, stream);
     case 1: return launch_fwd_t<64, 0, true>(a, tab, mq, mk, mv, stream);
     case 2: return launch_fwd_t<128, 0, false>(a, tab, mq, mk, mv, stream);

@@ -44,7 +44,13 @@
  *         softmax_max / softmax_sum: [T_q, N] fp32
  *   All tensors are dense, row-major, of p->dtype (bf16 by default) unless
  *   stated (statistics are fp32), device memory,
- *   16-byte aligned.  D must be 64 or 128.
+ *   16-byte aligned.  D is a multiple of 8 from 8 to 128 (a row of D
+ *   elements then starts on a 16-byte boundary).  The kernels compute on 64
+ *   (D <= 64) or 128 columns per row; the tensor maps fill the columns past D
+ *   with zeros, which changes no result, and nothing past D is written.  The
+ *   grad API's own pre-processing pads special head dims such as 72 and 88
+ *   (aclnnFlashAttentionUnpaddingScoreGradV2 article §8.2, the API layer);
+ *   here the padding costs no copy.
  *
  * Variable length (TND): cu_seqlens_q / cu_seqlens_kv are HOST arrays of
  * length B holding cumulative sequence ends without a leading 0 (doc
@@ -86,7 +92,7 @@ typedef enum {
   SWA_OK = 0,
   SWA_ERR_PARAM_NULLPTR = 161001, /* a required pointer is NULL */
   SWA_ERR_PARAM_INVALID = 161002, /* a value is outside its documented range */
-  SWA_ERR_UNSUPPORTED = 161100,   /* valid per the API but not built (e.g. D not in {64, 128}) */
+  SWA_ERR_UNSUPPORTED = 161100,   /* valid per the API but not built (e.g. D past 128 or not a multiple of 8) */
   SWA_ERR_WORKSPACE = 161101,     /* workspace NULL or smaller than the size query says */
   SWA_ERR_CUDA = 161102,          /* a CUDA runtime call failed (text in swa_last_error) */
   SWA_ERR_TIMEOUT = 161103        /* a kernel gave up a bounded wait (swa_workspace_status) */
@@ -94,7 +100,7 @@ typedef enum {
 
 typedef struct {
   int32_t layout;               /* swa_layout_t */
-  int64_t B, N, D;              /* batch, heads (headNum), head dim (64 or 128) */
+  int64_t B, N, D;              /* batch, heads (headNum), head dim (8..128, a multiple of 8) */
   int64_t S_q, S_kv;            /* BNSD sequence lengths (ignored for TND) */
   int64_t T_q, T_kv;            /* TND total rows (ignored for BNSD) */
   const int64_t *cu_seqlens_q;  /* TND: host, length B, cumulative ends (see above) */

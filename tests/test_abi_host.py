@@ -86,7 +86,14 @@ BASE = dict(layout="BNSD", B=1, N=2, D=128, S_q=256, S_kv=256, scale=0.1, sparse
     ({"N": 0}, swa.SWA_ERR_PARAM_INVALID),
     ({"N": 257}, swa.SWA_ERR_PARAM_INVALID),
     ({"B": 0}, swa.SWA_ERR_PARAM_INVALID),
-    ({"D": 96}, swa.SWA_ERR_UNSUPPORTED),
+    # head dims: multiples of 8 up to 128 (computed on 64 or 128 columns)
+    ({"D": 96}, swa.SWA_OK),
+    ({"D": 72}, swa.SWA_OK),
+    ({"D": 88}, swa.SWA_OK),
+    ({"D": 8}, swa.SWA_OK),
+    ({"D": 36}, swa.SWA_ERR_UNSUPPORTED),
+    ({"D": 136}, swa.SWA_ERR_UNSUPPORTED),
+    ({"D": 192}, swa.SWA_ERR_UNSUPPORTED),
     ({"D": 1000}, swa.SWA_ERR_PARAM_INVALID),
     ({"S_q": 0}, swa.SWA_ERR_PARAM_INVALID),
     ({"pre_tokens": -10, "next_tokens": 5}, swa.SWA_ERR_PARAM_INVALID),

@@ -75,6 +75,9 @@ CASES = {
     "bnsd_band_d64_fp16": dict(layout="BNSD", B=1, N=3, D=64, S_q=270, S_kv=270, scale=0.125, sparse_mode=4,
                                pre_tokens=90, next_tokens=10, keep_prob=0.9, dropout_gen=1, dropout_seed=3,
                                dropout_offset=2, dtype="fp16"),
+    "bnsd_band_d72": dict(layout="BNSD", B=1, N=2, D=72, S_q=300, S_kv=300, scale=72 ** -0.5, sparse_mode=4,
+                          pre_tokens=110, next_tokens=20, keep_prob=0.8, dropout_gen=1, dropout_seed=17,
+                          dropout_offset=4),
 }
 
 

@@ -145,6 +145,21 @@ SMALL = {
     "tnd_gqa2_varlen_band_d128": dict(layout="TND", B=3, N=4, N_kv=2, D=128, cu_seqlens_q=[200, 200, 520],
                                       cu_seqlens_kv=[200, 200, 520], scale=0.09, sparse_mode=4, pre_tokens=100,
                                       next_tokens=20),
+    # head dims other than 64 / 128: computed on 64 or 128 zero-padded columns
+    "bnsd_band_d72_ragged": dict(layout="BNSD", B=1, N=3, D=72, S_q=333, S_kv=333, scale=72 ** -0.5,
+                                 sparse_mode=4, pre_tokens=150, next_tokens=0),
+    "bnsd_nomask_d88": dict(layout="BNSD", B=2, N=2, D=88, S_q=260, S_kv=260, scale=88 ** -0.5, sparse_mode=0),
+    "tnd_varlen_band_dropout_d96": dict(layout="TND", B=3, N=2, D=96, cu_seqlens_q=[150, 150, 420],
+                                        cu_seqlens_kv=[150, 150, 420], scale=96 ** -0.5, sparse_mode=4,
+                                        pre_tokens=90, next_tokens=30, keep_prob=0.85),
+    "bnsd_gqa2_band_d32": dict(layout="BNSD", B=1, N=4, N_kv=2, D=32, S_q=300, S_kv=300, scale=32 ** -0.5,
+                               sparse_mode=4, pre_tokens=120, next_tokens=10),
+    "bnsd_band_d8": dict(layout="BNSD", B=1, N=2, D=8, S_q=200, S_kv=200, scale=8 ** -0.5, sparse_mode=4,
+                         pre_tokens=60, next_tokens=60),
+    "bnsd_band_d120_fp16": dict(layout="BNSD", B=1, N=2, D=120, S_q=270, S_kv=270, scale=120 ** -0.5,
+                                sparse_mode=4, pre_tokens=100, next_tokens=0, dtype="fp16"),
+    "bnsd_rect_band_d40": dict(layout="BNSD", B=1, N=2, D=40, S_q=150, S_kv=330, scale=40 ** -0.5, sparse_mode=4,
+                               pre_tokens=40, next_tokens=160),
 }
 
 
