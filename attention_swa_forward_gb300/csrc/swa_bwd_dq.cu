@@ -16,10 +16,13 @@
 //   warp  8    TMA producer: Q, dY once; K through a 3-stage ring (a K tile
 //              is read by S and, last, by dQ) and V through a 2-stage ring
 //              (read by dP only, so it is released early)
-//   warp  9    tcgen05 issuer of S and dP (both SS)
+//   warp  9    tcgen05 issuer of S (SS)
 //   warp 10    tcgen05 issuer of dQ += dS K (TS)
-// Two issuing threads keep the tensor pipe fed: its queue is shallow, so
-// every barrier wait of a single issuer between GEMMs left it idle.
+//   warp 11    tcgen05 issuer of dP (SS)
+// One issuing thread per GEMM stream: the tensor pipe's queue is shallow, so
+// a thread issuing one GEMM blocks until most of it has run, and a GEMM whose
+// inputs are ready must not wait behind another GEMM's issue (with S and dP
+// on one thread, S(j+1) sat ~700 cycles behind dP(j)).
 // TMEM columns: S [0,128), dP [128,256), dQ [256,256+D), and two bf16 dS
 // buffers [384,448), [448,512) that the dQ MMA reads as its A operand.
 // S(j+1) is issued as soon as the compute warps hold S(j) in registers and
@@ -38,12 +41,12 @@ struct DqSmem {
   alignas(1024) uint8_t k[3][kTileBytes];
   alignas(1024) uint8_t v[2][kTileBytes];
   uint64_t qdy_full, k_full[3], k_empty[3], v_full[2], v_empty[2];
-  uint64_t s_full, s_loaded, dp_full, dp_loaded, ds_full[2], ds_free[2], drain_sdp, drain_dq;
+  uint64_t s_full, s_loaded, dp_full, dp_loaded, ds_full[2], ds_free[2], drain_s, drain_dp, drain_dq;
   uint32_t tmem_base;
 };
 static_assert(sizeof(DqSmem<128>) + 1024 <= 232448, "shared memory budget");
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kComputeThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384;  // dS buffer b at kColDS + 64*b
@@ -101,7 +104,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.s_loaded, kComputeThreads);
     mbar_init(&s.dp_full, 1);
     mbar_init(&s.dp_loaded, kComputeThreads);
-    mbar_init(&s.drain_sdp, 1);
+    mbar_init(&s.drain_s, 1);
+    mbar_init(&s.drain_dp, 1);
     mbar_init(&s.drain_dq, 1);
     fence_mbar_init();
   }
@@ -150,60 +154,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (uses > 0) mbar_wait_drain(&s.v_full[b], (uses - 1) & 1);
       }
     }
-  } else if (warp == 9) {
-    // ----------------------------------------------------- tcgen05 issuer --
+  } else if (warp == 9 || warp == 11) {
+    // ------------------------------------------ tcgen05 issuers of S, dP --
     if (lane == 0 && n_kv > 0) {
       constexpr uint32_t kIdS = idesc_f16_f32(kTileM, kTileN, false, false, F16);  // S, dP
       const uint32_t q_addr = smem_u32(s.q), dy_addr = smem_u32(s.dy);
       const int nk = d_steps(g);
-      auto issue_s = [&](int j) {  // S(j) = Q K_j^T
-        const uint32_t k_addr = smem_u32(s.k[j % 3]);
+      if (warp == 9) {
+        // S(j) = Q K_j^T; S(j+1) once the compute warps hold S(j) in registers
+        for (int j = 0; j < n_kv; ++j) {
+          if (j == 0 && !mbar_wait(&s.qdy_full, 0, a.err, kErrBwdMma)) break;
+          if (j > 0 && !mbar_wait(&s.s_loaded, (j - 1) & 1, a.err, kErrBwdMma)) break;
+          if (!mbar_wait(&s.k_full[j % 3], (j / 3) & 1, a.err, kErrBwdMma)) break;
+          tc_fence_after_sync();
+          const uint32_t k_addr = smem_u32(s.k[j % 3]);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          if (kk >= nk) break;
-          const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-          umma_bf16_ss(tmem + kColS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), kIdS,
-                       kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            if (kk >= nk) break;
+            const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
+            umma_bf16_ss(tmem + kColS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), kIdS,
+                         kk > 0);
+          }
+          umma_commit(&s.s_full);
         }
-        umma_commit(&s.s_full);
-      };
-      auto issue_dp = [&](int j) {  // dP(j) = dY V_j^T
-        const uint32_t v_addr = smem_u32(s.v[j & 1]);
+        umma_commit(&s.drain_s);
+        mbar_wait_drain(&s.drain_s, 0);
+      } else {
+        // dP(j) = dY V_j^T; dP(j+1) once the compute warps hold dP(j)
+        for (int j = 0; j < n_kv; ++j) {
+          if (j == 0 && !mbar_wait(&s.qdy_full, 0, a.err, kErrBwdMma)) break;
+          if (j > 0 && !mbar_wait(&s.dp_loaded, (j - 1) & 1, a.err, kErrBwdMma)) break;
+          if (!mbar_wait(&s.v_full[j & 1], (j >> 1) & 1, a.err, kErrBwdMma)) break;
+          tc_fence_after_sync();
+          const uint32_t v_addr = smem_u32(s.v[j & 1]);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          if (kk >= nk) break;
-          const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-          umma_bf16_ss(tmem + kColDP, sdesc_sw128(dy_addr + off, 16, 1024), sdesc_sw128(v_addr + off, 16, 1024), kIdS,
-                       kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            if (kk >= nk) break;
+            const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
+            umma_bf16_ss(tmem + kColDP, sdesc_sw128(dy_addr + off, 16, 1024), sdesc_sw128(v_addr + off, 16, 1024),
+                         kIdS, kk > 0);
+          }
+          umma_commit(&s.dp_full);
+          umma_commit(&s.v_empty[j & 1]);
         }
-        umma_commit(&s.dp_full);
-        umma_commit(&s.v_empty[j & 1]);
-      };
-      // S(j+1) may be issued once the compute warps hold S(j) in registers,
-      // dP(j+1) once they hold dP(j): neither waits for the other's consumer.
-      bool ok = mbar_wait(&s.qdy_full, 0, a.err, kErrBwdMma) && mbar_wait(&s.k_full[0], 0, a.err, kErrBwdMma);
-      if (ok) {
-        tc_fence_after_sync();
-        issue_s(0);
-        ok = mbar_wait(&s.v_full[0], 0, a.err, kErrBwdMma);
+        umma_commit(&s.drain_dp);
+        mbar_wait_drain(&s.drain_dp, 0);
       }
-      if (ok) {
-        tc_fence_after_sync();
-        issue_dp(0);
-      }
-      for (int j = 0; ok && j + 1 < n_kv; ++j) {
-        const int n = j + 1;
-        if (!mbar_wait(&s.s_loaded, j & 1, a.err, kErrBwdMma)) break;
-        if (!mbar_wait(&s.k_full[n % 3], (n / 3) & 1, a.err, kErrBwdMma)) break;
-        tc_fence_after_sync();
-        issue_s(n);
-        if (!mbar_wait(&s.dp_loaded, j & 1, a.err, kErrBwdMma)) break;
-        if (!mbar_wait(&s.v_full[n & 1], (n >> 1) & 1, a.err, kErrBwdMma)) break;
-        tc_fence_after_sync();
-        issue_dp(n);
-      }
-      umma_commit(&s.drain_sdp);
-      mbar_wait_drain(&s.drain_sdp, 0);
     }
   } else if (warp == 10) {
     // ------------------------------------------------ dQ += dS K issuer --
