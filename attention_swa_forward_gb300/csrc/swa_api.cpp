@@ -151,6 +151,7 @@ swa_status_t make_plan(const swa_params_t* p, Plan& plan) {
     for (int64_t b = 0; b < p->B; ++b)
       plan.seqs[b] = Seq{0, p->S_q, 0, p->S_kv, b * p->N * p->S_q * p->S_kv};
     plan.q_rows = p->B * p->S_q;
+    g.T_q = static_cast<int32_t>(plan.q_rows);
     plan.kv_rows = p->B * p->S_kv;
     plan.mask_bits = p->B * p->N * p->S_q * p->S_kv;
     max_len = std::max(p->S_q, p->S_kv);
@@ -173,6 +174,7 @@ swa_status_t make_plan(const swa_params_t* p, Plan& plan) {
     g.S_q = 0;
     g.S_kv = 0;
     plan.q_rows = p->T_q;
+    g.T_q = static_cast<int32_t>(plan.q_rows);
     plan.kv_rows = p->T_kv;
     plan.mask_bits = bits;
   }

@@ -2,7 +2,7 @@
 //
 //  * preprocess: per query row, D = rowsum(dY * O) (PyPTO-Gym article,
 //    "反向公式") and lse2 = softmax_max*log2(e) + log2(softmax_sum) (+inf for
-//    an empty row, so that the recomputed P is 0).
+//    an empty row, so that the recomputed P is 0), stored head-major.
 //
 // Both layouts address a query row (b, n, i) / (t, n) the same way once
 // flattened: row id r -> elements [r*D, r*D + D), statistics index r.
@@ -59,8 +59,10 @@ __global__ void __launch_bounds__(256) swa_prep_kernel(const PrepArgs a) {
   for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, m);
   if (lane == 0) {
     const float l = a.ssum[row];
-    a.dsum[row] = acc;
-    a.lse2[row] = (l > 0.f) ? a.smax[row] * kLog2e + __log2f(l) : INFINITY;
+    // workspace position: head-major (row = t*N + n in TND, already head-major in BNSD)
+    const int64_t ws = a.g.layout == 0 ? row : (row % a.g.N) * a.g.T_q + row / a.g.N;
+    a.dsum[ws] = acc;
+    a.lse2[ws] = (l > 0.f) ? a.smax[row] * kLog2e + __log2f(l) : INFINITY;
   }
 }
 

@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float l2 = INFINITY, dd = 0.f;
           uint32_t bits[4] = {0u, 0u, 0u, 0u};
           if (i < sq.q_len) {
-            const int64_t si = stat_index(g, sq, w.b, qn, i);
+            const int64_t si = ws_stat_index(g, sq, w.b, qn, i);
             l2 = a.lse2[si];
             dd = a.dsum[si];
             if constexpr (DM == 1) load_keep_bits(a.mask, sq, qn, i, j0, bits);

@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     key_window(g, sq, i, wlo, whi);
     float lse2 = INFINITY, drow = 0.f;
     if (row_valid) {
-      const int64_t si = stat_index(g, sq, w.b, w.n, i);
+      const int64_t si = ws_stat_index(g, sq, w.b, w.n, i);
       lse2 = a.lse2[si];
       drow = a.dsum[si];
     }

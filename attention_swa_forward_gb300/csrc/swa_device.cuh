@@ -31,8 +31,8 @@ __device__ __forceinline__ Item resolve_item(const SeqTable<CAP>& tab, const Geo
   }
   const SeqDesc& d = tab.d[lo];
   const int local = k - d.item_begin;
-  const int rank = local / d.heads;
-  const int h = local - rank * d.heads;
+  const int h = local / d.tiles;  // head by head: the CTAs in flight share a head's tiles in L2
+  const int rank = local - h * d.tiles;
   Item it;
   it.tile = d.descending ? d.tiles - 1 - rank : rank;
   if (d.b < 0) {
@@ -65,6 +65,15 @@ __device__ __forceinline__ int64_t kv_elem(const Geometry& g, const SeqInfo& s, 
 __device__ __forceinline__ int64_t stat_index(const Geometry& g, const SeqInfo& s, int b, int n, int i) {
   return g.layout == 0 ? (static_cast<int64_t>(b) * g.N + n) * g.S_q + i
                        : static_cast<int64_t>(s.q_start + i) * g.N + n;
+}
+
+// Position of local query row i of head n in the backward workspace's lse2 /
+// D arrays: head-major in both layouts ([B,N,S] for BNSD, [N,T] for TND), so
+// that the 128 rows of one head in a query tile are contiguous (in the [T,N]
+// order of the statistics they would be N elements apart, one cache line each).
+__device__ __forceinline__ int64_t ws_stat_index(const Geometry& g, const SeqInfo& s, int b, int n, int i) {
+  return g.layout == 0 ? (static_cast<int64_t>(b) * g.N + n) * g.S_q + i
+                       : static_cast<int64_t>(n) * g.T_q + (s.q_start + i);
 }
 
 // Keys visible to local query row i: [lo, hi] (empty when lo > hi).

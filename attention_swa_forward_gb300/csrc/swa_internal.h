@@ -22,9 +22,11 @@ struct SeqInfo {
 
 // Work description passed to a kernel as a parameter (no device upload):
 // a run of `heads * tiles` work items per entry.  A work item is one 128-row
-// query tile (forward) or key tile (backward) of one (batch, head).  For BNSD a
-// single entry covers all B*N heads (b < 0; b = head / N); for TND each entry
-// is one sequence (b >= 0; head = n).  Entries are ordered heaviest first and
+// query tile (forward) or key tile (backward) of one (batch, head), numbered
+// head by head (the tiles of one head are consecutive items, so the CTAs in
+// flight share that head's tiles in L2).  For BNSD a single entry covers all
+// B*N heads (b < 0; b = head / N); for TND each entry is one sequence (b >= 0;
+// head = n).  Entries are ordered heaviest first and
 // `descending` visits the tiles of an entry from the last one, so that the
 // CTAs that start first carry the most work.
 struct SeqDesc {
@@ -83,6 +85,7 @@ struct Geometry {
   int32_t drop_gen;   // 1: keep bits generated from (seed, offset) instead of read
   uint32_t seed_lo, seed_hi, off_lo;
   uint32_t keep_thr;  // element kept iff its Philox byte < keep_thr (0..256)
+  int32_t T_q;        // query rows per head: B*S_q (BNSD) or T_q (TND)
 };
 
 struct FwdArgs {
@@ -97,8 +100,8 @@ struct FwdArgs {
 struct BwdArgs {
   Geometry g;
   const uint8_t* mask;
-  const float* lse2;   // per query row: softmax_max*log2(e) + log2(softmax_sum); +inf for empty rows
-  const float* dsum;   // per query row: D = rowsum(dY * O)
+  const float* lse2;   // per query row, head-major (ws_stat_index): softmax_max*log2(e) + log2(softmax_sum); +inf for empty rows
+  const float* dsum;   // per query row, head-major: D = rowsum(dY * O)
   __nv_bfloat16* dq;   // written by the query-major pass
   __nv_bfloat16* dk;   // written by the key-major pass
   __nv_bfloat16* dv;
