@@ -66,6 +66,52 @@ __global__ void __launch_bounds__(256) swa_prep_kernel(const PrepArgs a) {
   }
 }
 
+// The same for D = 64 or 128 exactly, with more bytes in flight: a row is
+// split over D/8 lanes (16 bytes of dY and of O each), a warp covers 32/(D/8)
+// rows per load step and kSteps steps, all loads issued before any use.
+template <int D, bool F16>
+__global__ void __launch_bounds__(256) swa_prep_wide_kernel(const PrepArgs a) {
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerStep = 32 / kLanesPerRow;
+  constexpr int kSteps = 4;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0;  // fresh error word for this backward call
+  const int64_t row0 = warp * (kRowsPerStep * kSteps) + lane / kLanesPerRow;
+  const int col = (lane % kLanesPerRow) * 8;
+  uint4 dy[kSteps], o[kSteps];
+#pragma unroll
+  for (int k = 0; k < kSteps; ++k) {
+    const int64_t row = row0 + k * kRowsPerStep;
+    if (row < a.rows) {
+      dy[k] = __ldg(reinterpret_cast<const uint4*>(a.dy + row * D + col));
+      o[k] = __ldg(reinterpret_cast<const uint4*>(a.out + row * D + col));
+    } else {
+      dy[k] = o[k] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kSteps; ++k) {
+    const uint32_t d4[4] = {dy[k].x, dy[k].y, dy[k].z, dy[k].w}, o4[4] = {o[k].x, o[k].y, o[k].z, o[k].w};
+    float acc = 0.f;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float2 df = unpack2<F16>(d4[t]), of = unpack2<F16>(o4[t]);
+      acc = fmaf(df.x, of.x, acc);
+      acc = fmaf(df.y, of.y, acc);
+    }
+#pragma unroll
+    for (int m = kLanesPerRow / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, m);
+    const int64_t row = row0 + k * kRowsPerStep;
+    if (lane % kLanesPerRow == 0 && row < a.rows) {
+      const float l = a.ssum[row];
+      const int64_t ws = a.g.layout == 0 ? row : (row % a.g.N) * a.g.T_q + row / a.g.N;
+      a.dsum[ws] = acc;
+      a.lse2[ws] = (l > 0.f) ? a.smax[row] * kLog2e + __log2f(l) : INFINITY;
+    }
+  }
+}
+
 // The keep mask a seed / offset pair stands for, in the packed drop_mask
 // layout: thread = one query row of a 128-row tile; it generates its row's
 // keep bits 16 keys at a time and ORs them into the zeroed 32-bit words (a
@@ -105,6 +151,18 @@ template cudaError_t launch_dropout_mask<kLargeTable>(const MaskGenArgs&, const 
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream) {
   if (a.rows == 0) return cudaSuccess;
+  if (a.g.D == 64 || a.g.D == 128) {
+    const int64_t rows_per_block = 8 * (32 / (a.g.D / 8)) * 4;  // 8 warps x rows per step x 4 steps
+    const unsigned gr = static_cast<unsigned>((a.rows + rows_per_block - 1) / rows_per_block);
+    if (a.g.D == 64) {
+      if (a.g.f16) swa_prep_wide_kernel<64, true><<<gr, 256, 0, stream>>>(a);
+      else swa_prep_wide_kernel<64, false><<<gr, 256, 0, stream>>>(a);
+    } else {
+      if (a.g.f16) swa_prep_wide_kernel<128, true><<<gr, 256, 0, stream>>>(a);
+      else swa_prep_wide_kernel<128, false><<<gr, 256, 0, stream>>>(a);
+    }
+    return cudaGetLastError();
+  }
   const int64_t threads = a.rows * 32;
   const int block = 256;
   const int64_t grid = (threads + block - 1) / block;
