@@ -69,6 +69,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Has the phase with the given parity completed?  A non-blocking probe
+// (never suspends the thread): a query costs ~100 cycles on this part, so a
+// thread that will need a barrier later issues the probe early, does other
+// work while the answer is in flight, and only waits if the answer was no.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Slow path of mbar_wait.  The spin itself only polls the barrier and the
 // SM cycle counter; the error word (a global load, ~1000 cycles) and the wall
 // clock are consulted about every 2^20 cycles, so a completed phase is seen

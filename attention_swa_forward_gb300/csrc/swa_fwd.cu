@@ -188,10 +188,11 @@ __global__ void __launch_bounds__(224, 1)
     const float c = g.scale_log2;
     float m_use = -INFINITY, m_true = -INFINITY, l = 0.f;
     bool ok = true;
+    bool s_ready = false;  // S(it) known complete from a probe issued during the previous tile
     for (int it = 0; it < n_kv; ++it) {
       const int sb = it & 1;
       // warp-uniform outcome: the tcgen05.ld below is warp-collective
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&s.s_full[sb], (it >> 1) & 1, a.err, kErrFwdSoftmax))) {
+      if (!s_ready && !__all_sync(0xFFFFFFFFu, mbar_wait(&s.s_full[sb], (it >> 1) & 1, a.err, kErrFwdSoftmax))) {
         ok = false;
         break;
       }
@@ -215,6 +216,9 @@ __global__ void __launch_bounds__(224, 1)
       }
       tc_fence_before_sync();
       mbar_arrive(&s.s_free[sb]);
+      // P buffer sb was last read by PV(it-2): probe now, use the answer
+      // after the exponentials
+      const bool p_free = it < 2 || mbar_test(&s.o_done[sb], ((it >> 1) - 1) & 1);
       auto X = [&](int t) -> float { return __uint_as_float(xr[t]); };
 
       const int j0 = (kv_t0 + it) * kTileN;
@@ -288,7 +292,8 @@ __global__ void __launch_bounds__(224, 1)
       // rescale its rows of O also waits for PV(it-1); the others write P(it)
       // while PV(it-1) may still run, so the tensor pipe never waits for the
       // softmax's hand-off in the common case.
-      if (it >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait(&s.o_done[sb], ((it >> 1) - 1) & 1, a.err, kErrFwdSoftmax))) {
+      if (!__all_sync(0xFFFFFFFFu, p_free) &&
+          !__all_sync(0xFFFFFFFFu, mbar_wait(&s.o_done[sb], ((it >> 1) - 1) & 1, a.err, kErrFwdSoftmax))) {
         ok = false;
         break;
       }
@@ -312,11 +317,14 @@ __global__ void __launch_bounds__(224, 1)
           }
         }
       }
+      // probe the next tile's S while P is stored; the answer is used at the top of the next tile
+      const bool s_next = it + 1 < n_kv && mbar_test(&s.s_full[sb ^ 1], ((it + 1) >> 1) & 1);
       tmem_st_32x32b_x32(tmem + lane_off + kColP + sb * 64, *reinterpret_cast<const uint32_t(*)[32]>(&xr[0]));
       tmem_st_32x32b_x32(tmem + lane_off + kColP + sb * 64 + 32, *reinterpret_cast<const uint32_t(*)[32]>(&xr[32]));
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(&s.p_full[sb]);
+      s_ready = __all_sync(0xFFFFFFFFu, s_next);
     }
     if (ok && n_kv > 0) {
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s.o_done[(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1, a.err, kErrFwdSoftmax));
