@@ -125,11 +125,12 @@ swa_status_t make_plan(const swa_params_t* p, Plan& plan) {
   g.scale = static_cast<float>(p->scale);
   g.scale_log2 = static_cast<float>(p->scale * kLog2e);
   g.inv_keep = static_cast<float>(1.0 / p->keep_prob);
-  if (p->dtype == SWA_DTYPE_FP32)
-    return fail(SWA_ERR_UNSUPPORTED, "FLOAT32 inputs are not built (bf16 and fp16 are)");
-  if (p->dtype != SWA_DTYPE_BF16 && p->dtype != SWA_DTYPE_FP16)
+  if (p->dtype != SWA_DTYPE_BF16 && p->dtype != SWA_DTYPE_FP16 && p->dtype != SWA_DTYPE_FP32)
     return fail(SWA_ERR_PARAM_INVALID, "dtype should be 0 (bf16), 1 (fp16) or 2 (fp32), got %d", p->dtype);
+  // fp32: the kernels run on bf16 copies of the inputs made in the workspace
+  // and store fp32 outputs
   g.f16 = p->dtype == SWA_DTYPE_FP16 ? 1 : 0;
+  g.out_f32 = p->dtype == SWA_DTYPE_FP32 ? 1 : 0;
   if (p->dropout_gen != 0 && p->dropout_gen != 1)
     return fail(SWA_ERR_PARAM_INVALID, "dropout_gen should be 0 or 1, got %d", p->dropout_gen);
   g.has_mask = p->keep_prob < 1.0;
@@ -332,15 +333,43 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+size_t q_elems(const Plan& plan) { return static_cast<size_t>(plan.q_rows) * plan.g.N * plan.g.D; }
+size_t kv_elems(const Plan& plan) { return static_cast<size_t>(plan.kv_rows) * plan.g.N_kv * plan.g.D; }
+
+// fp32 inputs: bf16 copies of q, k, v (and for the backward dy, out) follow
+// the header / statistics in the workspace, each 256-byte aligned.
+struct FwdLayout {
+  size_t q16, k16, v16, total;
+};
+FwdLayout fwd_layout(const Plan& plan) {
+  FwdLayout l{};
+  l.total = kHeaderBytes;
+  if (plan.g.out_f32) {
+    l.q16 = l.total;
+    l.k16 = l.q16 + round256(q_elems(plan) * 2);
+    l.v16 = l.k16 + round256(kv_elems(plan) * 2);
+    l.total = l.v16 + round256(kv_elems(plan) * 2);
+  }
+  return l;
+}
+
 struct BwdLayout {
-  size_t lse2, dsum, total;
+  size_t lse2, dsum, q16, k16, v16, dy16, out16, total;
 };
 BwdLayout bwd_layout(const Plan& plan) {
   const size_t rows = static_cast<size_t>(plan.q_rows) * plan.g.N;
-  BwdLayout l;
+  BwdLayout l{};
   l.lse2 = kHeaderBytes;
   l.dsum = l.lse2 + round256(rows * 4);
   l.total = l.dsum + round256(rows * 4);
+  if (plan.g.out_f32) {
+    l.q16 = l.total;
+    l.k16 = l.q16 + round256(q_elems(plan) * 2);
+    l.v16 = l.k16 + round256(kv_elems(plan) * 2);
+    l.dy16 = l.v16 + round256(kv_elems(plan) * 2);
+    l.out16 = l.dy16 + round256(q_elems(plan) * 2);
+    l.total = l.out16 + round256(q_elems(plan) * 2);
+  }
   return l;
 }
 
@@ -379,7 +408,7 @@ swa_status_t swa_forward_workspace_size(const swa_params_t* p, size_t* bytes) {
   Plan plan;
   swa_status_t st = make_plan(p, plan);
   if (st != SWA_OK) return st;
-  *bytes = kHeaderBytes;
+  *bytes = fwd_layout(plan).total;
   return SWA_OK;
 }
 
@@ -407,9 +436,25 @@ swa_status_t swa_forward(const swa_params_t* p, const void* q, const void* k, co
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(softmax_max) ||
       !aligned16(softmax_sum) || !aligned16(drop_mask))
     return fail(SWA_ERR_PARAM_INVALID, "tensor pointers (and drop_mask) must be 16-byte aligned");
-  if (!workspace || workspace_bytes < kHeaderBytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return fail(SWA_ERR_WORKSPACE, "workspace must be >= %zu bytes and 256-byte aligned", kHeaderBytes);
+  const FwdLayout lay = fwd_layout(plan);
+  if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(SWA_ERR_WORKSPACE, "workspace must be >= %zu bytes and 256-byte aligned (got %zu)", lay.total,
+                workspace_bytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (plan.g.out_f32) {  // bf16 copies of the fp32 inputs
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const void* src[3] = {q, k, v};
+    const size_t off[3] = {lay.q16, lay.k16, lay.v16}, n[3] = {q_elems(plan), kv_elems(plan), kv_elems(plan)};
+    for (int t = 0; t < 3; ++t) {
+      e = launch_to_bf16(static_cast<const float*>(src[t]), reinterpret_cast<__nv_bfloat16*>(ws + off[t]),
+                         static_cast<int64_t>(n[t]), s);
+      if (e != cudaSuccess) return cuda_fail(e, "fp32 -> bf16 conversion launch");
+    }
+    q = ws + lay.q16;
+    k = ws + lay.k16;
+    v = ws + lay.v16;
+  }
 
   CUtensorMap mq, mk, mv;
   if ((st = make_map(&mq, q, plan, true, "q")) != SWA_OK) return st;
@@ -419,12 +464,12 @@ swa_status_t swa_forward(const swa_params_t* p, const void* q, const void* k, co
   FwdArgs a{};
   a.g = plan.g;
   a.mask = drop_mask;
-  a.out = static_cast<__nv_bfloat16*>(out);
+  a.out = out;
   a.smax = softmax_max;
   a.ssum = softmax_sum;
   a.err = static_cast<int32_t*>(workspace);
 
-  cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
+  e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
   const std::vector<SeqDesc> descs = build_descs(plan, true);
   if (t_ev[0]) cudaEventRecord(t_ev[0], s);
@@ -458,6 +503,23 @@ swa_status_t swa_backward(const swa_params_t* p, const void* q, const void* k, c
     return fail(SWA_ERR_WORKSPACE, "workspace must be >= %zu bytes and 256-byte aligned (got %zu)", lay.total,
                 workspace_bytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (plan.g.out_f32) {  // bf16 copies of the fp32 inputs (out only feeds the preprocess)
+    const void* src[5] = {q, k, v, dy, out};
+    const size_t off[5] = {lay.q16, lay.k16, lay.v16, lay.dy16, lay.out16};
+    const size_t n[5] = {q_elems(plan), kv_elems(plan), kv_elems(plan), q_elems(plan), q_elems(plan)};
+    for (int t = 0; t < 5; ++t) {
+      const cudaError_t ce = launch_to_bf16(static_cast<const float*>(src[t]),
+                                            reinterpret_cast<__nv_bfloat16*>(ws + off[t]),
+                                            static_cast<int64_t>(n[t]), s);
+      if (ce != cudaSuccess) return cuda_fail(ce, "fp32 -> bf16 conversion launch");
+    }
+    q = ws + lay.q16;
+    k = ws + lay.k16;
+    v = ws + lay.v16;
+    dy = ws + lay.dy16;
+    out = ws + lay.out16;
+  }
 
   CUtensorMap mq, mk, mv, mdy;
   if ((st = make_map(&mq, q, plan, true, "q")) != SWA_OK) return st;
@@ -465,7 +527,6 @@ swa_status_t swa_backward(const swa_params_t* p, const void* q, const void* k, c
   if ((st = make_map(&mv, v, plan, false, "v")) != SWA_OK) return st;
   if ((st = make_map(&mdy, dy, plan, true, "dy")) != SWA_OK) return st;
 
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* lse2 = reinterpret_cast<float*>(ws + lay.lse2);
   float* dsum = reinterpret_cast<float*>(ws + lay.dsum);
   const int64_t rows = plan.q_rows * plan.g.N;
@@ -488,9 +549,9 @@ swa_status_t swa_backward(const swa_params_t* p, const void* q, const void* k, c
   a.mask = drop_mask;
   a.lse2 = lse2;
   a.dsum = dsum;
-  a.dq = static_cast<__nv_bfloat16*>(dq);
-  a.dk = static_cast<__nv_bfloat16*>(dk);
-  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
   a.err = reinterpret_cast<int32_t*>(ws);
   // key-major pass: dK, dV (one work item per key tile)
   const std::vector<SeqDesc> kv_descs = build_descs(plan, false);

@@ -149,6 +149,28 @@ cudaError_t launch_dropout_mask(const MaskGenArgs& a, const SeqTable<CAP>& tab, 
 template cudaError_t launch_dropout_mask<kSmallTable>(const MaskGenArgs&, const SeqTable<kSmallTable>&, cudaStream_t);
 template cudaError_t launch_dropout_mask<kLargeTable>(const MaskGenArgs&, const SeqTable<kLargeTable>&, cudaStream_t);
 
+// fp32 -> bf16, eight elements (two 16-byte loads, one 16-byte store) per
+// thread and grid-stride step.
+__global__ void __launch_bounds__(256) swa_to_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* __restrict__ out,
+                                                          int64_t n8) {
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n8;
+       k += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(in) + 2 * k);
+    const float4 b = __ldg(reinterpret_cast<const float4*>(in) + 2 * k + 1);
+    const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    reinterpret_cast<uint4*>(out)[k] = pack8<false>(x);
+  }
+}
+
+cudaError_t launch_to_bf16(const float* in, __nv_bfloat16* out, int64_t n, cudaStream_t stream) {
+  const int64_t n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  const int64_t want = (n8 + 255) / 256;
+  const unsigned grid = static_cast<unsigned>(want < 152 * 16 ? want : 152 * 16);
+  swa_to_bf16_kernel<<<grid, 256, 0, stream>>>(in, out, n8);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream) {
   if (a.rows == 0) return cudaSuccess;
   if (a.g.D == 64 || a.g.D == 128) {

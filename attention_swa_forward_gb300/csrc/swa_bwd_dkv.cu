@@ -468,7 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool kv_valid = j < sq.kv_len;
       const uint32_t dcol = h == 0 ? kColDV : kColDK;
       const float mul = h == 0 ? 1.f : g.scale;
-      __nv_bfloat16* dst = (h == 0 ? a.dv : a.dk) + kv_elem(g, sq, w.b, w.n, j);
+      void* dbase = h == 0 ? a.dv : a.dk;
+      const int64_t dst = kv_elem(g, sq, w.b, w.n, j);
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
         if (ch * 32 >= g.D) break;  // columns past D are padding
@@ -486,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kv_valid) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
-            if (ch * 32 + q4 * 8 < g.D) reinterpret_cast<uint4*>(dst + ch * 32)[q4] = pack8<F16>(&o[q4 * 8]);
+            if (ch * 32 + q4 * 8 < g.D) store8<F16>(dbase, dst + ch * 32 + q4 * 8, &o[q4 * 8], g.out_f32);
         }
       }
     }

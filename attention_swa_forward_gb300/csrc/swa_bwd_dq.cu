@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       // epilogue: dQ = scale * acc, row r, columns [h*D/2, h*D/2 + D/2)
       constexpr int kCols = D / 2;
-      __nv_bfloat16* dst = a.dq + q_elem(g, sq, w.b, w.n, i) + h * kCols;
+      const int64_t dst = q_elem(g, sq, w.b, w.n, i) + h * kCols;
 #pragma unroll
       for (int ch = 0; ch < kCols / 32; ++ch) {
         if (h * kCols + ch * 32 >= g.D) break;  // columns past D are padding
@@ -360,8 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row_valid) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
-            if (h * kCols + ch * 32 + q4 * 8 < g.D)
-              reinterpret_cast<uint4*>(dst + ch * 32)[q4] = pack8<F16>(&o[q4 * 8]);
+            if (h * kCols + ch * 32 + q4 * 8 < g.D) store8<F16>(a.dq, dst + ch * 32 + q4 * 8, &o[q4 * 8], g.out_f32);
         }
       }
     }

@@ -217,4 +217,18 @@ __device__ __forceinline__ uint4 pack8(const float* x) {
   return v;
 }
 
+// Eight consecutive output elements from element e of `base` on: packed to
+// the element type (bf16 / fp16), or stored as fp32 when `f32`.  e is a
+// multiple of 8, so both forms are 16-byte aligned.
+template <bool F16>
+__device__ __forceinline__ void store8(void* base, int64_t e, const float* x, bool f32) {
+  if (f32) {
+    float4* d = reinterpret_cast<float4*>(static_cast<float*>(base) + e);
+    d[0] = make_float4(x[0], x[1], x[2], x[3]);
+    d[1] = make_float4(x[4], x[5], x[6], x[7]);
+  } else {
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + e) = pack8<F16>(x);
+  }
+}
+
 }  // namespace swa

@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(224, 1)
     if (ok) {
       // epilogue: O = acc / (l * keep), statistics before dropout
       const float inv = (l > 0.f) ? g.inv_keep / l : 0.f;
-      __nv_bfloat16* orow = a.out + q_elem(g, sq, w.b, w.n, i);
+      const int64_t orow = q_elem(g, sq, w.b, w.n, i);
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
         if (ch * 32 >= g.D) break;  // columns past D are padding
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(224, 1)
         if (row_valid) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
-            if (ch * 32 + q4 * 8 < g.D) reinterpret_cast<uint4*>(orow + ch * 32)[q4] = pack8<F16>(&o[q4 * 8]);
+            if (ch * 32 + q4 * 8 < g.D) store8<F16>(a.out, orow + ch * 32 + q4 * 8, &o[q4 * 8], g.out_f32);
         }
       }
       if (row_valid) {

@@ -86,12 +86,13 @@ struct Geometry {
   uint32_t seed_lo, seed_hi, off_lo;
   uint32_t keep_thr;  // element kept iff its Philox byte < keep_thr (0..256)
   int32_t T_q;        // query rows per head: B*S_q (BNSD) or T_q (TND)
+  int32_t out_f32;    // outputs (out, dq, dk, dv) are fp32; the kernels then read bf16 copies of the inputs
 };
 
 struct FwdArgs {
   Geometry g;
   const uint8_t* mask;
-  __nv_bfloat16* out;
+  void* out;  // bf16 / fp16, or fp32 when g.out_f32
   float* smax;
   float* ssum;
   int32_t* err;
@@ -102,9 +103,9 @@ struct BwdArgs {
   const uint8_t* mask;
   const float* lse2;   // per query row, head-major (ws_stat_index): softmax_max*log2(e) + log2(softmax_sum); +inf for empty rows
   const float* dsum;   // per query row, head-major: D = rowsum(dY * O)
-  __nv_bfloat16* dq;   // written by the query-major pass
-  __nv_bfloat16* dk;   // written by the key-major pass
-  __nv_bfloat16* dv;
+  void* dq;   // written by the query-major pass (element type as FwdArgs::out)
+  void* dk;   // written by the key-major pass
+  void* dv;
   int32_t* err;
 };
 
@@ -141,6 +142,8 @@ cudaError_t launch_backward_dq(const BwdArgs& a, const SeqTable<CAP>& tab, const
                                const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdy,
                                cudaStream_t stream);
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream);
+// fp32 -> bf16 (round to nearest even) of n elements, n a multiple of 8, both 16-byte aligned.
+cudaError_t launch_to_bf16(const float* in, __nv_bfloat16* out, int64_t n, cudaStream_t stream);
 
 // The packed keep mask a seed / offset pair stands for: one CTA per query
 // tile of a (batch, head) from the forward's work table, one thread per

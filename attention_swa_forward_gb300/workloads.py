@@ -148,7 +148,7 @@ def draw(geom: Geometry, seed: int, lengths: tuple | None = None, with_dy: bool 
         lens = torch.randint(lo, hi + 1, (count,), generator=g).tolist()
         cu = np.cumsum(lens).tolist()
         geom = Geometry(**{**geom.as_dict(), "B": count, "cu_seqlens_q": cu, "cu_seqlens_kv": list(cu)})
-    dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[geom.dtype]
+    dt = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[geom.dtype]
     q = torch.randn(geom.q_shape(), generator=g).to(dt)
     k = torch.randn(geom.kv_shape(), generator=g).to(dt)
     v = torch.randn(geom.kv_shape(), generator=g).to(dt)

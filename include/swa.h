@@ -122,8 +122,12 @@ typedef struct {
   uint64_t dropout_seed;
   uint64_t dropout_offset;
   int32_t dtype;                /* element type of q, k, v, dy, out, dq, dk, dv (doc: FLOAT16 /
-                                   BFLOAT16 / FLOAT32): SWA_DTYPE_BF16 (0, default) or
-                                   SWA_DTYPE_FP16 (1); FLOAT32 returns SWA_ERR_UNSUPPORTED */
+                                   BFLOAT16 / FLOAT32): SWA_DTYPE_BF16 (0, default),
+                                   SWA_DTYPE_FP16 (1) or SWA_DTYPE_FP32 (2).  fp32: the
+                                   tensor-core operands are bf16 copies of the inputs
+                                   (rounded to nearest even, made in the workspace), every
+                                   accumulation is fp32 as for the other types, and the
+                                   outputs are stored in fp32 */
 } swa_params_t;
 
 typedef enum { SWA_DTYPE_BF16 = 0, SWA_DTYPE_FP16 = 1, SWA_DTYPE_FP32 = 2 } swa_dtype_t;
@@ -134,11 +138,13 @@ typedef enum { SWA_DTYPE_BF16 = 0, SWA_DTYPE_FP16 = 1, SWA_DTYPE_FP32 = 2 } swa_
 SWA_API void swa_params_default(swa_params_t *p);
 
 /* Device workspace bytes that swa_forward needs for these parameters (a
- * status word; the work schedule travels as a kernel parameter).  Errors: SWA_ERR_PARAM_NULLPTR, SWA_ERR_PARAM_INVALID, SWA_ERR_UNSUPPORTED. */
+ * status word; the work schedule travels as a kernel parameter; with fp32
+ * inputs also bf16 copies of q, k and v).  Errors: SWA_ERR_PARAM_NULLPTR,
+ * SWA_ERR_PARAM_INVALID, SWA_ERR_UNSUPPORTED. */
 SWA_API swa_status_t swa_forward_workspace_size(const swa_params_t *p, size_t *bytes);
 
 /* Forward (doc formula; PyPTO-Gym "前向公式").
- *   q, k, v       device, p->dtype (bf16 / fp16), layout per p->layout
+ *   q, k, v       device, p->dtype (bf16 / fp16 / fp32), layout per p->layout
  *   drop_mask     device, packed keep bits, 16-byte aligned; NULL iff keep_prob == 1
  *                 or dropout_gen == 1
  *   out           device, p->dtype, q's shape
@@ -153,7 +159,8 @@ SWA_API swa_status_t swa_forward(const swa_params_t *p, const void *q, const voi
 
 /* Device workspace bytes that swa_backward needs: a status word, and per
  * query row D = rowsum(dY*O) and the log2-sum-exp of the forward statistics
- * (8 bytes per query row and head). */
+ * (8 bytes per query row and head); with fp32 inputs also bf16 copies of q,
+ * k, v, dy and out. */
 SWA_API swa_status_t swa_backward_workspace_size(const swa_params_t *p, size_t *bytes);
 
 /* Backward (PyPTO-Gym "反向公式"; aclnnFlashAttentionUnpaddingScoreGradV2

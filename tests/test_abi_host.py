@@ -108,9 +108,9 @@ BASE = dict(layout="BNSD", B=1, N=2, D=128, S_q=256, S_kv=256, scale=0.1, sparse
     ({"N": 8, "N_kv": 3}, swa.SWA_ERR_PARAM_INVALID),
     ({"N": 4, "N_kv": 8}, swa.SWA_ERR_PARAM_INVALID),
     ({"N": 4, "N_kv": -2}, swa.SWA_ERR_PARAM_INVALID),
-    # element types: bf16 and fp16 built, fp32 not
+    # element types: bf16, fp16, and fp32 (computed on bf16 copies, fp32 outputs)
     ({"dtype": "fp16"}, swa.SWA_OK),
-    ({"dtype": "fp32"}, swa.SWA_ERR_UNSUPPORTED),
+    ({"dtype": "fp32"}, swa.SWA_OK),
 ])
 def test_parameter_checks(lib, change, status):
     st, _ = _size(Geometry(**{**BASE, **change}))
@@ -177,3 +177,19 @@ def test_workspace_sizes_scale_with_rows(lib):
     assert f == 256
     assert b >= 2 * rows * 4  # D + lse2 per query row and head
     assert b < 2 * rows * 4 + 4096
+
+
+def test_fp32_workspace_holds_bf16_copies(lib):
+    """fp32 inputs: the workspace also holds bf16 copies of q, k, v (forward)
+    and of q, k, v, dy, out (backward), each 256-byte aligned."""
+    g = Geometry("BNSD", 2, 4, 72, S_q=300, S_kv=200, N_kv=2, sparse_mode=0, dtype="fp32")
+    st_f, f = _size(g)
+    st_b, b = _size(g, backward=True)
+    assert st_f == swa.SWA_OK and st_b == swa.SWA_OK
+    r256 = lambda x: (x + 255) // 256 * 256
+    qe, kve = 2 * 4 * 300 * 72, 2 * 2 * 200 * 72
+    assert f == 256 + r256(2 * qe) + 2 * r256(2 * kve)
+    stats = 2 * r256(2 * 4 * 300 * 4)
+    assert b == 256 + stats + 3 * r256(2 * qe) + 2 * r256(2 * kve)
+    g16 = Geometry(**{**g.as_dict(), "dtype": "bf16"})
+    assert _size(g16)[1] == 256 and _size(g16, backward=True)[1] == 256 + stats

@@ -160,6 +160,14 @@ SMALL = {
                                 sparse_mode=4, pre_tokens=100, next_tokens=0, dtype="fp16"),
     "bnsd_rect_band_d40": dict(layout="BNSD", B=1, N=2, D=40, S_q=150, S_kv=330, scale=40 ** -0.5, sparse_mode=4,
                                pre_tokens=40, next_tokens=160),
+    # fp32 inputs and outputs (the MMAs take bf16 copies of the inputs)
+    "bnsd_band_d128_ragged_fp32": dict(layout="BNSD", B=1, N=3, D=128, S_q=517, S_kv=517, scale=128 ** -0.5,
+                                       sparse_mode=4, pre_tokens=200, next_tokens=0, dtype="fp32"),
+    "tnd_varlen_band_dropout_d64_fp32": dict(layout="TND", B=4, N=3, D=64, cu_seqlens_q=[200, 201, 460, 0],
+                                             cu_seqlens_kv=[200, 201, 460, 0], scale=0.125, sparse_mode=4,
+                                             pre_tokens=100, next_tokens=17, keep_prob=0.85, dtype="fp32"),
+    "bnsd_gqa2_nomask_d72_fp32": dict(layout="BNSD", B=1, N=4, N_kv=2, D=72, S_q=290, S_kv=290, scale=72 ** -0.5,
+                                      sparse_mode=0, dtype="fp32"),
 }
 
 
@@ -168,9 +176,24 @@ def test_small_parity(name):
     geom = Geometry(**SMALL[name])
     inp = draw(geom, 5000 + sum(map(ord, name)))
     pr = to_problem(geom)
+    res = as_np(run_gpu(inp))
+    if geom.dtype == "fp32":
+        # fp32 inputs are computed on their bf16 roundings (include/swa.h): every
+        # gate against the oracle on those operands, and the out / gradient
+        # gates also against the oracle on the exact fp32 inputs
+        rq, rk, rv, rdy = (t.to(torch.bfloat16).to(torch.float32) for t in (inp.q, inp.k, inp.v, inp.dy))
+        out, smax, ssum = orc.forward(pr, rq, rk, rv, inp.drop_mask)
+        dq, dk, dv = orc.backward(pr, rq, rk, rv, rdy, inp.drop_mask)
+        check_forward(res, out, smax, ssum, name)
+        check_grads(res, dq, dk, dv, name)
+        out_x, _, _ = orc.forward(pr, inp.q, inp.k, inp.v, inp.drop_mask)
+        dq_x, dk_x, dv_x = orc.backward(pr, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask)
+        e_out, a_out = rel_l2(res["out"], out_x), excess(res["out"], out_x)
+        assert e_out <= TOL_OUT and a_out <= 0.0, (name, "out vs exact fp32 inputs", e_out, a_out)
+        check_grads(res, dq_x, dk_x, dv_x, name + " vs exact fp32 inputs")
+        return
     out, smax, ssum = orc.forward(pr, inp.q, inp.k, inp.v, inp.drop_mask)
     dq, dk, dv = orc.backward(pr, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask)
-    res = as_np(run_gpu(inp))
     check_forward(res, out, smax, ssum, name)
     check_grads(res, dq, dk, dv, name)
 
