@@ -1,0 +1,212 @@
+// swa_host.cpp — swa_step_host: forward + backward of a problem whose inputs
+// and outputs live in host memory, with the host <-> device copies overlapped
+// with the computation.
+//
+// The heads are split into `chunks` equal groups.  Each group is a complete
+// smaller problem (heads are independent in every step of the method), so it
+// is copied into its own compact device tensors, computed by swa_forward and
+// swa_backward on the caller's stream, and copied back.  Chunk c+1's inputs
+// travel host -> device on one stream and chunk c-1's results device -> host
+// on another while chunk c computes.  A head group of a BNSD tensor is one
+// contiguous block per batch, and of a TND tensor one block per row, so every
+// copy is a single 2-D copy (rows = batches or tokens, pitch = the full row).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "swa.h"
+#include "swa_internal.h"
+
+namespace {
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Copy geometry of one tensor for one head group: `rows` rows of `width`
+// bytes at `pitch` on the host, packed back to back on the device.
+struct Span {
+  size_t rows = 0, width = 0, pitch = 0, first = 0;  // first: byte offset of head group 0's first row
+  size_t dev_bytes() const { return rows * width; }
+  size_t host_offset(int c) const { return first + static_cast<size_t>(c) * width; }
+};
+
+struct Layout {
+  swa_params_t sub;             // the per-chunk problem
+  Span q, kv, st;               // q-like (q, dy, out, dq), k-like (k, v, dk, dv), statistics
+  size_t q_off, k_off, v_off, dy_off, out_off, dq_off, dk_off, dv_off, smax_off, ssum_off;  // within a chunk
+  size_t fws_off, bws_off, chunk_bytes;
+  size_t fws_bytes, bws_bytes;
+  size_t total;
+};
+
+swa_status_t make_layout(const swa_params_t* p, int chunks, Layout& L) {
+  if (!p) return swa::set_error(SWA_ERR_PARAM_NULLPTR, "params is NULL");
+  if (chunks < 1) return swa::set_error(SWA_ERR_PARAM_INVALID, "chunks must be >= 1, got %d", chunks);
+  const int64_t n_kv = p->N_kv == 0 ? p->N : p->N_kv;
+  if (p->N % chunks != 0 || n_kv % chunks != 0)
+    return swa::set_error(SWA_ERR_PARAM_INVALID, "chunks = %d must divide N = %lld and N_kv = %lld", chunks,
+                          (long long)p->N, (long long)n_kv);
+  if (p->keep_prob < 1.0 && (p->dropout_gen == 0 || chunks != 1))
+    return swa::set_error(SWA_ERR_PARAM_INVALID,
+                          "swa_step_host takes no drop_mask: dropout needs dropout_gen = 1 and chunks = 1 "
+                          "(the generated keep bits are indexed by the whole problem's heads)");
+  L.sub = *p;
+  L.sub.N = p->N / chunks;
+  L.sub.N_kv = p->N_kv == 0 ? 0 : p->N_kv / chunks;
+  // validates everything else, on the chunk's problem
+  swa_status_t st = swa_forward_workspace_size(&L.sub, &L.fws_bytes);
+  if (st != SWA_OK) return st;
+  if ((st = swa_backward_workspace_size(&L.sub, &L.bws_bytes)) != SWA_OK) return st;
+
+  const size_t elt = p->dtype == SWA_DTYPE_FP32 ? 4 : 2;
+  const size_t D = static_cast<size_t>(p->D), Nq = static_cast<size_t>(p->N), Nk = static_cast<size_t>(n_kv);
+  const size_t nq = Nq / chunks, nk = Nk / chunks;
+  if (p->layout == SWA_LAYOUT_BNSD) {
+    const size_t B = static_cast<size_t>(p->B), Sq = static_cast<size_t>(p->S_q), Sk = static_cast<size_t>(p->S_kv);
+    L.q = Span{B, nq * Sq * D * elt, Nq * Sq * D * elt, 0};
+    L.kv = Span{B, nk * Sk * D * elt, Nk * Sk * D * elt, 0};
+    L.st = Span{B, nq * Sq * 4, Nq * Sq * 4, 0};
+  } else {
+    const size_t Tq = static_cast<size_t>(p->T_q), Tk = static_cast<size_t>(p->T_kv);
+    L.q = Span{Tq, nq * D * elt, Nq * D * elt, 0};
+    L.kv = Span{Tk, nk * D * elt, Nk * D * elt, 0};
+    L.st = Span{Tq, nq * 4, Nq * 4, 0};
+  }
+  size_t o = 0;
+  auto take = [&o](size_t bytes) { const size_t at = o; o += round256(bytes); return at; };
+  L.q_off = take(L.q.dev_bytes());
+  L.k_off = take(L.kv.dev_bytes());
+  L.v_off = take(L.kv.dev_bytes());
+  L.dy_off = take(L.q.dev_bytes());
+  L.out_off = take(L.q.dev_bytes());
+  L.dq_off = take(L.q.dev_bytes());
+  L.dk_off = take(L.kv.dev_bytes());
+  L.dv_off = take(L.kv.dev_bytes());
+  L.smax_off = take(L.st.dev_bytes());
+  L.ssum_off = take(L.st.dev_bytes());
+  L.fws_off = take(L.fws_bytes);  // each chunk keeps its own status words
+  L.bws_off = take(L.bws_bytes);
+  L.chunk_bytes = o;
+  L.total = o * static_cast<size_t>(chunks);
+  return SWA_OK;
+}
+
+cudaError_t copy_in(const Span& s, int c, void* dev, const void* host, cudaStream_t st) {
+  return cudaMemcpy2DAsync(dev, s.width, static_cast<const uint8_t*>(host) + s.host_offset(c), s.pitch, s.width,
+                           s.rows, cudaMemcpyHostToDevice, st);
+}
+cudaError_t copy_out(const Span& s, int c, void* host, const void* dev, cudaStream_t st) {
+  return cudaMemcpy2DAsync(static_cast<uint8_t*>(host) + s.host_offset(c), s.pitch, dev, s.width, s.width, s.rows,
+                           cudaMemcpyDeviceToHost, st);
+}
+
+swa_status_t cuda_fail(cudaError_t e, const char* what) {
+  return swa::set_error(SWA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+swa_status_t swa_step_host_buffer_size(const swa_params_t* p, int chunks, size_t* bytes) {
+  if (!bytes) return swa::set_error(SWA_ERR_PARAM_NULLPTR, "bytes is NULL");
+  Layout L;
+  swa_status_t st = make_layout(p, chunks, L);
+  if (st != SWA_OK) return st;
+  *bytes = L.total;
+  return SWA_OK;
+}
+
+swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, const void* k, const void* v,
+                           const void* dy, void* out, float* softmax_max, float* softmax_sum, void* dq, void* dk,
+                           void* dv, void* device_buffer, size_t device_bytes, swa_stream_t stream) {
+  Layout L;
+  swa_status_t st = make_layout(p, chunks, L);
+  if (st != SWA_OK) return st;
+  if (!q || !k || !v || !dy || !out || !softmax_max || !softmax_sum || !dq || !dk || !dv)
+    return swa::set_error(SWA_ERR_PARAM_NULLPTR, "a required host pointer is NULL");
+  if (!device_buffer || device_bytes < L.total || (reinterpret_cast<uintptr_t>(device_buffer) & 255u))
+    return swa::set_error(SWA_ERR_WORKSPACE, "device_buffer must be >= %zu bytes and 256-byte aligned (got %zu)",
+                          L.total, device_bytes);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // Two copy streams and their events, released by the driver once their
+  // work has run (cudaStreamDestroy / cudaEventDestroy on pending work).
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  std::vector<cudaEvent_t> ev;
+  auto release = [&]() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    if (s_in) cudaStreamDestroy(s_in);
+    if (s_out) cudaStreamDestroy(s_out);
+  };
+  auto event = [&](cudaEvent_t* e) {
+    const cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
+    if (r == cudaSuccess) ev.push_back(*e);
+    return r;
+  };
+  cudaError_t e = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking);
+  cudaEvent_t start = nullptr, done = nullptr;
+  if (e == cudaSuccess) e = event(&start);
+  if (e == cudaSuccess) e = event(&done);
+  // the copies may not start before what the caller queued earlier (which may still use the buffer)
+  if (e == cudaSuccess) e = cudaEventRecord(start, cs);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_in, start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, start, 0);
+  if (e != cudaSuccess) {
+    release();
+    return cuda_fail(e, "setting up the copy streams");
+  }
+  uint8_t* base = static_cast<uint8_t*>(device_buffer);
+  for (int c = 0; c < chunks; ++c) {
+    uint8_t* d = base + static_cast<size_t>(c) * L.chunk_bytes;
+    cudaEvent_t in_done = nullptr, comp_done = nullptr;
+    if ((e = event(&in_done)) != cudaSuccess || (e = event(&comp_done)) != cudaSuccess) break;
+    if ((e = copy_in(L.q, c, d + L.q_off, q, s_in)) != cudaSuccess) break;
+    if ((e = copy_in(L.kv, c, d + L.k_off, k, s_in)) != cudaSuccess) break;
+    if ((e = copy_in(L.kv, c, d + L.v_off, v, s_in)) != cudaSuccess) break;
+    if ((e = copy_in(L.q, c, d + L.dy_off, dy, s_in)) != cudaSuccess) break;
+    if ((e = cudaEventRecord(in_done, s_in)) != cudaSuccess) break;
+    if ((e = cudaStreamWaitEvent(cs, in_done, 0)) != cudaSuccess) break;
+    st = swa_forward(&L.sub, d + L.q_off, d + L.k_off, d + L.v_off, nullptr, d + L.out_off,
+                     reinterpret_cast<float*>(d + L.smax_off), reinterpret_cast<float*>(d + L.ssum_off),
+                     d + L.fws_off, L.fws_bytes, stream);
+    if (st != SWA_OK) break;
+    st = swa_backward(&L.sub, d + L.q_off, d + L.k_off, d + L.v_off, d + L.dy_off, d + L.out_off,
+                      reinterpret_cast<const float*>(d + L.smax_off), reinterpret_cast<const float*>(d + L.ssum_off),
+                      nullptr, d + L.dq_off, d + L.dk_off, d + L.dv_off, d + L.bws_off, L.bws_bytes, stream);
+    if (st != SWA_OK) break;
+    if ((e = cudaEventRecord(comp_done, cs)) != cudaSuccess) break;
+    if ((e = cudaStreamWaitEvent(s_out, comp_done, 0)) != cudaSuccess) break;
+    if ((e = copy_out(L.q, c, out, d + L.out_off, s_out)) != cudaSuccess) break;
+    if ((e = copy_out(L.st, c, softmax_max, d + L.smax_off, s_out)) != cudaSuccess) break;
+    if ((e = copy_out(L.st, c, softmax_sum, d + L.ssum_off, s_out)) != cudaSuccess) break;
+    if ((e = copy_out(L.q, c, dq, d + L.dq_off, s_out)) != cudaSuccess) break;
+    if ((e = copy_out(L.kv, c, dk, d + L.dk_off, s_out)) != cudaSuccess) break;
+    if ((e = copy_out(L.kv, c, dv, d + L.dv_off, s_out)) != cudaSuccess) break;
+  }
+  // the caller's stream completes only after the last result has reached the host
+  if (e == cudaSuccess) e = cudaEventRecord(done, s_out);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, done, 0);
+  release();
+  if (st != SWA_OK) return st;
+  if (e != cudaSuccess) return cuda_fail(e, "host step copies");
+  return SWA_OK;
+}
+
+swa_status_t swa_step_host_status(const swa_params_t* p, int chunks, const void* device_buffer,
+                                  swa_stream_t stream) {
+  Layout L;
+  swa_status_t st = make_layout(p, chunks, L);
+  if (st != SWA_OK) return st;
+  if (!device_buffer) return swa::set_error(SWA_ERR_PARAM_NULLPTR, "device_buffer is NULL");
+  const uint8_t* base = static_cast<const uint8_t*>(device_buffer);
+  for (int c = 0; c < chunks; ++c) {
+    const uint8_t* d = base + static_cast<size_t>(c) * L.chunk_bytes;
+    if ((st = swa_workspace_status(d + L.fws_off, stream)) != SWA_OK) return st;
+    if ((st = swa_workspace_status(d + L.bws_off, stream)) != SWA_OK) return st;
+  }
+  return SWA_OK;
+}
+
+}  // extern "C"

@@ -90,6 +90,13 @@ def lib() -> ctypes.CDLL:
             L.swa_workspace_status.restype = st
             L.swa_dropout_mask.argtypes = [P, vp, sz, vp]
             L.swa_dropout_mask.restype = st
+            ci = ctypes.c_int
+            L.swa_step_host_buffer_size.argtypes = [P, ci, ctypes.POINTER(sz)]
+            L.swa_step_host_buffer_size.restype = st
+            L.swa_step_host.argtypes = [P, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.swa_step_host.restype = st
+            L.swa_step_host_status.argtypes = [P, ci, vp, vp]
+            L.swa_step_host_status.restype = st
             L.swa_set_timing_events.argtypes = [vp]
             L.swa_set_timing_events.restype = None
             L.swa_last_error.argtypes = []
@@ -101,7 +108,8 @@ def lib() -> ctypes.CDLL:
 def exported_symbols():
     return ["swa_params_default", "swa_forward_workspace_size", "swa_forward", "swa_backward_workspace_size",
             "swa_backward", "swa_backward_noalloc", "swa_workspace_status", "swa_set_timing_events",
-            "swa_last_error", "swa_dropout_mask"]
+            "swa_last_error", "swa_dropout_mask", "swa_step_host_buffer_size", "swa_step_host",
+            "swa_step_host_status"]
 
 
 def _check(status: int):
@@ -186,6 +194,19 @@ def swa_dropout_mask(params: "Params", mask, mask_bytes: int, stream) -> int:
     return lib().swa_dropout_mask(params.ref(), mask, mask_bytes, stream)
 
 
+def swa_step_host_buffer_size(params: "Params", chunks: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().swa_step_host_buffer_size(params.ref(), int(chunks), ctypes.byref(n)))
+    return n.value
+
+
+def swa_step_host(params: "Params", chunks, q, k, v, dy, out, softmax_max, softmax_sum, dq, dk, dv, device_buffer,
+                  device_bytes, stream) -> int:
+    """Raw call: host pointers for the tensors, a device pointer for the buffer."""
+    return lib().swa_step_host(params.ref(), int(chunks), q, k, v, dy, out, softmax_max, softmax_sum, dq, dk, dv,
+                               device_buffer, device_bytes, stream)
+
+
 _timing_handles = None
 
 
@@ -257,6 +278,27 @@ def dropout_mask(geom, device="cuda:0", stream=None):
     mask = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
     _check(swa_dropout_mask(Params(geom), _ptr(mask), mask.numel(), _stream_handle(stream)))
     return mask
+
+
+def step_host(geom, q, k, v, dy, out, softmax_max, softmax_sum, dq, dk, dv, chunks=1, device_buffer=None,
+              stream=None, device="cuda:0"):
+    """Enqueue swa_step_host on host tensors (page-locked for overlap): forward
+    and backward with the copies overlapped with the computation.  Results
+    land in the given host tensors when the stream completes.  Returns the
+    device buffer (reuse it for the next call)."""
+    p = Params(geom)
+    need = swa_step_host_buffer_size(p, chunks)
+    if device_buffer is None:
+        device_buffer = torch.empty(need, dtype=torch.uint8, device=device)
+    _check(swa_step_host(p, chunks, _ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(out), _ptr(softmax_max),
+                         _ptr(softmax_sum), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(device_buffer), device_buffer.numel(),
+                         _stream_handle(stream)))
+    return device_buffer
+
+
+def check_step_host(geom, chunks, device_buffer, stream=None):
+    """Wait for the stream and raise if a kernel of a swa_step_host call gave up a bounded wait."""
+    _check(lib().swa_step_host_status(Params(geom).ref(), int(chunks), _ptr(device_buffer), _stream_handle(stream)))
 
 
 def check_workspace(workspace, stream=None):

@@ -350,7 +350,19 @@ def run_swa(args, name: str):
             hmask.numel() if hmask is not None else 0)
         d2h = sum(t.numel() * t.element_size() for t in h_out)
 
+        # swa_step_host (host buffers through the C ABI, copies overlapped with
+        # the computation in head groups) wherever it applies; a packed keep
+        # mask has no host-step form, so that case copies and calls the device API
+        chunks = 0
+        if hmask is None:
+            n_kv = g.N_kv or g.N
+            chunks = next(c for c in (8, 4, 2, 1) if g.N % c == 0 and n_kv % c == 0 and (c == 1 or g.keep_prob == 1.0))
+            step_buf = torch.empty(swa.swa_step_host_buffer_size(p, chunks), dtype=torch.uint8, device=dev)
+
         def e2e_step():
+            if chunks:
+                swa.step_host(g, hq, hk, hv, hdy, *h_out, chunks=chunks, device_buffer=step_buf, stream=stream)
+                return
             q.copy_(hq, non_blocking=True)
             k.copy_(hk, non_blocking=True)
             v.copy_(hv, non_blocking=True)
@@ -372,7 +384,10 @@ def run_swa(args, name: str):
         t_e2e = (time.perf_counter() - t0) / n_e2e
         t_e2e = max_over_ranks(t_e2e, ws, dev)
         e2e = {"value": whole_job_value(fl["total"], ws, t_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3}
+               "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
+               "api": f"swa_step_host, {chunks} head groups" if chunks else "copies + swa_forward / swa_backward"}
+        if chunks:
+            swa.check_step_host(g, chunks, step_buf, stream)
 
     if rank != 0:
         barrier(ws)

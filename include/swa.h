@@ -198,9 +198,36 @@ SWA_API swa_status_t swa_backward_noalloc(const swa_params_t *p, const void *q, 
                                           const float *softmax_sum, const uint8_t *drop_mask, void *dq, void *dk,
                                           void *dv, swa_stream_t stream);
 
-/* Wait for `stream`, then report whether any kernel of the last call that
- * used `workspace` gave up a bounded wait: SWA_OK or SWA_ERR_TIMEOUT
- * (SWA_ERR_CUDA if the stream itself failed). */
+/* Forward + backward of one problem whose tensors live in HOST memory (an
+ * addition of this library; the pages' operators take device tensors).  The
+ * heads are split into `chunks` equal groups; each group is copied to its own
+ * compact device tensors inside `device_buffer`, computed (swa_forward, then
+ * swa_backward, on `stream`) and copied back, and the copies of the next and
+ * the previous group run on two internal streams while a group computes.
+ * Heads are independent, so the results equal those of one swa_forward +
+ * swa_backward on device copies of the same tensors, bit for bit.
+ *   q, k, v, dy   host, p->dtype, shapes and layout as for swa_forward /
+ *                 swa_backward; page-locked memory lets the copies overlap
+ *   out, softmax_max, softmax_sum, dq, dk, dv
+ *                 host, written when `stream` completes
+ *   chunks        >= 1, dividing N and N_kv.  Dropout needs dropout_gen = 1
+ *                 and chunks = 1: there is no drop_mask argument, and the
+ *                 generated keep bits are indexed by the whole problem's heads
+ *   device_buffer device, >= swa_step_host_buffer_size bytes, 256-byte aligned
+ * All work is enqueued behind the work already on `stream`, and `stream`
+ * completes only once every result is in host memory.  Errors: those of
+ * swa_forward / swa_backward, SWA_ERR_PARAM_INVALID (chunks), and
+ * SWA_ERR_CUDA; on an error part of the work may already be enqueued. */
+SWA_API swa_status_t swa_step_host_buffer_size(const swa_params_t *p, int chunks, size_t *bytes);
+SWA_API swa_status_t swa_step_host(const swa_params_t *p, int chunks, const void *q, const void *k,
+                                   const void *v, const void *dy, void *out, float *softmax_max,
+                                   float *softmax_sum, void *dq, void *dk, void *dv, void *device_buffer,
+                                   size_t device_bytes, swa_stream_t stream);
+/* swa_workspace_status over every chunk's forward and backward workspace
+ * inside a swa_step_host device_buffer. */
+SWA_API swa_status_t swa_step_host_status(const swa_params_t *p, int chunks, const void *device_buffer,
+                                          swa_stream_t stream);
+
 /* Write the keep mask that p->dropout_seed / p->dropout_offset stand for
  * (see "Dropout" above) in the drop_mask layout: ceil(bits / 8) bytes, bits =
  * sum over sequences of N * Sq_b * Skv_b.  mask is device memory of
@@ -212,6 +239,9 @@ SWA_API swa_status_t swa_backward_noalloc(const swa_params_t *p, const void *q, 
 SWA_API swa_status_t swa_dropout_mask(const swa_params_t *p, uint8_t *mask, size_t mask_bytes,
                                       swa_stream_t stream);
 
+/* Wait for `stream`, then report whether any kernel of the last call that
+ * used `workspace` gave up a bounded wait: SWA_OK or SWA_ERR_TIMEOUT
+ * (SWA_ERR_CUDA if the stream itself failed). */
 SWA_API swa_status_t swa_workspace_status(const void *workspace, swa_stream_t stream);
 
 /* Measurement support.  `events` is NULL (stop recording) or an array of six

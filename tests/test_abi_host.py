@@ -193,3 +193,24 @@ def test_fp32_workspace_holds_bf16_copies(lib):
     assert b == 256 + stats + 3 * r256(2 * qe) + 2 * r256(2 * kve)
     g16 = Geometry(**{**g.as_dict(), "dtype": "bf16"})
     assert _size(g16)[1] == 256 and _size(g16, backward=True)[1] == 256 + stats
+
+
+def test_step_host_buffer_sizes(lib):
+    """swa_step_host's device buffer: per head group, compact copies of q, k,
+    v, dy, out, dq, dk, dv and the statistics plus that group's workspaces;
+    the chunk count must divide N and N_kv, and dropout needs one chunk."""
+    g = Geometry("BNSD", 2, 8, 64, S_q=256, S_kv=256, N_kv=4, sparse_mode=0)
+    p = swa.Params(g)
+    r256 = lambda x: (x + 255) // 256 * 256
+    for chunks in (1, 2, 4):
+        qb, kb = 2 * (8 // chunks) * 256 * 64 * 2, 2 * (4 // chunks) * 256 * 64 * 2
+        sb = 2 * (8 // chunks) * 256 * 4
+        sub = Geometry(**{**g.as_dict(), "N": 8 // chunks, "N_kv": 4 // chunks})
+        fws, bws = _size(sub)[1], _size(sub, backward=True)[1]
+        per = 4 * r256(qb) + 4 * r256(kb) + 2 * r256(sb) + r256(fws) + r256(bws)
+        assert swa.swa_step_host_buffer_size(p, chunks) == chunks * per
+    n = ctypes.c_size_t(0)
+    assert swa.lib().swa_step_host_buffer_size(p.ref(), 3, ctypes.byref(n)) == swa.SWA_ERR_PARAM_INVALID
+    assert swa.lib().swa_step_host_buffer_size(p.ref(), 0, ctypes.byref(n)) == swa.SWA_ERR_PARAM_INVALID
+    d = swa.Params(Geometry(**{**g.as_dict(), "keep_prob": 0.9}))  # a packed mask cannot be passed
+    assert swa.lib().swa_step_host_buffer_size(d.ref(), 1, ctypes.byref(n)) == swa.SWA_ERR_PARAM_INVALID
