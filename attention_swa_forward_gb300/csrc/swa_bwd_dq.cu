@@ -377,13 +377,9 @@ template <int D, int DM, bool F16, int CAP>
 cudaError_t launch_dq_t(const BwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdy, cudaStream_t stream) {
   const size_t smem = sizeof(DqSmem<D>) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(swa_bwd_dq_kernel<D, DM, F16, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  const cudaError_t e = set_smem_limit(swa_bwd_dq_kernel<D, DM, F16, CAP>, smem, smem_set);
+  if (e != cudaSuccess) return e;
   swa_bwd_dq_kernel<D, DM, F16, CAP><<<tab.n_items, kThreads, smem, stream>>>(a, tab, mq, mk, mv, mdy);
   return cudaGetLastError();
 }

@@ -222,10 +222,12 @@ __global__ void __launch_bounds__(224, 1)
       auto X = [&](int t) -> float { return __uint_as_float(xr[t]); };
 
       const int j0 = (kv_t0 + it) * kTileN;
-      // Fast path (tiles inside the window, positive scale): the maximum is
-      // taken on the raw scores and the scale folds into one packed FMA per
-      // pair, p = exp2(x*c - m).  Otherwise scale, mask, then exp2(x - m).
-      const bool fast = tile_fully_visible(g, sq, q0, j0) && c > 0.f;
+      // With a positive scale the maximum is taken on the raw scores and the
+      // scale folds into one packed FMA per pair, p = exp2(x*c - m); keys
+      // outside the window (partial tiles only) become -inf first, and
+      // exp2(-inf*c - m) = 0.  A scale <= 0 takes scale, mask, exp2(x - m).
+      const bool fold = c > 0.f;
+      const bool fast = fold && tile_fully_visible(g, sq, q0, j0);
       float mx;
       {
         float m8[8];  // eight independent partial maxima: no long dependency chain
@@ -238,13 +240,14 @@ __global__ void __launch_bounds__(224, 1)
           const int lo_t = wlo - j0, hi_t = whi - j0;  // visible t in [lo_t, hi_t]
 #pragma unroll
           for (int t = 0; t < kTileN; ++t) {
-            const float v = ((t >= lo_t) & (t <= hi_t)) ? X(t) * c : -INFINITY;  // selects, not branches
+            const bool vis = (t >= lo_t) & (t <= hi_t);
+            const float v = vis ? (fold ? X(t) : X(t) * c) : -INFINITY;  // selects, not branches
             xr[t] = __float_as_uint(v);
             m8[t & 7] = fmaxf(m8[t & 7], v);
           }
         }
         mx = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], fmax3(m8[5], m8[6], m8[7])));
-        if (fast) mx *= c;
+        if (fold) mx *= c;
       }
       const float m_new = fmaxf(m_true, mx);
       m_true = m_new;
@@ -271,7 +274,7 @@ __global__ void __launch_bounds__(224, 1)
 #pragma unroll
       for (int t = 0; t < kTileN; t += 2) {
         float p0, p1;
-        if (fast) {
+        if (fold) {
           ffma2_bcast(p0, p1, X(t), X(t + 1), c, -msub);
         } else {
           p0 = X(t) - msub;
@@ -334,20 +337,24 @@ __global__ void __launch_bounds__(224, 1)
       // epilogue: O = acc / (l * keep), statistics before dropout
       const float inv = (l > 0.f) ? g.inv_keep / l : 0.f;
       const int64_t orow = q_elem(g, sq, w.b, w.n, i);
+      uint32_t acc[D / 32][32];  // the row of O (fp32 bits); zero when no key is visible
+      if (n_kv > 0) {
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) tmem_ld_32x32b_x32(tmem + lane_off + kColO + ch * 32, acc[ch]);
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) tmem_ld_wait(acc[ch]);  // one wait for all the loads
+      } else {
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch)
+#pragma unroll
+          for (int t = 0; t < 32; ++t) acc[ch][t] = 0u;
+      }
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
         if (ch * 32 >= g.D) break;  // columns past D are padding
         float o[32];
-        if (n_kv > 0) {
-          uint32_t t32[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + kColO + ch * 32, t32);
-          tmem_ld_wait(t32);
 #pragma unroll
-          for (int t = 0; t < 32; ++t) o[t] = __uint_as_float(t32[t]) * inv;
-        } else {
-#pragma unroll
-          for (int t = 0; t < 32; ++t) o[t] = 0.f;
-        }
+        for (int t = 0; t < 32; ++t) o[t] = __uint_as_float(acc[ch][t]) * inv;
         if (row_valid) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
@@ -374,13 +381,9 @@ template <int D, int DM, bool F16, int CAP>
 cudaError_t launch_fwd_t(const FwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, cudaStream_t stream) {
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(swa_fwd_kernel<D, DM, F16, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  const cudaError_t e = set_smem_limit(swa_fwd_kernel<D, DM, F16, CAP>, smem, smem_set);
+  if (e != cudaSuccess) return e;
   swa_fwd_kernel<D, DM, F16, CAP><<<tab.n_items, 224, smem, stream>>>(a, tab, mq, mk, mv);
   return cudaGetLastError();
 }

@@ -1,5 +1,6 @@
 // swa_internal.h — shapes shared by the host scheduler and the kernels.
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -57,6 +58,22 @@ struct WsHeader {
   int32_t pad[63];
 };
 constexpr size_t kHeaderBytes = 256;
+
+// Raise a kernel's dynamic shared memory limit to `smem` bytes on the current
+// device.  The setting belongs to the device's context, so it is made once
+// per device (devices past 63 make it on every call); `done` is the kernel's
+// own bit set, safe to share between host threads.
+template <typename Kernel>
+cudaError_t set_smem_limit(Kernel kernel, size_t smem, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Error codes a kernel stores into WsHeader::error.
 enum : int32_t {
