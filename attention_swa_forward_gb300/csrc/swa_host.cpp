@@ -185,9 +185,17 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
     if ((e = copy_out(L.kv, c, dk, d + L.dk_off, s_out)) != cudaSuccess) break;
     if ((e = copy_out(L.kv, c, dv, d + L.dv_off, s_out)) != cudaSuccess) break;
   }
-  // the caller's stream completes only after the last result has reached the host
-  if (e == cudaSuccess) e = cudaEventRecord(done, s_out);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, done, 0);
+  // The caller's stream completes only after the last result has reached the
+  // host, and, after a failure part-way, only after every copy already
+  // enqueued on either copy stream has run: host memory is never written
+  // once the caller has seen the stream finish.
+  cudaEvent_t in_end = nullptr;
+  cudaError_t e_end = event(&in_end);
+  if (e_end == cudaSuccess) e_end = cudaEventRecord(in_end, s_in);
+  if (e_end == cudaSuccess) e_end = cudaStreamWaitEvent(cs, in_end, 0);
+  if (e_end == cudaSuccess) e_end = cudaEventRecord(done, s_out);
+  if (e_end == cudaSuccess) e_end = cudaStreamWaitEvent(cs, done, 0);
+  if (e == cudaSuccess) e = e_end;
   release();
   if (st != SWA_OK) return st;
   if (e != cudaSuccess) return cuda_fail(e, "host step copies");

@@ -217,7 +217,9 @@ SWA_API swa_status_t swa_backward_noalloc(const swa_params_t *p, const void *q, 
  * All work is enqueued behind the work already on `stream`, and `stream`
  * completes only once every result is in host memory.  Errors: those of
  * swa_forward / swa_backward, SWA_ERR_PARAM_INVALID (chunks), and
- * SWA_ERR_CUDA; on an error part of the work may already be enqueued. */
+ * SWA_ERR_CUDA.  On an error part of the work may already be enqueued;
+ * `stream` then still completes only after every copy enqueued by the call
+ * has run, so the host buffers may be released once it has. */
 SWA_API swa_status_t swa_step_host_buffer_size(const swa_params_t *p, int chunks, size_t *bytes);
 SWA_API swa_status_t swa_step_host(const swa_params_t *p, int chunks, const void *q, const void *k,
                                    const void *v, const void *dy, void *out, float *softmax_max,
