@@ -91,6 +91,9 @@ FD_CASES = {
                        scale=0.75, sparse_mode=0),
     "tnd_band_dropout": dict(layout="TND", B=2, N=1, D=4, cu_seqlens_q=[4, 9], cu_seqlens_kv=[4, 9], scale=0.9,
                              sparse_mode=4, pre_tokens=1, next_tokens=1, keep_prob=0.6),
+    # the pages put no sign on scale: a negative one reverses the score order
+    "bnsd_band_negative_scale": dict(layout="BNSD", B=1, N=2, D=4, S_q=7, S_kv=7, scale=-0.8, sparse_mode=4,
+                                     pre_tokens=3, next_tokens=1),
 }
 
 
@@ -146,6 +149,9 @@ SDPA_CASES = {
                      next_tokens=5),
     "rect": dict(layout="BNSD", B=1, N=2, D=8, S_q=20, S_kv=37, scale=0.3, sparse_mode=4, pre_tokens=4,
                  next_tokens=12),
+    "band_negative_scale": dict(layout="BNSD", B=1, N=2, D=8, S_q=40, S_kv=40, scale=-0.3, sparse_mode=4,
+                                pre_tokens=11, next_tokens=0),
+    "nomask_zero_scale": dict(layout="BNSD", B=1, N=2, D=8, S_q=21, S_kv=21, scale=0.0, sparse_mode=0),
 }
 
 

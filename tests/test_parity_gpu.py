@@ -115,6 +115,10 @@ SMALL = {
                            pre_tokens=2147483647, next_tokens=2147483647),
     "bnsd_zero_band": dict(layout="BNSD", B=1, N=2, D=64, S_q=200, S_kv=200, scale=0.125, sparse_mode=4,
                            pre_tokens=0, next_tokens=0),
+    # a scale <= 0 takes the forward's scale-then-mask path on every tile (full ones included)
+    "bnsd_band_negative_scale": dict(layout="BNSD", B=1, N=2, D=64, S_q=520, S_kv=520, scale=-0.125,
+                                     sparse_mode=4, pre_tokens=300, next_tokens=0),
+    "bnsd_nomask_zero_scale": dict(layout="BNSD", B=1, N=2, D=128, S_q=260, S_kv=260, scale=0.0, sparse_mode=0),
     "tnd_varlen_nomask": dict(layout="TND", B=5, N=2, D=128, cu_seqlens_q=[130, 130, 387, 388, 452],
                               cu_seqlens_kv=[130, 130, 387, 388, 452], scale=0.09, sparse_mode=0),
     "tnd_varlen_band_dropout_d64": dict(layout="TND", B=4, N=3, D=64, cu_seqlens_q=[200, 201, 460, 0],
