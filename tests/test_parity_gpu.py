@@ -98,6 +98,10 @@ def check_grads(res, dq, dk, dv, label=""):
 
 
 # ----------------------------------------------------------- small cases --
+# 600 short sequences: more work entries than one launch's table holds (512),
+# so every pass runs as two launches
+_CU600 = np.cumsum(np.random.default_rng(600).integers(1, 41, 600)).tolist()
+
 SMALL = {
     "bnsd_nomask_d64_ragged": dict(layout="BNSD", B=2, N=2, D=64, S_q=300, S_kv=300, scale=0.125, sparse_mode=0),
     "bnsd_band_d128_ragged": dict(layout="BNSD", B=1, N=3, D=128, S_q=517, S_kv=517, scale=128 ** -0.5,
@@ -119,6 +123,8 @@ SMALL = {
     "bnsd_band_negative_scale": dict(layout="BNSD", B=1, N=2, D=64, S_q=520, S_kv=520, scale=-0.125,
                                      sparse_mode=4, pre_tokens=300, next_tokens=0),
     "bnsd_nomask_zero_scale": dict(layout="BNSD", B=1, N=2, D=128, S_q=260, S_kv=260, scale=0.0, sparse_mode=0),
+    "tnd_600_sequences_band": dict(layout="TND", B=600, N=2, D=64, cu_seqlens_q=_CU600, cu_seqlens_kv=_CU600,
+                                   scale=0.125, sparse_mode=4, pre_tokens=7, next_tokens=3),
     "tnd_varlen_nomask": dict(layout="TND", B=5, N=2, D=128, cu_seqlens_q=[130, 130, 387, 388, 452],
                               cu_seqlens_kv=[130, 130, 387, 388, 452], scale=0.09, sparse_mode=0),
     "tnd_varlen_band_dropout_d64": dict(layout="TND", B=4, N=3, D=64, cu_seqlens_q=[200, 201, 460, 0],
