@@ -169,3 +169,47 @@ def draw(geom: Geometry, seed: int, lengths: tuple | None = None, with_dy: bool 
 def draw_workload(name: str) -> Inputs:
     w = WORKLOADS[name]
     return draw(w.geom, w.seed, w.lengths)
+
+
+def _local_positions(geom: Geometry, q_side: bool) -> torch.Tensor:
+    """Index of every row inside its own sequence, shaped to broadcast over
+    the q-side ([B,N,S_q,1] / [T_q,1,1]) or k-side layout."""
+    if geom.layout == "BNSD":
+        S = geom.S_q if q_side else geom.S_kv
+        return torch.arange(S, dtype=torch.float32).view(1, 1, S, 1)
+    pos = []
+    for lq, lk in geom.seq_lens():
+        pos.append(torch.arange(lq if q_side else lk, dtype=torch.float32))
+    return torch.cat(pos).view(-1, 1, 1)
+
+
+def edge_probe_inputs(geom: Geometry, k_rand: torch.Tensor, dy_rand: torch.Tensor, alpha: float):
+    """q, k, v, dy (bf16, D >= 8) that put each query row's probability at one
+    edge of its visible window, with exact scores.
+
+    With i, j the positions inside the sequence:
+        q_i  = alpha * (1, 256, -(i mod 256), -256 * (i div 256), 0, ...)
+        k_j  = (j mod 256, j div 256, 1, 1, r_j)
+        v_j  = (j mod 256, j div 256, 1, 1, 0, ...)
+        dy_i = (1, 256, -(i mod 256), -256 * (i div 256), u_i)
+    where r_j and u_i are the last D - 4 columns of k_rand and dy_rand.  Every
+    entry is an integer below 2^15 (exact in bf16), so q_i.k_j = alpha*(j - i)
+    and dy_i.v_j = j - i exactly in fp32.  With scale 1 the probability of
+    key j in row i falls by e^|alpha| per key away from the leftmost visible
+    key (alpha < 0) or the rightmost (alpha > 0)."""
+    assert geom.D >= 8 and geom.dtype == "bf16"
+    i = _local_positions(geom, True)
+    j = _local_positions(geom, False)
+    q = torch.zeros(geom.q_shape(), dtype=torch.float32)
+    qi = torch.cat([torch.ones_like(i), 256.0 * torch.ones_like(i), -torch.remainder(i, 256.0),
+                    -256.0 * torch.div(i, 256.0, rounding_mode="floor")], dim=-1)
+    q[..., :4] = alpha * qi
+    k = k_rand.float().clone()
+    k[..., 0:1] = torch.remainder(j, 256.0)
+    k[..., 1:2] = torch.div(j, 256.0, rounding_mode="floor")
+    k[..., 2:4] = 1.0
+    v = torch.zeros(geom.kv_shape(), dtype=torch.float32)
+    v[..., :4] = k[..., :4]
+    dy = dy_rand.float().clone()
+    dy[..., :4] = qi
+    return tuple(t.to(torch.bfloat16) for t in (q, k, v, dy))

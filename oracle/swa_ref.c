@@ -273,9 +273,10 @@ static void dkv_col(const orc_params *p, const orc_seq *s, int64_t b, int64_t h,
  * t*N+n for TND) to (b, n, local i).  Returns 0 if the row belongs to no
  * sequence. */
 static int locate_q(const orc_params *p, int64_t id, int64_t *b, int64_t *n, int64_t *i) {
+  if (id < 0) return 0;
   if (p->layout == 0) {
     *i = id % p->S_q; *n = (id / p->S_q) % p->N; *b = id / (p->S_q * p->N);
-    return 1;
+    return *b < p->B;
   }
   int64_t t = id / p->N;
   *n = id % p->N;
@@ -289,9 +290,10 @@ static int locate_q(const orc_params *p, int64_t id, int64_t *b, int64_t *n, int
 /* Map a flat key-row id ((b*N_kv+h)*S_kv+j for BNSD, t*N_kv+h for TND) to
  * (b, key/value head h, local j). */
 static int locate_kv(const orc_params *p, int64_t id, int64_t *b, int64_t *n, int64_t *j) {
+  if (id < 0) return 0;
   if (p->layout == 0) {
     *j = id % p->S_kv; *n = (id / p->S_kv) % p->N_kv; *b = id / (p->S_kv * p->N_kv);
-    return 1;
+    return *b < p->B;
   }
   int64_t t = id / p->N_kv;
   *n = id % p->N_kv;

@@ -28,3 +28,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    # the max-abs error every parity check reached, per case and tensor;
+    # also written to the file SWA_PARITY_REPORT names, when set
+    from tests import helpers
+
+    if not helpers.REPORT:
+        return
+    lines = helpers.format_report()
+    for line in lines:
+        terminalreporter.write_line(line)
+    path = os.environ.get("SWA_PARITY_REPORT")
+    if path:
+        with open(path, "w") as f:
+            f.write("\n".join(lines) + "\n")

@@ -19,11 +19,10 @@ from attention_swa_forward_gb300 import build as B
 from attention_swa_forward_gb300 import swa
 from attention_swa_forward_gb300.workloads import Geometry, draw
 from oracle import swa_oracle as orc
-from tests.helpers import rel_l2, to_problem
+from tests.helpers import TOL_GRAD, TOL_OUT, check_stat, check_tensor, out_dtype, to_problem
 
 pytestmark = pytest.mark.gpu
 
-TOL_OUT, TOL_GRAD, TOL_ABS, TOL_REL_ELEM, TOL_STAT = 5e-3, 1e-2, 2e-2, 1e-2, 1e-3
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -31,10 +30,6 @@ def built():
     B.build()
     orc.build()
     swa.lib()
-
-
-def _excess(got, ref):
-    return float(np.max(np.abs(got - ref) - (TOL_ABS + TOL_REL_ELEM * np.abs(ref)))) if got.size else 0.0
 
 
 MASKS = {
@@ -103,13 +98,13 @@ def test_generated_dropout_parity(name):
     out, smax, ssum = orc.forward(pr, inp.q, inp.k, inp.v, mask)
     dq, dk, dv = orc.backward(pr, inp.q, inp.k, inp.v, inp.dy, mask)
     res = _gpu(geom, inp)
-    assert rel_l2(res["out"], out) <= TOL_OUT and _excess(res["out"], out) <= 0.0
-    for stat, ref in (("smax", smax), ("ssum", ssum)):
-        fin = np.isfinite(ref)
-        assert np.array_equal(np.isfinite(res[stat]), fin)
-        assert np.max(np.abs(res[stat][fin] - ref[fin]) / np.maximum(np.abs(ref[fin]), 1.0)) <= TOL_STAT
+    dt = out_dtype(geom)
+    label = f"generated dropout {name}"
+    check_tensor(label, "out", res["out"], out, dt, TOL_OUT)
+    check_stat(label, "softmax_max", res["smax"], smax)
+    check_stat(label, "softmax_sum", res["ssum"], ssum)
     for n, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
-        assert rel_l2(res[n], ref) <= TOL_GRAD and _excess(res[n], ref) <= 0.0, n
+        check_tensor(label, n, res[n], ref, dt, TOL_GRAD)
     # the materialised mask through the drop_mask path gives the same bits out
     gm = swa.dropout_mask(geom)
     geom_mask = Geometry(**{**CASES[name], "dropout_gen": 0})

@@ -9,7 +9,11 @@
   no dropout, TND sequence == BNSD with B = 1, Skv = 1 -> out = v,
   pre = next = 0 -> out_i = v_i, empty rows, dropout bit order checked with
   numpy.unpackbits;
-- the sampled-row / sampled-column entry points equal the full ones.
+- the sampled-row / sampled-column entry points equal the full ones;
+- key_ranges (the visible window of each row) equals the dense BAND mask on
+  every row, empty rows included;
+- the edge probe the GPU masked-set tests use moves dV and dQ far past the
+  element gate on every row and key that a window error of one pair touches.
 """
 import json
 import math
@@ -21,7 +25,8 @@ import torch
 
 from attention_swa_forward_gb300.workloads import Geometry, draw
 from oracle import swa_oracle as orc
-from tests.helpers import to_problem
+from attention_swa_forward_gb300.workloads import edge_probe_inputs
+from tests.helpers import TOL_ABS, half_ulp, to_problem
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -354,10 +359,6 @@ def test_sampled_entry_points_match_full(layout):
     assert np.allclose(dq_s, flat_q(dq)[rows], rtol=1e-13, atol=1e-15)
     assert np.allclose(dk_s, flat_q(dk)[cols], rtol=1e-13, atol=1e-15)
     assert np.allclose(dv_s, flat_q(dv)[cols], rtol=1e-13, atol=1e-15)
-    lo, hi = orc.key_ranges(pr, rows)
-    for t, r in enumerate(rows):
-        # the visible range reproduces softmax_sum with zero scores
-        assert hi[t] >= lo[t]
 
 
 def test_visible_pair_count_matches_dense_mask():
@@ -528,3 +529,150 @@ def test_generated_mask_seed_offset_and_bounds():
     assert _mask_bits(orc.generate_keep_mask(one, 5, 0), geom.mask_bits()).all()
     zero = to_problem(Geometry(**{**geom.as_dict(), "keep_prob": 1e-4}))
     assert not _mask_bits(orc.generate_keep_mask(zero, 5, 0), geom.mask_bits()).any()
+
+
+# ------------------------------------------- visible windows (key_ranges) --
+KEY_RANGE_CASES = {
+    **SDPA_CASES,
+    "band_negative_pre": dict(layout="BNSD", B=1, N=2, D=8, S_q=60, S_kv=60, scale=0.3, sparse_mode=4,
+                              pre_tokens=-5, next_tokens=9),
+    "band_negative_next": dict(layout="BNSD", B=2, N=1, D=8, S_q=50, S_kv=50, scale=0.3, sparse_mode=4,
+                               pre_tokens=12, next_tokens=-4),
+    "rect_wide_kv": dict(layout="BNSD", B=1, N=1, D=8, S_q=17, S_kv=90, scale=0.3, sparse_mode=4, pre_tokens=3,
+                         next_tokens=40),
+    "tnd_band_skipped": dict(layout="TND", B=5, N=3, D=8, cu_seqlens_q=[20, 20, 61, 0, 0],
+                             cu_seqlens_kv=[31, 40, 70, 0, 0], scale=0.3, sparse_mode=4, pre_tokens=6,
+                             next_tokens=2),
+    "tnd_nomask": dict(layout="TND", B=3, N=2, D=8, cu_seqlens_q=[9, 30, 44], cu_seqlens_kv=[12, 12, 40],
+                       scale=0.3, sparse_mode=0),
+}
+
+
+def _windows_dense(geom):
+    """(lo, hi) of every statistics row from the dense BAND mask, -1 / -2 for
+    a row that sees no key; rows in statistics order ([B,N,S] / [T,N])."""
+    pr = to_problem(geom)
+    out = []
+    for b, (lq, lk) in enumerate(geom.seq_lens()):
+        if lq == 0:
+            continue
+        if lk == 0:  # a sequence without keys: every row is empty
+            out.append((np.full(lq, -1), np.full(lq, -2)))
+            continue
+        m = _dense_mask(pr, lq, lk)
+        lo = np.where(m.any(1), m.argmax(1), -1)
+        hi = np.where(m.any(1), lk - 1 - m[:, ::-1].argmax(1), -2)
+        out.append((lo, hi))
+    rows_lo, rows_hi = [], []
+    if geom.layout == "BNSD":
+        for lo, hi in out:
+            for _ in range(geom.N):
+                rows_lo.append(lo)
+                rows_hi.append(hi)
+        return np.concatenate(rows_lo), np.concatenate(rows_hi)
+    for lo, hi in out:  # [T, N]: every head of a token in turn
+        rows_lo.append(np.repeat(lo, geom.N))
+        rows_hi.append(np.repeat(hi, geom.N))
+    return np.concatenate(rows_lo), np.concatenate(rows_hi)
+
+
+@pytest.mark.parametrize("name", sorted(KEY_RANGE_CASES))
+def test_key_ranges_equal_dense_mask(name):
+    geom = Geometry(**KEY_RANGE_CASES[name])
+    pr = to_problem(geom)
+    rows = np.arange(int(np.prod(geom.stat_shape())))
+    lo, hi = orc.key_ranges(pr, rows)
+    dlo, dhi = _windows_dense(geom)
+    empty = dlo < 0
+    assert np.array_equal(lo > hi, empty)
+    # an empty row is reported as lo = 0, hi = -1
+    assert np.all(lo[empty] == 0) and np.all(hi[empty] == -1)
+    assert np.array_equal(lo[~empty], dlo[~empty]) and np.array_equal(hi[~empty], dhi[~empty])
+    # rows past the table (beyond the last statistics row) see nothing
+    lo2, hi2 = orc.key_ranges(pr, np.array([rows.size, rows.size + 7]))
+    assert np.all(lo2 > hi2)
+
+
+# -------------------------------- edge probe: one-pair window errors show --
+EDGE_CASES = {
+    "band": dict(layout="BNSD", B=1, N=2, D=64, S_q=400, S_kv=400, sparse_mode=4, pre_tokens=120, next_tokens=5),
+    "band_negative_pre": dict(layout="BNSD", B=1, N=1, D=64, S_q=300, S_kv=300, sparse_mode=4, pre_tokens=-40,
+                              next_tokens=90),
+    "rect_band": dict(layout="BNSD", B=2, N=1, D=64, S_q=150, S_kv=400, sparse_mode=4, pre_tokens=10,
+                      next_tokens=200),
+    "tnd_band": dict(layout="TND", B=3, N=2, D=64, cu_seqlens_q=[150, 150, 420], cu_seqlens_kv=[130, 140, 500],
+                     sparse_mode=4, pre_tokens=60, next_tokens=90),
+    "gqa_band": dict(layout="BNSD", B=1, N=4, N_kv=2, D=64, S_q=300, S_kv=300, sparse_mode=4, pre_tokens=100,
+                     next_tokens=30),
+}
+
+
+def _key_flat_ids(geom, b, j):
+    """Flat key-row ids (rows of dk / dv reshaped to [-1, D]) of local key j of
+    sequence b, one per key/value head."""
+    nkv = geom.n_kv
+    if geom.layout == "BNSD":
+        return [(b * nkv + h) * geom.S_kv + j for h in range(nkv)]
+    start = sum(lk for _, lk in geom.seq_lens()[:b])
+    return [(start + j) * nkv + h for h in range(nkv)]
+
+
+def _changed(geom, pr_a, pr_b):
+    """Rows (statistics ids) whose window under pr_b differs from the true
+    one under pr_a, and the flat key ids whose set of seeing rows differs.
+
+    Only rows that see a key under pr_a count: a row the forward found empty
+    has P = 0 in both backward passes whatever window they use, so an error
+    there changes nothing.  A row left with no key by pr_b after one key
+    under pr_a counts for its key (dV loses P * dY) but not for dQ: the
+    dS of a lone pair is P * (dP - P dP) = 0."""
+    rows = np.arange(int(np.prod(geom.stat_shape())))
+    la, ha = orc.key_ranges(pr_a, rows)
+    lb, hb = orc.key_ranges(pr_b, rows)
+    ea, eb = la > ha, lb > hb
+    diff = ~ea & ~((la == lb) & (ha == hb) & ~eb)
+    lone_lost = diff & eb & (ha == la)
+    keys = set()
+    seq_of_row, local = [], []
+    for b, (lq, _) in enumerate(geom.seq_lens()):
+        seq_of_row += [b] * lq
+        local += list(range(lq))
+    for r in np.nonzero(diff)[0]:
+        if geom.layout == "BNSD":
+            b = r // (geom.N * geom.S_q)
+        else:
+            b = seq_of_row[r // geom.N]
+        sa = set() if ea[r] else set(range(la[r], ha[r] + 1))
+        sb = set() if eb[r] else set(range(lb[r], hb[r] + 1))
+        for j in sa ^ sb:
+            keys.update(_key_flat_ids(geom, b, j))
+    return np.nonzero(diff & ~lone_lost)[0], np.array(sorted(keys), dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", sorted(EDGE_CASES))
+def test_edge_probe_exposes_one_pair_window_errors(name):
+    """A backward pass whose window has one pair too many or too few at an
+    edge (it recomputes P from the forward's statistics over the wrong set)
+    moves dQ (query-major pass) on every row it touches and dV (key-major
+    pass) on every key it touches by more than three times the element gate
+    (2e-2 + half a bf16 ulp) of the GPU parity tests: the edge probe makes
+    the GPU masked-set tests exact up to one pair."""
+    geom = Geometry(**{**EDGE_CASES[name], "scale": 1.0})
+    inp = draw(geom, 13)
+    for alpha, edge in ((-2.0, "pre_tokens"), (2.0, "next_tokens")):
+        q, k, v, dy = edge_probe_inputs(geom, inp.k, inp.dy, alpha)
+        pr = to_problem(geom)
+        out, m, l = orc.forward(pr, q, k, v)
+        dq_t, _, dv_t = orc.backward(pr, q, k, v, dy, None, out, m, l)
+        D = geom.D
+        for delta in (+1, -1):
+            bad = to_problem(Geometry(**{**geom.as_dict(), edge: getattr(geom, edge) + delta}))
+            dq_b, _, dv_b = orc.backward(bad, q, k, v, dy, None, out, m, l)
+            rows, keys = _changed(geom, pr, bad)
+            assert rows.size > 0 and keys.size > 0, (name, edge, delta)
+            rq_t, rq_b = dq_t.reshape(-1, D)[rows, 4:], dq_b.reshape(-1, D)[rows, 4:]
+            gate = TOL_ABS + half_ulp(rq_t, "bf16")
+            assert np.all(np.max(np.abs(rq_b - rq_t) - 3 * gate, axis=1) > 0), (name, edge, delta, "dq")
+            kv_t, kv_b = dv_t.reshape(-1, D)[keys, 4:], dv_b.reshape(-1, D)[keys, 4:]
+            gate = TOL_ABS + half_ulp(kv_t, "bf16")
+            assert np.all(np.max(np.abs(kv_b - kv_t) - 3 * gate, axis=1) > 0), (name, edge, delta, "dv")
