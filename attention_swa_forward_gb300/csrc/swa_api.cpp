@@ -9,6 +9,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -19,12 +20,14 @@
 #include <vector>
 
 #include "swa_internal.h"
+#include "swa_sched.h"
 
 using namespace swa;
 
 namespace {
 
 thread_local std::string t_last_error = "no error";
+std::atomic<int32_t> g_stall{0};  // swa_debug_stall: read into Geometry::stall by every call
 thread_local cudaEvent_t t_ev[6] = {};  // start/stop around: forward, dK/dV pass, dQ pass
 
 swa_status_t fail(swa_status_t st, const char* fmt, ...) {
@@ -139,6 +142,7 @@ swa_status_t make_plan(const swa_params_t* p, Plan& plan) {
   g.seed_hi = static_cast<uint32_t>(p->dropout_seed >> 32);
   g.off_lo = static_cast<uint32_t>(p->dropout_offset);
   g.keep_thr = static_cast<uint32_t>(std::min(256L, std::max(0L, std::lround(p->keep_prob * 256.0))));
+  g.stall = g_stall.load(std::memory_order_relaxed);
 
   int64_t max_len = 0;
   if (p->layout == SWA_LAYOUT_BNSD) {
@@ -187,25 +191,26 @@ swa_status_t make_plan(const swa_params_t* p, Plan& plan) {
 }
 
 // ------------------------------------------------------------ scheduler --
-// Number of key tiles a query tile visits (forward) or query tiles a key tile
-// visits (backward), by the BAND inequality i - pre <= j <= i + next.
+SeqInfo info_of(const Seq& s) {
+  SeqInfo x{};
+  x.q_start = static_cast<int32_t>(s.q_start);
+  x.q_len = static_cast<int32_t>(s.q_len);
+  x.kv_start = static_cast<int32_t>(s.kv_start);
+  x.kv_len = static_cast<int32_t>(s.kv_len);
+  x.mask_base = s.mask_base;
+  return x;
+}
+// Number of key tiles a query tile visits (forward, query-major pass) or
+// query tiles a key tile visits (key-major pass): the kernels' own ranges.
 int64_t fwd_tile_cost(const Geometry& g, const Seq& s, int64_t t) {
-  const int64_t q0 = t * kTileM, q_last = std::min(q0 + kTileM - 1, s.q_len - 1);
-  int64_t lo = 0, hi = s.kv_len - 1;
-  if (g.sparse_mode == 4) {
-    lo = std::max<int64_t>(lo, q0 - g.pre);
-    hi = std::min<int64_t>(hi, q_last + g.next);
-  }
-  return lo <= hi ? hi / kTileN - lo / kTileN + 1 : 0;
+  int t0, n;
+  key_tiles_of_query_tile(g, info_of(s), static_cast<int>(t), &t0, &n);
+  return n;
 }
 int64_t bwd_tile_cost(const Geometry& g, const Seq& s, int64_t t) {
-  const int64_t j0 = t * kTileN, j_last = std::min(j0 + kTileN - 1, s.kv_len - 1);
-  int64_t lo = 0, hi = s.q_len - 1;
-  if (g.sparse_mode == 4) {
-    lo = std::max<int64_t>(lo, j0 - g.next);
-    hi = std::min<int64_t>(hi, j_last + g.pre);
-  }
-  return lo <= hi ? hi / kTileM - lo / kTileM + 1 : 0;
+  int t0, n;
+  query_tiles_of_key_tile(g, info_of(s), static_cast<int>(t), &t0, &n);
+  return n;
 }
 
 // Work entries of one launch family, heaviest first.
@@ -609,6 +614,45 @@ swa_status_t swa_workspace_status(const void* workspace, swa_stream_t stream) {
   if (word != 0) return fail(SWA_ERR_TIMEOUT, "a kernel gave up a bounded wait (code %d)", word);
   return SWA_OK;
 }
+
+swa_status_t swa_debug_schedule(const swa_params_t* p, int32_t pass, int32_t* items, int64_t capacity,
+                                int64_t* count) {
+  if (!count) return fail(SWA_ERR_PARAM_NULLPTR, "count is NULL");
+  if (pass != 0 && pass != 1) return fail(SWA_ERR_PARAM_INVALID, "pass should be 0 or 1, got %d", pass);
+  Plan plan;
+  swa_status_t st = make_plan(p, plan);
+  if (st != SWA_OK) return st;
+  const bool query_side = pass == 0;
+  const int nh = query_side ? plan.g.N : plan.g.N_kv;
+  const std::vector<SeqDesc> descs = build_descs(plan, query_side);
+  int64_t n = 0;
+  int32_t launch = 0;
+  auto emit = [&](const auto& tab) -> cudaError_t {
+    for (int k = 0; k < tab.n_items; ++k) {
+      const Item it = resolve_item(tab, plan.g, k, nh);
+      int t0, cnt;
+      if (query_side) key_tiles_of_query_tile(plan.g, it.s, it.tile, &t0, &cnt);
+      else query_tiles_of_key_tile(plan.g, it.s, it.tile, &t0, &cnt);
+      if (items && n < capacity) {
+        int32_t* r = items + 6 * n;
+        r[0] = launch;
+        r[1] = it.b;
+        r[2] = it.n;
+        r[3] = it.tile;
+        r[4] = t0;
+        r[5] = cnt;
+      }
+      ++n;
+    }
+    ++launch;
+    return cudaSuccess;
+  };
+  run_tables(descs, emit, emit);
+  *count = n;
+  return SWA_OK;
+}
+
+void swa_debug_stall(int32_t kernels) { g_stall.store(kernels & 7, std::memory_order_relaxed); }
 
 void swa_set_timing_events(void* const* events) {
   for (int i = 0; i < 6; ++i) t_ev[i] = events ? static_cast<cudaEvent_t>(events[i]) : nullptr;

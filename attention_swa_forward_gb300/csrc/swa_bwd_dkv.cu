@@ -57,6 +57,7 @@ struct DkvSmem {
   // can be a full phase behind
   uint64_t s_full[2], s_loaded, dp_full, pt_full[2], ds_full[2], region_free[2], mma_done, drain_sdp, drain_kv;
   uint64_t gen_full[2];  // generated keep bits of the tile in that stage written (compute threads)
+  uint64_t never;        // completed by nothing: the target of the stall test hook
   uint32_t tmem_base;
 };
 constexpr size_t kMaxSmem = 232448;
@@ -101,19 +102,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Item w = resolve_item(tab, a.g, static_cast<int>(blockIdx.x), a.g.N_kv);  // w.n: key/value head
   const SeqInfo sq = w.s;
   const int j0 = w.tile * kTileN;
-  const int j_last = min(j0 + kTileN - 1, sq.kv_len - 1);
 
   // query tiles that see this key tile
-  int lo = 0, hi = sq.q_len - 1;
-  if (g.sparse_mode == 4) {
-    lo = max(lo, j0 - g.next);
-    hi = min(hi, j_last + g.pre);
-  }
-  int q_t0 = 0, n_q = 0;
-  if (lo <= hi) {
-    q_t0 = lo / kTileM;
-    n_q = hi / kTileM - q_t0 + 1;
-  }
+  int q_t0, n_q;
+  query_tiles_of_key_tile(g, sq, w.tile, &q_t0, &n_q);
   // The CTA walks those query tiles for each query head that reads this
   // key/value head (one head without grouping): step it is query tile
   // q_t0 + it % n_q of query head w.n * group + it / n_q, and dK / dV sum
@@ -143,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.mma_done, 1);
     mbar_init(&s.drain_sdp, 1);
     mbar_init(&s.drain_kv, 1);
+    mbar_init(&s.never, 1);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -334,8 +327,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mbar_arrive(&s.gen_full[stage]);
     };
+    // test hook: wait on a barrier that nothing completes, so the bounded
+    // wait runs out and the launch reports it
+    if (g.stall & kStallKeyMajor) ok = compute_wait(&s.never, 0, a.err);
     if (DM == 2 && n_it > 0) gen_tile_bits(0);
-    for (int it = 0; it < n_it; ++it) {
+    for (int it = 0; ok && it < n_it; ++it) {
       const int st = it & 1;
       const int i0 = (q_t0 + it % n_q) * kTileM;
       const bool full = tile_fully_visible(g, sq, i0, j0);

@@ -42,6 +42,7 @@ struct DqSmem {
   alignas(1024) uint8_t v[2][kTileBytes];
   uint64_t qdy_full, k_full[3], k_empty[3], v_full[2], v_empty[2];
   uint64_t s_full, s_loaded, dp_full, dp_loaded, ds_full[2], ds_free[2], drain_s, drain_dp, drain_dq;
+  uint64_t never;  // completed by nothing: the target of the stall test hook
   uint32_t tmem_base;
 };
 static_assert(sizeof(DqSmem<128>) + 1024 <= 232448, "shared memory budget");
@@ -72,19 +73,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hk = w.n / a.g.group;  // the key/value head this query head reads
   const SeqInfo sq = w.s;
   const int q0 = w.tile * kTileM;
-  const int q_last = min(q0 + kTileM - 1, sq.q_len - 1);
 
   // key tiles touched by this query tile
-  int lo = 0, hi = sq.kv_len - 1;
-  if (g.sparse_mode == 4) {
-    lo = max(lo, q0 - g.pre);
-    hi = min(hi, q_last + g.next);
-  }
-  int kv_t0 = 0, n_kv = 0;
-  if (lo <= hi) {
-    kv_t0 = lo / kTileN;
-    n_kv = hi / kTileN - kv_t0 + 1;
-  }
+  int kv_t0, n_kv;
+  key_tiles_of_query_tile(g, sq, w.tile, &kv_t0, &n_kv);
 
   if (threadIdx.x == 0) {
     mbar_init(&s.qdy_full, 1);
@@ -107,6 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.drain_s, 1);
     mbar_init(&s.drain_dp, 1);
     mbar_init(&s.drain_dq, 1);
+    mbar_init(&s.never, 1);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -256,7 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t n_kb0 = 0xFFFFFFFFu, n_kb1 = 0xFFFFFFFFu;
     if (DM != 0 && n_kv > 0) fetch_bits(0, n_kb0, n_kb1);
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
+    // test hook: wait on a barrier that nothing completes, so the bounded
+    // wait runs out and the launch reports it
+    if (g.stall & kStallQueryMajor) ok = compute_wait(&s.never, 0, a.err);
+    for (int j = 0; ok && j < n_kv; ++j) {
       const int b = j & 1;
       const uint32_t u = (j >> 1) & 1;
       const uint32_t kb0 = n_kb0, kb1 = n_kb1;

@@ -4,6 +4,7 @@
 #pragma once
 #include "sm103.cuh"
 #include "swa_internal.h"
+#include "swa_sched.h"
 
 namespace swa {
 
@@ -11,44 +12,6 @@ constexpr int kAtomBytes = 128 * 128;  // one atom column: 128 rows x 128 bytes
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
-// A resolved work item: which (batch, head, tile) this CTA owns, and the
-// geometry of its sequence.
-struct Item {
-  int b, n, tile;
-  SeqInfo s;
-};
-
-// `nh` is the number of heads per batch the table enumerates: query heads
-// for the query-major kernels, key/value heads for the key-major one.
-template <int CAP>
-__device__ __forceinline__ Item resolve_item(const SeqTable<CAP>& tab, const Geometry& g, int k, int nh) {
-  int lo = 0, hi = tab.count - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (tab.d[mid].item_begin <= k) lo = mid; else hi = mid - 1;
-  }
-  const SeqDesc& d = tab.d[lo];
-  const int local = k - d.item_begin;
-  const int h = local / d.tiles;  // head by head: the CTAs in flight share a head's tiles in L2
-  const int rank = local - h * d.tiles;
-  Item it;
-  it.tile = d.descending ? d.tiles - 1 - rank : rank;
-  if (d.b < 0) {
-    it.b = h / nh;
-    it.n = h - it.b * nh;
-    it.s.mask_base = static_cast<int64_t>(it.b) * g.N * g.S_q * static_cast<int64_t>(g.S_kv);
-  } else {
-    it.b = d.b;
-    it.n = h;
-    it.s.mask_base = d.mask_base;
-  }
-  it.s.q_start = d.q_start;
-  it.s.q_len = d.q_len;
-  it.s.kv_start = d.kv_start;
-  it.s.kv_len = d.kv_len;
-  return it;
 }
 
 // Element offset of local query row i of (b, n): BNSD [B,N,S,D] or TND [T,N,D].

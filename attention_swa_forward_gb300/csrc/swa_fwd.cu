@@ -34,6 +34,7 @@ struct FwdSmem {
   alignas(1024) uint8_t v[kStages][kTileBytes];
   uint64_t q_full, k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
   uint64_t s_full[2], s_free[2], p_full[2], o_done[2], drain_s, drain_pv;  // o_done[b]: PV of P buffer b
+  uint64_t never;  // completed by nothing: the target of the stall test hook
   uint32_t tmem_base;
 };
 static_assert(sizeof(FwdSmem<128>) + 1024 <= 232448, "shared memory budget");
@@ -58,19 +59,10 @@ __global__ void __launch_bounds__(224, 1)
   const int hk = w.n / a.g.group;  // the key/value head this query head reads
   const SeqInfo sq = w.s;
   const int q0 = w.tile * kTileM;
-  const int q_last = min(q0 + kTileM - 1, sq.q_len - 1);
 
   // key tiles touched by this query tile
-  int lo = 0, hi = sq.kv_len - 1;
-  if (g.sparse_mode == 4) {
-    lo = max(lo, q0 - g.pre);
-    hi = min(hi, q_last + g.next);
-  }
-  int kv_t0 = 0, n_kv = 0;
-  if (lo <= hi) {
-    kv_t0 = lo / kTileN;
-    n_kv = hi / kTileN - kv_t0 + 1;
-  }
+  int kv_t0, n_kv;
+  key_tiles_of_query_tile(g, sq, w.tile, &kv_t0, &n_kv);
 
   if (threadIdx.x == 0) {
     mbar_init(&s.q_full, 1);
@@ -89,6 +81,7 @@ __global__ void __launch_bounds__(224, 1)
     mbar_init(&s.o_done[1], 1);
     mbar_init(&s.drain_s, 1);
     mbar_init(&s.drain_pv, 1);
+    mbar_init(&s.never, 1);
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -188,8 +181,12 @@ __global__ void __launch_bounds__(224, 1)
     const float c = g.scale_log2;
     float m_use = -INFINITY, m_true = -INFINITY, l = 0.f;
     bool ok = true;
+    // test hook: wait on a barrier that nothing completes, so the bounded
+    // wait runs out and the launch reports it
+    if (g.stall & kStallForward)
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s.never, 0, a.err, kErrFwdSoftmax));
     bool s_ready = false;  // S(it) known complete from a probe issued during the previous tile
-    for (int it = 0; it < n_kv; ++it) {
+    for (int it = 0; ok && it < n_kv; ++it) {
       const int sb = it & 1;
       // warp-uniform outcome: the tcgen05.ld below is warp-collective
       if (!s_ready && !__all_sync(0xFFFFFFFFu, mbar_wait(&s.s_full[sb], (it >> 1) & 1, a.err, kErrFwdSoftmax))) {

@@ -104,7 +104,12 @@ struct Geometry {
   uint32_t keep_thr;  // element kept iff its Philox byte < keep_thr (0..256)
   int32_t T_q;        // query rows per head: B*S_q (BNSD) or T_q (TND)
   int32_t out_f32;    // outputs (out, dq, dk, dv) are fp32; the kernels then read bf16 copies of the inputs
+  int32_t stall;      // test hook (swa_debug_stall): kStall* bits of kernels whose compute warps first wait
+                      // on a barrier that nothing completes, so that the bounded wait runs out
 };
+
+// Geometry::stall bits.
+enum : int32_t { kStallForward = 1, kStallKeyMajor = 2, kStallQueryMajor = 4 };
 
 struct FwdArgs {
   Geometry g;

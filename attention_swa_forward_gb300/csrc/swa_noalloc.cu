@@ -18,8 +18,6 @@
 
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "swa_internal.h"
 
 namespace {
@@ -30,30 +28,22 @@ constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
 // symbol; its device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 128;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached.
-swa_status_t scratch_on_current_device(void** out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess)
-    return swa::set_error(SWA_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices)
-    return swa::set_error(SWA_ERR_UNSUPPORTED, "device ordinal %d is beyond the %d this library tracks", dev,
-                          kMaxDevices);
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess || !ptr)
-      return swa::set_error(SWA_ERR_CUDA, "cudaGetSymbolAddress of the no-alloc scratch failed on device %d: %s",
-                            dev, cudaGetErrorString(e));
-    g_scratch_ptr[dev] = ptr;
+// Device address of the scratch in the current context, looked up on every
+// call.  A cached address could outlive its context (after cudaDeviceReset,
+// or under another context on the same device) and send the kernels to
+// memory that is no longer the scratch; the lookup is cheap once the module
+// is loaded.  The first lookup on a device may load the module, which is why
+// the first call should come before any stream capture.
+swa_status_t scratch_in_current_context(void** out) {
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+  if (e != cudaSuccess || !ptr) {
+    int dev = -1;
+    cudaGetDevice(&dev);
+    return swa::set_error(SWA_ERR_CUDA, "cudaGetSymbolAddress of the no-alloc scratch failed on device %d: %s", dev,
+                          cudaGetErrorString(e));
   }
-  *out = g_scratch_ptr[dev];
+  *out = ptr;
   return SWA_OK;
 }
 
@@ -72,7 +62,7 @@ extern "C" swa_status_t swa_backward_noalloc(const swa_params_t* p, const void* 
                           "(64 MiB); use swa_backward with a workspace",
                           need, kNoAllocScratchBytes);
   void* scratch = nullptr;
-  st = scratch_on_current_device(&scratch);
+  st = scratch_in_current_context(&scratch);
   if (st != SWA_OK) return st;
   return swa_backward(p, q, k, v, dy, out, softmax_max, softmax_sum, drop_mask, dq, dk, dv, scratch,
                       kNoAllocScratchBytes, stream);

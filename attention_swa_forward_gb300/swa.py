@@ -99,6 +99,10 @@ def lib() -> ctypes.CDLL:
             L.swa_step_host_status.restype = st
             L.swa_set_timing_events.argtypes = [vp]
             L.swa_set_timing_events.restype = None
+            L.swa_debug_schedule.argtypes = [P, ctypes.c_int32, vp, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]
+            L.swa_debug_schedule.restype = st
+            L.swa_debug_stall.argtypes = [ctypes.c_int32]
+            L.swa_debug_stall.restype = None
             L.swa_last_error.argtypes = []
             L.swa_last_error.restype = ctypes.c_char_p
             _lib = L
@@ -109,7 +113,7 @@ def exported_symbols():
     return ["swa_params_default", "swa_forward_workspace_size", "swa_forward", "swa_backward_workspace_size",
             "swa_backward", "swa_backward_noalloc", "swa_workspace_status", "swa_set_timing_events",
             "swa_last_error", "swa_dropout_mask", "swa_step_host_buffer_size", "swa_step_host",
-            "swa_step_host_status"]
+            "swa_step_host_status", "swa_debug_schedule", "swa_debug_stall"]
 
 
 def _check(status: int):
@@ -224,6 +228,25 @@ def swa_set_timing_events(events=None):
 
 def swa_last_error() -> str:
     return lib().swa_last_error().decode()
+
+
+def swa_debug_schedule(params: "Params", pass_: int):
+    """The scheduler's work items of one pass as an int32 array [items, 6]:
+    launch, batch, head, tile, first partner tile, partner tile count."""
+    import numpy as np
+
+    count = ctypes.c_int64(0)
+    _check(lib().swa_debug_schedule(params.ref(), int(pass_), None, 0, ctypes.byref(count)))
+    out = np.zeros((max(count.value, 1), 6), dtype=np.int32)
+    _check(lib().swa_debug_schedule(params.ref(), int(pass_), out.ctypes.data_as(ctypes.c_void_p), count.value,
+                                    ctypes.byref(count)))
+    return out[:count.value]
+
+
+def swa_debug_stall(kernels: int):
+    """Test hook: kernels (bit 0 forward, 1 key-major, 2 query-major) whose
+    compute warps first wait on a barrier nothing completes; 0 turns it off."""
+    lib().swa_debug_stall(int(kernels))
 
 
 # ------------------------------------------------------- torch convenience --

@@ -187,16 +187,21 @@ def edge_probe_inputs(geom: Geometry, k_rand: torch.Tensor, dy_rand: torch.Tenso
     """q, k, v, dy (bf16, D >= 8) that put each query row's probability at one
     edge of its visible window, with exact scores.
 
-    With i, j the positions inside the sequence:
+    With i, j the positions inside the sequence and s_j = 1 - 2 (j mod 2):
         q_i  = alpha * (1, 256, -(i mod 256), -256 * (i div 256), 0, ...)
         k_j  = (j mod 256, j div 256, 1, 1, r_j)
-        v_j  = (j mod 256, j div 256, 1, 1, 0, ...)
-        dy_i = (1, 256, -(i mod 256), -256 * (i div 256), u_i)
-    where r_j and u_i are the last D - 4 columns of k_rand and dy_rand.  Every
-    entry is an integer below 2^15 (exact in bf16), so q_i.k_j = alpha*(j - i)
-    and dy_i.v_j = j - i exactly in fp32.  With scale 1 the probability of
-    key j in row i falls by e^|alpha| per key away from the leftmost visible
-    key (alpha < 0) or the rightmost (alpha > 0)."""
+        v_j  = (s_j, 0, ...)
+        dy_i = (1, 0, 0, 0, u_i)
+    where r_j and u_i are the last D - 4 columns of k_rand and dy_rand.  The
+    entries of q and k are integers below 2^15 (exact in bf16), so
+    q_i.k_j = alpha * (j - i) exactly in fp32.  With alpha = +-1 and scale
+    ln 2 the probability of key j in row i halves per key away from the
+    leftmost visible key (alpha < 0) or the rightmost (alpha > 0): the
+    probabilities are powers of two to within 2^-w of a w-key window, exact
+    in bf16, so thousands of rows sharing one edge key (a window clipped at
+    the sequence start) add no common rounding error.  dy_i.v_j = s_j alternates
+    from key to key, so the row's dS at its edge key is never small, and
+    out = P v stays within [-1, 1]."""
     assert geom.D >= 8 and geom.dtype == "bf16"
     i = _local_positions(geom, True)
     j = _local_positions(geom, False)
@@ -209,7 +214,8 @@ def edge_probe_inputs(geom: Geometry, k_rand: torch.Tensor, dy_rand: torch.Tenso
     k[..., 1:2] = torch.div(j, 256.0, rounding_mode="floor")
     k[..., 2:4] = 1.0
     v = torch.zeros(geom.kv_shape(), dtype=torch.float32)
-    v[..., :4] = k[..., :4]
+    v[..., 0:1] = 1.0 - 2.0 * torch.remainder(j, 2.0)
     dy = dy_rand.float().clone()
-    dy[..., :4] = qi
+    dy[..., 0] = 1.0
+    dy[..., 1:4] = 0.0
     return tuple(t.to(torch.bfloat16) for t in (q, k, v, dy))

@@ -185,9 +185,11 @@ SWA_API swa_status_t swa_backward(const swa_params_t *p, const void *q, const vo
  * fixed 64 MiB device array compiled into the library: every GPU that loads
  * the library keeps it until the process exits.  A problem needing more than
  * 64 MiB of scratch (swa_backward_workspace_size) is rejected with
- * SWA_ERR_WORKSPACE.  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  All calls on a device share the array and
+ * SWA_ERR_WORKSPACE.  Every call looks up the array's device address in the
+ * current context (cudaGetSymbolAddress), so an address never outlives its
+ * context; the first lookup on a device may load the library's device code,
+ * so make the first call before any stream capture.  All calls on a device
+ * share the array and
  * each call clears what must start at zero, so calls whose kernels overlap on
  * the GPU (concurrent streams, other threads) race and must be serialised by
  * the caller.  Allocates nothing: no cudaMalloc, cudaFree or allocating
@@ -253,6 +255,40 @@ SWA_API swa_status_t swa_workspace_status(const void *workspace, swa_stream_t st
  * attention kernel launch (swa_forward's forward kernel; swa_backward's
  * key-major dK/dV kernel and query-major dQ kernel).  No other effect. */
 SWA_API void swa_set_timing_events(void *const *events);
+
+/* Test and inspection support (additions of this library; the pages have no
+ * counterpart).
+ *
+ * swa_debug_schedule: the work items that the band / varlen tile scheduler
+ * hands to the kernels of one pass, computed on the host by the same code
+ * the kernels run (no GPU needed).  The window is the BAND inequality of the
+ * FlashAttentionVarLenScore doc (preTokens / nextTokens as the left and right
+ * edges): a 128-row query tile touches one run of 128-row key tiles and a
+ * key tile one run of query tiles; tiles outside the runs are skipped.
+ *   pass 0   forward and query-major dQ pass: one item per query tile of
+ *            each (batch, query head); partners are key tiles
+ *   pass 1   key-major dK / dV pass: one item per key tile of each (batch,
+ *            key/value head); partners are query tiles, walked for every
+ *            query head of the group
+ *   items    host, 6 int32 per item in launch order: launch index, batch,
+ *            head, tile, first partner tile, partner tile count; at most
+ *            `capacity` items are written (items may be NULL to count)
+ *   count    host, receives the number of items
+ * Errors: the size query's, SWA_ERR_PARAM_NULLPTR (count), and
+ * SWA_ERR_PARAM_INVALID (pass).
+ *
+ * swa_debug_stall: while `kernels` is non-zero, every later call makes the
+ * compute warps of the selected kernels (bit 0 forward, bit 1 key-major
+ * dK / dV, bit 2 query-major dQ) first wait on a barrier that nothing
+ * completes.  That wait gives up after its 2 s limit like any other, the
+ * kernel drains its copies and tensor-core work in flight, frees its tensor
+ * memory and returns, and swa_workspace_status then reports
+ * SWA_ERR_TIMEOUT: it exercises the bounded-wait failure path without a
+ * fault.  The outputs of such a call are undefined.  Process-wide; 0 turns
+ * it off. */
+SWA_API swa_status_t swa_debug_schedule(const swa_params_t *p, int32_t pass, int32_t *items, int64_t capacity,
+                                        int64_t *count);
+SWA_API void swa_debug_stall(int32_t kernels);
 
 /* Text describing the last non-OK status returned on this thread. */
 SWA_API const char *swa_last_error(void);

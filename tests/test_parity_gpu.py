@@ -15,6 +15,8 @@ two long ones (heads are independent problems, so the oracle runs on one
 head's slice): two heads of BNSD 1x32x32768x128 BAND(4096, 0) and two
 (sequence, head) slices of the TND workload.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -271,20 +273,20 @@ def test_masked_set_exact_forward(name):
         assert np.array_equal(np.rint(got), ref[~empty].astype(np.float64)), which
 
 
-@pytest.mark.parametrize("alpha", [-2.0, 2.0], ids=["left_edge", "right_edge"])
+@pytest.mark.parametrize("alpha", [-1.0, 1.0], ids=["left_edge", "right_edge"])
 @pytest.mark.parametrize("name", sorted(MASKSETS))
 def test_masked_set_exact_backward(name, alpha):
     """Both backward passes use exactly the oracle's visible pairs.
 
-    The edge probe (workloads.edge_probe_inputs) puts most of each row's probability
-    on the key at one edge of its window (alpha < 0: the leftmost visible
-    key, alpha > 0: the rightmost) and keeps the scores exact.  One pair too
-    many at that edge then has a probability e^2 times the row's largest, and
-    one pair too few drops about 0.86 of the row's mass, so dV (key-major
-    pass) and dQ (query-major pass) move far past the element gate on every
-    row and key the error touches; tests/test_oracle_pins.py shows that on
+    The edge probe (workloads.edge_probe_inputs) puts half of each row's
+    probability on the key at one edge of its window (alpha < 0: the
+    leftmost visible key, alpha > 0: the rightmost), halving per key inward,
+    with exact scores.  One pair too many at that edge then has twice the
+    row's largest probability, and one pair too few drops half of the row's
+    mass, so dV (key-major pass) and dQ (query-major pass) move far past the
+    element gate on every row and key the error touches; tests/test_oracle_pins.py shows that on
     the oracle with windows moved by one pair at each edge."""
-    geom = Geometry(**{**MASKSETS[name], "scale": 1.0})
+    geom = Geometry(**{**MASKSETS[name], "scale": math.log(2.0)})
     inp = draw(geom, 13)
     inp.q, inp.k, inp.v, inp.dy = edge_probe_inputs(geom, inp.k, inp.dy, alpha)
     pr = to_problem(geom)
@@ -293,7 +295,13 @@ def test_masked_set_exact_backward(name, alpha):
     dq, dk, dv = orc.backward(pr, inp.q, inp.k, inp.v, inp.dy)
     label = f"edge probe {name} alpha={alpha:+g}"
     check_forward(res, out, smax, ssum, label)
-    check_grads(res, dq, dk, dv, label)
+    # dQ columns 0-1 and dK columns 0-3 carry the position code of k and q
+    # (entries up to 255 and 32512): there the bf16 rounding of dS alone is
+    # above the gate, and they add nothing about the window that columns 4+
+    # do not show
+    check_tensor(label, "dq[2:]", res["dq"][..., 2:], dq[..., 2:], "bf16", TOL_GRAD)
+    check_tensor(label, "dk[4:]", res["dk"][..., 4:], dk[..., 4:], "bf16")
+    check_tensor(label, "dv", res["dv"], dv, "bf16", TOL_GRAD)
 
 
 # ------------------------------------------------- full-size workloads -----
