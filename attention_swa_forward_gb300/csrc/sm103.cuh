@@ -159,6 +159,20 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, b
   return r != 0;
 }
 
+// Named barrier that also counts the participating threads whose predicate
+// is true; every thread gets the count.
+__device__ __forceinline__ uint32_t named_barrier_popc(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.popc.u32 %0, %2, %3, p;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r;
+}
+
 // Generic-proxy shared-memory writes -> visible to the async proxy (tensor core).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -27,51 +27,131 @@
 // always has the next GEMM queued while the compute warps work.  Two issuing
 // threads keep it fed: its queue is shallow, so every barrier wait of a
 // single issuer between GEMMs left it idle.
+//
+// Shared memory: the seven 128-row tiles take all but 3 KB of the 227 KB a
+// CTA may have; the barriers and per-query statistics are placed around them
+// (DkvPlan), so the kernel needs no particular alignment of its dynamic
+// shared-memory base.
 #include "swa_device.cuh"
 
 namespace swa {
 namespace {
 
-template <bool DROP>
-struct KeepBits {
-  uint32_t w[2][kTileM][4];  // dropout keep bits: [stage][query row][key word]
-};
-template <>
-struct KeepBits<false> {};
-
-template <int D, bool DROP>
-struct DkvSmem {
-  static constexpr int kTileBytes = kTileM * D * 2;
-  // a third Q stage lets Q(i+2) load while tile i computes; it does not fit
-  // next to the dropout bits at D = 128
-  static constexpr int kQStages = (DROP && D == 128) ? 2 : 3;
-  alignas(1024) uint8_t k[kTileBytes];
-  alignas(1024) uint8_t v[kTileBytes];
-  alignas(1024) uint8_t q[kQStages][kTileBytes];
-  alignas(1024) uint8_t dy[2][kTileBytes];
-  float lse2[2][kTileM];  // per query column of the tile in that stage (+inf: row outside)
-  float dsum[2][kTileM];
-  KeepBits<DROP> keep;
-  uint64_t kv_full, q_full[kQStages], q_empty[kQStages], dy_full[2], dy_empty[2], stat_full[2];
-  // per-region barriers where the two issuers hand off, so that no waiter
-  // can be a full phase behind
-  uint64_t s_full[2], s_loaded, dp_full, pt_full[2], ds_full[2], region_free[2], mma_done, drain_sdp, drain_kv;
-  uint64_t gen_full[2];  // generated keep bits of the tile in that stage written (compute threads)
-  uint64_t never;        // completed by nothing: the target of the stall test hook
-  uint32_t tmem_base;
-};
-constexpr size_t kMaxSmem = 232448;
-static_assert(sizeof(DkvSmem<128, false>) <= kMaxSmem, "shared memory budget");
-static_assert(sizeof(DkvSmem<128, true>) + 1024 <= kMaxSmem, "shared memory budget");
-// Whether the launch can add 1 KB of slack to align the dynamic shared memory
-// base to 1024 bytes; without it the kernel checks the alignment itself.
-template <int D, bool DROP>
-constexpr bool kDkvSlack = sizeof(DkvSmem<D, DROP>) + 1024 <= kMaxSmem;
-
 constexpr int kThreads = 352;
 constexpr int kComputeThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColDV = 256;
+constexpr size_t kMaxSmem = 232448;
+
+// mbarrier slots
+enum : int {
+  kBarKvFull = 0,
+  kBarQFull = 1,       // [3]
+  kBarQEmpty = 4,      // [3]
+  kBarDyFull = 7,      // [2]
+  kBarDyEmpty = 9,     // [2]
+  kBarStatFull = 11,   // [2]
+  kBarGenFull = 13,    // [2] generated keep bits of the tile in that stage written (compute threads)
+  kBarSFull = 15,      // [2] per region: the two issuers hand off there, so no waiter is a phase behind
+  kBarPtFull = 17,     // [2]
+  kBarDsFull = 19,     // [2]
+  kBarRegionFree = 21, // [2]
+  kBarSLoaded = 23,
+  kBarDpFull,
+  kBarMmaDone,
+  kBarDrainSdp,
+  kBarDrainKv,
+  kBarNever,  // completed by nothing: the target of the stall test hook
+  kNumBars
+};
+
+// Shared-memory plan.  The tiles (K, V, the Q ring, the dY ring) need
+// 1024-byte alignment (128-byte swizzle atoms); the small items (barriers,
+// per-query statistics, keep bits) go into the gap before the first aligned
+// address where they fit and after the tiles otherwise, so the layout fits the
+// request for every 16-byte-aligned base of dynamic shared memory.
+template <int D, bool DROP>
+struct DkvPlan {
+  static constexpr int kTileBytes = kTileM * D * 2;
+  // a third Q stage lets Q(i+2) load while tile i computes; it does not fit
+  // next to the dropout bits at D = 128
+  static constexpr int kQStages = (DROP && D == 128) ? 2 : 3;
+  static constexpr int kTiles = 2 + kQStages + 2;
+  static constexpr size_t kTileRegion = static_cast<size_t>(kTiles) * kTileBytes;
+  static constexpr size_t kBarBytes = ((kNumBars * 8 + 4) + 15) / 16 * 16;  // barriers + TMEM address slot
+  static constexpr size_t kStatBytes = 2 * kTileM * 4;                      // lse2 (or D) of both stages
+  static constexpr size_t kKeepBytes = DROP ? 2 * kTileM * 4 * 4 : 0;       // keep words of both stages
+  static constexpr int kItems = DROP ? 4 : 3;
+  static constexpr size_t item(int i) {
+    return i == 0 ? kBarBytes : (i < 3 ? kStatBytes : kKeepBytes);  // barriers, lse2, D, keep bits
+  }
+  static constexpr size_t kSmallBytes = kBarBytes + 2 * kStatBytes + kKeepBytes;
+  static constexpr size_t kSmem =
+      kTileRegion + kSmallBytes + 1024 < kMaxSmem ? kTileRegion + kSmallBytes + 1024 : kMaxSmem;
+  // every 16-byte base offset modulo 1024 leaves room for the greedy placement
+  static constexpr bool fits() {
+    for (size_t x = 0; x < 1024; x += 16) {
+      size_t front = (1024 - x) & 1023;
+      if (kSmem < front + kTileRegion) return false;
+      size_t tail = kSmem - front - kTileRegion;
+      for (int i = 0; i < kItems; ++i) {
+        if (item(i) <= front) front -= item(i);
+        else if (item(i) <= tail) tail -= item(i);
+        else return false;
+      }
+    }
+    return true;
+  }
+};
+static_assert(DkvPlan<128, false>::fits() && DkvPlan<128, true>::fits(), "shared memory budget");
+static_assert(DkvPlan<64, false>::fits() && DkvPlan<64, true>::fits(), "shared memory budget");
+
+// Addresses of the plan's items; stage s of a ring or of the per-tile
+// arrays is found by arithmetic (no run-time indexed pointer arrays, which
+// would live in local memory).
+template <int D, bool DROP>
+struct DkvSmem {
+  using P = DkvPlan<D, DROP>;
+  uint8_t* tiles;  // K, V, Q stages, dY stages
+  uint64_t* bar;
+  uint32_t* tmem_slot;
+  float* lse2_base;    // [2][128]: per query column of the tile in that stage (+inf: row outside)
+  float* dsum_base;    // [2][128]
+  uint32_t* keep_base;  // [2][128][4]: dropout keep bits, [query row][key word]
+
+  __device__ explicit DkvSmem(uint8_t* raw) {
+    const uintptr_t base = reinterpret_cast<uintptr_t>(raw);
+    tiles = reinterpret_cast<uint8_t*>((base + 1023) & ~uintptr_t(1023));
+    uint8_t* front = raw;
+    size_t front_left = static_cast<size_t>(tiles - raw);
+    uint8_t* tail = tiles + P::kTileRegion;
+    auto take = [&](size_t n) -> uint8_t* {  // the same greedy rule DkvPlan::fits checks
+      uint8_t* p;
+      if (n <= front_left) {
+        p = front;
+        front += n;
+        front_left -= n;
+      } else {
+        p = tail;
+        tail += n;
+      }
+      return p;
+    };
+    uint8_t* b = take(P::kBarBytes);
+    bar = reinterpret_cast<uint64_t*>(b);
+    tmem_slot = reinterpret_cast<uint32_t*>(b + kNumBars * 8);
+    lse2_base = reinterpret_cast<float*>(take(P::kStatBytes));
+    dsum_base = reinterpret_cast<float*>(take(P::kStatBytes));
+    keep_base = DROP ? reinterpret_cast<uint32_t*>(take(P::kKeepBytes)) : nullptr;
+  }
+  __device__ uint8_t* k() const { return tiles; }
+  __device__ uint8_t* v() const { return tiles + P::kTileBytes; }
+  __device__ uint8_t* q(int st) const { return tiles + (2 + st) * P::kTileBytes; }
+  __device__ uint8_t* dy(int st) const { return tiles + (2 + P::kQStages + st) * P::kTileBytes; }
+  __device__ float* lse2(int st) const { return lse2_base + st * kTileM; }
+  __device__ float* dsum(int st) const { return dsum_base + st * kTileM; }
+  __device__ uint32_t* keep(int st) const { return keep_base + st * kTileM * 4; }
+};
 
 // Warp-uniform bounded wait of the compute warps.  A warp vote (not a
 // CTA-wide barrier) keeps each warp converged for its warp-collective TMEM
@@ -87,15 +167,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                        const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdy) {
   constexpr bool DROP = DM != 0;
-  using Smem = DkvSmem<D, DROP>;
-  constexpr int kQS = Smem::kQStages;
-  extern __shared__ uint8_t smem_raw[];
-  if (!kDkvSlack<D, DROP> && (smem_u32(smem_raw) & 1023u) != 0) {
-    if (threadIdx.x == 0) atomicCAS(a.err, 0, kErrSmemAlign);
-    return;
-  }
-  Smem& s = *reinterpret_cast<Smem*>(align1024(smem_raw));
-  constexpr int kTileBytes = Smem::kTileBytes;
+  using Plan = DkvPlan<D, DROP>;
+  constexpr int kQS = Plan::kQStages;
+  constexpr int kTileBytes = Plan::kTileBytes;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  const DkvSmem<D, DROP> s(smem_raw);
+  uint64_t* const bar = s.bar;
   constexpr uint32_t kColDK = kColDV + D;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Geometry& g = a.g;
@@ -113,39 +190,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_it = g.group * n_q;
 
   if (threadIdx.x == 0) {
-    mbar_init(&s.kv_full, 1);
+    mbar_init(&bar[kBarKvFull], 1);
     for (int st = 0; st < kQS; ++st) {
-      mbar_init(&s.q_full[st], 1);
-      mbar_init(&s.q_empty[st], 1);
+      mbar_init(&bar[kBarQFull + (st)], 1);
+      mbar_init(&bar[kBarQEmpty + (st)], 1);
     }
     for (int st = 0; st < 2; ++st) {
-      mbar_init(&s.dy_full[st], 1);
-      mbar_init(&s.dy_empty[st], 1);
-      mbar_init(&s.stat_full[st], 32);
-      mbar_init(&s.gen_full[st], kComputeThreads);
-      mbar_init(&s.s_full[st], 1);
+      mbar_init(&bar[kBarDyFull + (st)], 1);
+      mbar_init(&bar[kBarDyEmpty + (st)], 1);
+      mbar_init(&bar[kBarStatFull + (st)], 32);
+      mbar_init(&bar[kBarGenFull + (st)], kComputeThreads);
+      mbar_init(&bar[kBarSFull + (st)], 1);
     }
-    mbar_init(&s.s_loaded, kComputeThreads);
-    mbar_init(&s.dp_full, 1);
+    mbar_init(&bar[kBarSLoaded], kComputeThreads);
+    mbar_init(&bar[kBarDpFull], 1);
     for (int r = 0; r < 2; ++r) {
-      mbar_init(&s.pt_full[r], kComputeThreads);
-      mbar_init(&s.ds_full[r], kComputeThreads);
-      mbar_init(&s.region_free[r], 1);
+      mbar_init(&bar[kBarPtFull + (r)], kComputeThreads);
+      mbar_init(&bar[kBarDsFull + (r)], kComputeThreads);
+      mbar_init(&bar[kBarRegionFree + (r)], 1);
     }
-    mbar_init(&s.mma_done, 1);
-    mbar_init(&s.drain_sdp, 1);
-    mbar_init(&s.drain_kv, 1);
-    mbar_init(&s.never, 1);
+    mbar_init(&bar[kBarMmaDone], 1);
+    mbar_init(&bar[kBarDrainSdp], 1);
+    mbar_init(&bar[kBarDrainKv], 1);
+    mbar_init(&bar[kBarNever], 1);
     fence_mbar_init();
   }
   if (warp == 9) {
-    tmem_alloc(&s.tmem_base, kTmemCols);
+    tmem_alloc(s.tmem_slot, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const uint32_t tmem = s.tmem_base;
+  const uint32_t tmem = *s.tmem_slot;
 
   if (warp == 8) {
     // -------------------------------------------------- producer (warp) --
@@ -155,9 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&mk);
         tma_prefetch_desc(&mv);
         tma_prefetch_desc(&mdy);
-        mbar_arrive_expect_tx(&s.kv_full, 2 * kTileBytes);
-        tma_rows<D>(s.k, &mk, &s.kv_full, g, w.b, w.n, sq.kv_start, j0);
-        tma_rows<D>(s.v, &mv, &s.kv_full, g, w.b, w.n, sq.kv_start, j0);
+        mbar_arrive_expect_tx(&bar[kBarKvFull], 2 * kTileBytes);
+        tma_rows<D>(s.k(), &mk, &bar[kBarKvFull], g, w.b, w.n, sq.kv_start, j0);
+        tma_rows<D>(s.v(), &mv, &bar[kBarKvFull], g, w.b, w.n, sq.kv_start, j0);
       }
       int q_issued = 0, dy_issued = 0;
       for (int it = 0; it < n_it; ++it) {
@@ -166,22 +243,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qs = it % kQS;
         // Q(it) reuses the stage of Q(it - kQS), free once dK of that tile is done
         if (it >= kQS &&
-            !__all_sync(0xFFFFFFFFu, mbar_wait(&s.q_empty[qs], ((it / kQS) - 1) & 1, a.err, kErrBwdLoad)))
+            !__all_sync(0xFFFFFFFFu, mbar_wait(&bar[kBarQEmpty + (qs)], ((it / kQS) - 1) & 1, a.err, kErrBwdLoad)))
           break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&s.q_full[qs], kTileBytes);
-          tma_rows<D>(s.q[qs], &mq, &s.q_full[qs], g, w.b, qn, sq.q_start, i0);
+          mbar_arrive_expect_tx(&bar[kBarQFull + (qs)], kTileBytes);
+          tma_rows<D>(s.q(qs), &mq, &bar[kBarQFull + (qs)], g, w.b, qn, sq.q_start, i0);
         }
         ++q_issued;
         // dY and the statistics reuse stage (it & 1) once dV(it - 2) is done,
         // which also means the compute warps are through with tile it - 2
         const int st = it & 1;
         if (it >= 2 &&
-            !__all_sync(0xFFFFFFFFu, mbar_wait(&s.dy_empty[st], ((it >> 1) - 1) & 1, a.err, kErrBwdLoad)))
+            !__all_sync(0xFFFFFFFFu, mbar_wait(&bar[kBarDyEmpty + (st)], ((it >> 1) - 1) & 1, a.err, kErrBwdLoad)))
           break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&s.dy_full[st], kTileBytes);
-          tma_rows<D>(s.dy[st], &mdy, &s.dy_full[st], g, w.b, qn, sq.q_start, i0);
+          mbar_arrive_expect_tx(&bar[kBarDyFull + (st)], kTileBytes);
+          tma_rows<D>(s.dy(st), &mdy, &bar[kBarDyFull + (st)], g, w.b, qn, sq.q_start, i0);
         }
         ++dy_issued;
         // per-query statistics (and keep bits) of this tile: 4 rows per lane
@@ -197,25 +274,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             dd = a.dsum[si];
             if constexpr (DM == 1) load_keep_bits(a.mask, sq, qn, i, j0, bits);
           }
-          s.lse2[st][c] = l2;
-          s.dsum[st][c] = dd;
+          s.lse2(st)[c] = l2;
+          s.dsum(st)[c] = dd;
           if constexpr (DM == 1) {
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) s.keep.w[st][c][q4] = bits[q4];
+            for (int q4 = 0; q4 < 4; ++q4) s.keep(st)[(c) * 4 + (q4)] = bits[q4];
           }
         }
-        mbar_arrive(&s.stat_full[st]);
+        mbar_arrive(&bar[kBarStatFull + (st)]);
       }
       // every copy issued has landed before the CTA may exit
       if (lane == 0) {
-        mbar_wait_drain(&s.kv_full, 0);
+        mbar_wait_drain(&bar[kBarKvFull], 0);
         for (int st = 0; st < kQS; ++st) {
           const int uq = (q_issued - st + kQS - 1) / kQS;
-          if (uq > 0) mbar_wait_drain(&s.q_full[st], (uq - 1) & 1);
+          if (uq > 0) mbar_wait_drain(&bar[kBarQFull + (st)], (uq - 1) & 1);
         }
         for (int st = 0; st < 2; ++st) {
           const int ud = (dy_issued - st + 1) / 2;
-          if (ud > 0) mbar_wait_drain(&s.dy_full[st], (ud - 1) & 1);
+          if (ud > 0) mbar_wait_drain(&bar[kBarDyFull + (st)], (ud - 1) & 1);
         }
       }
     }
@@ -223,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------- tcgen05 issuer --
     if (lane == 0 && n_q > 0) {
       constexpr uint32_t kIdT = idesc_f16_f32(kTileN, kTileM, false, false, F16);  // S^T, dP^T
-      const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
+      const uint32_t k_addr = smem_u32(s.k()), v_addr = smem_u32(s.v());
       const int nk = d_steps(g);
       auto issue_ss = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {  // 128 x 128 x D, both K-major
 #pragma unroll
@@ -234,32 +311,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                        kk > 0);
         }
       };
-      bool ok = mbar_wait(&s.kv_full, 0, a.err, kErrBwdMma) && mbar_wait(&s.q_full[0], 0, a.err, kErrBwdMma);
+      bool ok = mbar_wait(&bar[kBarKvFull], 0, a.err, kErrBwdMma) && mbar_wait(&bar[kBarQFull + (0)], 0, a.err, kErrBwdMma);
       if (ok) {
         tc_fence_after_sync();
-        issue_ss(region(0), k_addr, smem_u32(s.q[0]));  // S^T(0) = K Q(0)^T
-        umma_commit(&s.s_full[0]);
+        issue_ss(region(0), k_addr, smem_u32(s.q(0)));  // S^T(0) = K Q(0)^T
+        umma_commit(&bar[kBarSFull + (0)]);
       }
       for (int it = 0; ok && it < n_it; ++it) {
         const int st = it & 1;
         // dP^T(it) over S^T(it), once every compute thread has read S^T(it)
-        if (!mbar_wait(&s.s_loaded, it & 1, a.err, kErrBwdMma)) break;
-        if (!mbar_wait(&s.dy_full[st], (it >> 1) & 1, a.err, kErrBwdMma)) break;
+        if (!mbar_wait(&bar[kBarSLoaded], it & 1, a.err, kErrBwdMma)) break;
+        if (!mbar_wait(&bar[kBarDyFull + (st)], (it >> 1) & 1, a.err, kErrBwdMma)) break;
         tc_fence_after_sync();
-        issue_ss(region(it), v_addr, smem_u32(s.dy[st]));  // dP^T = V dY^T
-        umma_commit(&s.dp_full);
+        issue_ss(region(it), v_addr, smem_u32(s.dy(st)));  // dP^T = V dY^T
+        umma_commit(&bar[kBarDpFull]);
         if (it + 1 < n_it) {
           // S^T(it+1) into the other region, once dK(it-1) has read it
-          if (it >= 1 && !mbar_wait(&s.region_free[(it - 1) & 1], ((it - 1) >> 1) & 1, a.err, kErrBwdMma)) break;
+          if (it >= 1 && !mbar_wait(&bar[kBarRegionFree + ((it - 1) & 1)], ((it - 1) >> 1) & 1, a.err, kErrBwdMma)) break;
           const int nq = (it + 1) % kQS;
-          if (!mbar_wait(&s.q_full[nq], ((it + 1) / kQS) & 1, a.err, kErrBwdMma)) break;
+          if (!mbar_wait(&bar[kBarQFull + (nq)], ((it + 1) / kQS) & 1, a.err, kErrBwdMma)) break;
           tc_fence_after_sync();
-          issue_ss(region(it + 1), k_addr, smem_u32(s.q[nq]));
-          umma_commit(&s.s_full[(it + 1) & 1]);
+          issue_ss(region(it + 1), k_addr, smem_u32(s.q(nq)));
+          umma_commit(&bar[kBarSFull + ((it + 1) & 1)]);
         }
       }
-      umma_commit(&s.drain_sdp);
-      mbar_wait_drain(&s.drain_sdp, 0);
+      umma_commit(&bar[kBarDrainSdp]);
+      mbar_wait_drain(&bar[kBarDrainSdp], 0);
     }
   } else if (warp == 10) {
     // ------------------------------------------------- dV / dK issuer --
@@ -271,27 +348,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         // query columns [64h, 64h+64) of the tile hold P^T in columns
         // [64h, 64h+32) and dS^T in [64h+32, 64h+64), two bf16 per column.
         // P^T is stored first, so dV(it) runs while dS^T is computed.
-        if (!mbar_wait(&s.pt_full[st], (it >> 1) & 1, a.err, kErrBwdMma)) break;
+        if (!mbar_wait(&bar[kBarPtFull + (st)], (it >> 1) & 1, a.err, kErrBwdMma)) break;
         tc_fence_after_sync();
         const uint32_t ra = tmem + region(it);
-        const uint32_t dy_addr = smem_u32(s.dy[st]), q_addr = smem_u32(s.q[qs]);
+        const uint32_t dy_addr = smem_u32(s.dy(st)), q_addr = smem_u32(s.q(qs));
 #pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk)  // dV += P^T dY  (K dim = query rows)
           umma_bf16_ts(tmem + kColDV, ra + (kk >> 2) * 64 + (kk & 3) * 8,
                        sdesc_sw128(dy_addr + kk * 2048, kAtomBytes, 1024), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&s.dy_empty[st]);  // dP^T(it) read dY(it) too; it finished before P^T(it) existed
-        if (!mbar_wait(&s.ds_full[st], (it >> 1) & 1, a.err, kErrBwdMma)) break;
+        umma_commit(&bar[kBarDyEmpty + (st)]);  // dP^T(it) read dY(it) too; it finished before P^T(it) existed
+        if (!mbar_wait(&bar[kBarDsFull + (st)], (it >> 1) & 1, a.err, kErrBwdMma)) break;
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk)  // dK += dS^T Q
           umma_bf16_ts(tmem + kColDK, ra + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
                        sdesc_sw128(q_addr + kk * 2048, kAtomBytes, 1024), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&s.q_empty[qs]);  // likewise S^T(it) for Q(it)
-        umma_commit(&s.region_free[st]);
-        if (it == n_it - 1) umma_commit(&s.mma_done);
+        umma_commit(&bar[kBarQEmpty + (qs)]);  // likewise S^T(it) for Q(it)
+        umma_commit(&bar[kBarRegionFree + (st)]);
+        if (it == n_it - 1) umma_commit(&bar[kBarMmaDone]);
       }
-      umma_commit(&s.drain_kv);
-      mbar_wait_drain(&s.drain_kv, 0);
+      umma_commit(&bar[kBarDrainKv]);
+      mbar_wait_drain(&bar[kBarDrainKv], 0);
     }
   } else {
     // ------------------------------------------- compute warps (0..7) -----
@@ -322,22 +399,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t words[2];
       gen_keep_words<2>(g, stat_index(g, sq, w.b, qn, row_i), (j0 + cbase) >> 4, words);
       if constexpr (DROP) {
-        s.keep.w[stage][r][2 * h] = words[0];
-        s.keep.w[stage][r][2 * h + 1] = words[1];
+        s.keep(stage)[(r) * 4 + (2 * h)] = words[0];
+        s.keep(stage)[(r) * 4 + (2 * h + 1)] = words[1];
       }
-      mbar_arrive(&s.gen_full[stage]);
+      mbar_arrive(&bar[kBarGenFull + (stage)]);
     };
     // test hook: wait on a barrier that nothing completes, so the bounded
     // wait runs out and the launch reports it
-    if (g.stall & kStallKeyMajor) ok = compute_wait(&s.never, 0, a.err);
+    if (g.stall & kStallKeyMajor) ok = compute_wait(&bar[kBarNever], 0, a.err);
     if (DM == 2 && n_it > 0) gen_tile_bits(0);
     for (int it = 0; ok && it < n_it; ++it) {
       const int st = it & 1;
       const int i0 = (q_t0 + it % n_q) * kTileM;
       const bool full = tile_fully_visible(g, sq, i0, j0);
       const uint32_t col = tmem + lane_off + region(it) + cbase;
-      if (!compute_wait(&s.s_full[st], (it >> 1) & 1, a.err)) { ok = false; break; }
-      if (!compute_wait(&s.stat_full[st], (it >> 1) & 1, a.err)) { ok = false; break; }
+      if (!compute_wait(&bar[kBarSFull + (st)], (it >> 1) & 1, a.err)) { ok = false; break; }
+      if (!compute_wait(&bar[kBarStatFull + (st)], (it >> 1) & 1, a.err)) { ok = false; break; }
       tc_fence_after_sync();
       // ---- S^T -> P^T (registers)
       float p[64];
@@ -348,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait(s0);
         tmem_ld_wait(s1);
         tc_fence_before_sync();
-        mbar_arrive(&s.s_loaded);  // region(it) may now receive dP^T(it)
+        mbar_arrive(&bar[kBarSLoaded]);  // region(it) may now receive dP^T(it)
         // Two copies of the loop: tiles entirely inside the window (nearly
         // all of them) need no per-element mask.  In the masked copy the
         // exp2 is unconditional and the comparisons use non-short-circuit
@@ -356,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (full) {
 #pragma unroll
           for (int t4 = 0; t4 < 16; ++t4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[st][cbase + t4 * 4]);
+            const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2(st)[cbase + t4 * 4]);
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
             for (int u = 0; u < 4; u += 2) {  // packed pairs: (s*c - lse2) in one f32x2 FMA
@@ -372,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int lo_t = qlo - (i0 + cbase), hi_t = qhi - (i0 + cbase);  // visible t in [lo_t, hi_t]
 #pragma unroll
           for (int t4 = 0; t4 < 16; ++t4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[st][cbase + t4 * 4]);
+            const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2(st)[cbase + t4 * 4]);
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -386,78 +463,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- next tile's generated keep bits, into the stage tile it-1 used
       // once every thread is through with tile it-1 (its ds_full)
       if (DM == 2 && it + 1 < n_it) {
-        if (it >= 1 && !compute_wait(&s.ds_full[(it - 1) & 1], ((it - 1) >> 1) & 1, a.err)) { ok = false; break; }
+        if (it >= 1 && !compute_wait(&bar[kBarDsFull + ((it - 1) & 1)], ((it - 1) >> 1) & 1, a.err)) { ok = false; break; }
         gen_tile_bits(it + 1);
       }
       // ---- dP^T -> dS^T; P^T*z/keep and dS^T packed bf16 into the same columns
-      if (DM == 2 && !compute_wait(&s.gen_full[st], (it >> 1) & 1, a.err)) { ok = false; break; }
-      if (!compute_wait(&s.dp_full, it & 1, a.err)) { ok = false; break; }
+      if (DM == 2 && !compute_wait(&bar[kBarGenFull + (st)], (it >> 1) & 1, a.err)) { ok = false; break; }
+      if (!compute_wait(&bar[kBarDpFull], it & 1, a.err)) { ok = false; break; }
       tc_fence_after_sync();
       {
-        uint32_t d0[32], d1[32];
-        tmem_ld_32x32b_x32(col, d0);
-        tmem_ld_32x32b_x32(col + 32, d1);
-        tmem_ld_wait(d0);
-        tmem_ld_wait(d1);
         // this thread's keep bits of the tile: bit t = (query cbase + t, key r)
         uint32_t km[2] = {~0u, ~0u};
         if constexpr (DROP) {
           km[0] = km[1] = 0u;
 #pragma unroll
-          for (int t = 0; t < 64; ++t) km[t >> 5] |= ((s.keep.w[st][cbase + t][wq] >> lane) & 1u) << (t & 31);
+          for (int t = 0; t < 64; ++t) km[t >> 5] |= ((s.keep(st)[(cbase + t) * 4 + (wq)] >> lane) & 1u) << (t & 31);
         }
-        // P^T * z / keep first (over the dP^T columns just read), so dV can start
+        // dS^T = P^T * (dP^T * z / keep - D) for the 32 query columns of one half
+        auto ds_half = [&](int half, const uint32_t (&d)[32], uint32_t* dk) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int t2 = 0; t2 < 16; ++t2) {
-            const int t = half * 32 + 2 * t2;
-            float p0 = p[t], p1 = p[t + 1];
+          for (int t4 = 0; t4 < 8; ++t4) {
+            const int tb = half * 32 + t4 * 4;
+            const float4 d4 = *reinterpret_cast<const float4*>(&s.dsum(st)[cbase + tb]);
+            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+            float dsv[4];
             if constexpr (DROP) {
-              p0 = ((km[t >> 5] >> (t & 31)) & 1u) ? p0 * g.inv_keep : 0.f;
-              p1 = ((km[(t + 1) >> 5] >> ((t + 1) & 31)) & 1u) ? p1 * g.inv_keep : 0.f;
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int t = tb + u;
+                float dp = __uint_as_float(d[t4 * 4 + u]);
+                dp = ((km[t >> 5] >> (t & 31)) & 1u) ? dp * g.inv_keep : 0.f;
+                dsv[u] = p[t] * (dp - dv4[u]);
+              }
+            } else {
+#pragma unroll
+              for (int u = 0; u < 4; u += 2)  // packed pairs
+                fmulsub2(dsv[u], dsv[u + 1], p[tb + u], p[tb + u + 1], __uint_as_float(d[t4 * 4 + u]),
+                         __uint_as_float(d[t4 * 4 + u + 1]), dv4[u], dv4[u + 1]);
             }
-            pk[t2] = pack2<F16>(p0, p1);
+            dk[t4 * 2] = pack2<F16>(dsv[0], dsv[1]);
+            dk[t4 * 2 + 1] = pack2<F16>(dsv[2], dsv[3]);
           }
-          tmem_st_32x32b_x16(col + half * 16, pk);
-        }
-        tmem_st_wait();
-        tc_fence_before_sync();
-        mbar_arrive(&s.pt_full[st]);
-        // dS^T = P^T * (dP^T * z / keep - D)
+        };
         uint32_t dk[32];
+        {
+          uint32_t d[32];  // dP^T columns [cbase, cbase + 32): read before P^T goes over them
+          tmem_ld_32x32b_x32(col, d);
+          tmem_ld_wait(d);
+          // P^T * z / keep first, so dV can start
 #pragma unroll
-        for (int t4 = 0; t4 < 16; ++t4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(&s.dsum[st][cbase + t4 * 4]);
-          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-          float dsv[4];
-          if constexpr (DROP) {
+          for (int half = 0; half < 2; ++half) {
+            uint32_t pk[16];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int t = t4 * 4 + u;
-              float dp = __uint_as_float(t < 32 ? d0[t] : d1[t - 32]);
-              dp = ((km[t >> 5] >> (t & 31)) & 1u) ? dp * g.inv_keep : 0.f;
-              dsv[u] = p[t] * (dp - dv4[u]);
+            for (int t2 = 0; t2 < 16; ++t2) {
+              const int t = half * 32 + 2 * t2;
+              float p0 = p[t], p1 = p[t + 1];
+              if constexpr (DROP) {
+                p0 = ((km[t >> 5] >> (t & 31)) & 1u) ? p0 * g.inv_keep : 0.f;
+                p1 = ((km[(t + 1) >> 5] >> ((t + 1) & 31)) & 1u) ? p1 * g.inv_keep : 0.f;
+              }
+              pk[t2] = pack2<F16>(p0, p1);
             }
-          } else {
-#pragma unroll
-            for (int u = 0; u < 4; u += 2) {  // packed pairs
-              const int t = t4 * 4 + u;
-              fmulsub2(dsv[u], dsv[u + 1], p[t], p[t + 1], __uint_as_float(t < 32 ? d0[t] : d1[t - 32]),
-                       __uint_as_float(t + 1 < 32 ? d0[t + 1] : d1[t - 31]), dv4[u], dv4[u + 1]);
-            }
+            tmem_st_32x32b_x16(col + half * 16, pk);
           }
-          dk[t4 * 2] = pack2<F16>(dsv[0], dsv[1]);
-          dk[t4 * 2 + 1] = pack2<F16>(dsv[2], dsv[3]);
+          tmem_st_wait();
+          tc_fence_before_sync();
+          mbar_arrive(&bar[kBarPtFull + (st)]);
+          ds_half(0, d, dk);
+        }
+        {
+          uint32_t d[32];  // dP^T columns [cbase + 32, cbase + 64), where dS^T goes
+          tmem_ld_32x32b_x32(col + 32, d);
+          tmem_ld_wait(d);
+          ds_half(1, d, dk + 16);
         }
         tmem_st_32x32b_x32(col + 32, dk);
       }
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&s.ds_full[st]);
+      mbar_arrive(&bar[kBarDsFull + (st)]);
     }
-    if (ok && n_q > 0) ok = compute_wait(&s.mma_done, 0, a.err);  // every MMA done
+    if (ok && n_q > 0) ok = compute_wait(&bar[kBarMmaDone], 0, a.err);  // every MMA done
     if (ok) {
       tc_fence_after_sync();
       // epilogue: thread r owns key row j0 + r; warps 0-3 write dV, 4-7 dK
@@ -499,8 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, int DM, bool F16, int CAP>
 cudaError_t launch_dkv_t(const BwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, const CUtensorMap& mdy, cudaStream_t stream) {
-  constexpr bool DROP = DM != 0;
-  const size_t smem = sizeof(DkvSmem<D, DROP>) + (kDkvSlack<D, DROP> ? 1024 : 0);
+  constexpr size_t smem = DkvPlan<D, DM != 0>::kSmem;
   static std::atomic<uint64_t> smem_set{0};
   const cudaError_t e = set_smem_limit(swa_bwd_dkv_kernel<D, DM, F16, CAP>, smem, smem_set);
   if (e != cudaSuccess) return e;
