@@ -5,11 +5,15 @@
 // The heads are split into `chunks` equal groups.  Each group is a complete
 // smaller problem (heads are independent in every step of the method), so it
 // is copied into its own compact device tensors, computed by swa_forward and
-// swa_backward on the caller's stream, and copied back.  Chunk c+1's inputs
-// travel host -> device on one stream and chunk c-1's results device -> host
-// on another while chunk c computes.  A head group of a BNSD tensor is one
-// contiguous block per batch, and of a TND tensor one block per row, so every
-// copy is a single 2-D copy (rows = batches or tokens, pitch = the full row).
+// swa_backward, and copied back.  Chunk c+1's inputs travel host -> device on
+// one stream and chunk c-1's results device -> host on another while chunk c
+// computes.  Consecutive chunks compute on two internal streams in turn, so
+// the kernels of chunk c+1 can start on the SMs that chunk c's last wave of
+// CTAs leaves idle: smaller chunks (a shorter pipeline fill and drain of the
+// copies) then cost no kernel efficiency.  A head group of a BNSD tensor is
+// one contiguous block per batch, and of a TND tensor one block per row, so
+// every copy is a single 2-D copy (rows = batches or tokens, pitch = the full
+// row).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -130,14 +134,17 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
     return swa::set_error(SWA_ERR_WORKSPACE, "device_buffer must be >= %zu bytes and 256-byte aligned (got %zu)",
                           L.total, device_bytes);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  // Two copy streams and their events, released by the driver once their
-  // work has run (cudaStreamDestroy / cudaEventDestroy on pending work).
-  cudaStream_t s_in = nullptr, s_out = nullptr;
+  // Two copy streams, two compute streams and their events, released by the
+  // driver once their work has run (cudaStreamDestroy / cudaEventDestroy on
+  // pending work).
+  cudaStream_t s_in = nullptr, s_out = nullptr, s_comp[2] = {nullptr, nullptr};
   std::vector<cudaEvent_t> ev;
   auto release = [&]() {
     for (cudaEvent_t e : ev) cudaEventDestroy(e);
     if (s_in) cudaStreamDestroy(s_in);
     if (s_out) cudaStreamDestroy(s_out);
+    for (cudaStream_t x : s_comp)
+      if (x) cudaStreamDestroy(x);
   };
   auto event = [&](cudaEvent_t* e) {
     const cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
@@ -146,13 +153,14 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
   };
   cudaError_t e = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking);
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&s_comp[i], cudaStreamNonBlocking);
   cudaEvent_t start = nullptr, done = nullptr;
   if (e == cudaSuccess) e = event(&start);
   if (e == cudaSuccess) e = event(&done);
-  // the copies may not start before what the caller queued earlier (which may still use the buffer)
+  // nothing may start before what the caller queued earlier (which may still use the buffer)
   if (e == cudaSuccess) e = cudaEventRecord(start, cs);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_in, start, 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, start, 0);
+  for (cudaStream_t x : {s_in, s_out, s_comp[0], s_comp[1]})
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(x, start, 0);
   if (e != cudaSuccess) {
     release();
     return cuda_fail(e, "setting up the copy streams");
@@ -160,6 +168,8 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
   uint8_t* base = static_cast<uint8_t*>(device_buffer);
   for (int c = 0; c < chunks; ++c) {
     uint8_t* d = base + static_cast<size_t>(c) * L.chunk_bytes;
+    cudaStream_t comp = s_comp[c & 1];
+    const swa_stream_t comp_h = reinterpret_cast<swa_stream_t>(comp);
     cudaEvent_t in_done = nullptr, comp_done = nullptr;
     if ((e = event(&in_done)) != cudaSuccess || (e = event(&comp_done)) != cudaSuccess) break;
     if ((e = copy_in(L.q, c, d + L.q_off, q, s_in)) != cudaSuccess) break;
@@ -167,16 +177,16 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
     if ((e = copy_in(L.kv, c, d + L.v_off, v, s_in)) != cudaSuccess) break;
     if ((e = copy_in(L.q, c, d + L.dy_off, dy, s_in)) != cudaSuccess) break;
     if ((e = cudaEventRecord(in_done, s_in)) != cudaSuccess) break;
-    if ((e = cudaStreamWaitEvent(cs, in_done, 0)) != cudaSuccess) break;
+    if ((e = cudaStreamWaitEvent(comp, in_done, 0)) != cudaSuccess) break;
     st = swa_forward(&L.sub, d + L.q_off, d + L.k_off, d + L.v_off, nullptr, d + L.out_off,
                      reinterpret_cast<float*>(d + L.smax_off), reinterpret_cast<float*>(d + L.ssum_off),
-                     d + L.fws_off, L.fws_bytes, stream);
+                     d + L.fws_off, L.fws_bytes, comp_h);
     if (st != SWA_OK) break;
     st = swa_backward(&L.sub, d + L.q_off, d + L.k_off, d + L.v_off, d + L.dy_off, d + L.out_off,
                       reinterpret_cast<const float*>(d + L.smax_off), reinterpret_cast<const float*>(d + L.ssum_off),
-                      nullptr, d + L.dq_off, d + L.dk_off, d + L.dv_off, d + L.bws_off, L.bws_bytes, stream);
+                      nullptr, d + L.dq_off, d + L.dk_off, d + L.dv_off, d + L.bws_off, L.bws_bytes, comp_h);
     if (st != SWA_OK) break;
-    if ((e = cudaEventRecord(comp_done, cs)) != cudaSuccess) break;
+    if ((e = cudaEventRecord(comp_done, comp)) != cudaSuccess) break;
     if ((e = cudaStreamWaitEvent(s_out, comp_done, 0)) != cudaSuccess) break;
     if ((e = copy_out(L.q, c, out, d + L.out_off, s_out)) != cudaSuccess) break;
     if ((e = copy_out(L.st, c, softmax_max, d + L.smax_off, s_out)) != cudaSuccess) break;
@@ -189,10 +199,15 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
   // host, and, after a failure part-way, only after every copy already
   // enqueued on either copy stream has run: host memory is never written
   // once the caller has seen the stream finish.
-  cudaEvent_t in_end = nullptr;
+  cudaEvent_t in_end = nullptr, comp_end[2] = {nullptr, nullptr};
   cudaError_t e_end = event(&in_end);
   if (e_end == cudaSuccess) e_end = cudaEventRecord(in_end, s_in);
   if (e_end == cudaSuccess) e_end = cudaStreamWaitEvent(cs, in_end, 0);
+  for (int i = 0; i < 2; ++i) {
+    if (e_end == cudaSuccess) e_end = event(&comp_end[i]);
+    if (e_end == cudaSuccess) e_end = cudaEventRecord(comp_end[i], s_comp[i]);
+    if (e_end == cudaSuccess) e_end = cudaStreamWaitEvent(cs, comp_end[i], 0);
+  }
   if (e_end == cudaSuccess) e_end = cudaEventRecord(done, s_out);
   if (e_end == cudaSuccess) e_end = cudaStreamWaitEvent(cs, done, 0);
   if (e == cudaSuccess) e = e_end;

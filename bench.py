@@ -356,7 +356,8 @@ def run_swa(args, name: str):
         chunks = 0
         if hmask is None:
             n_kv = g.N_kv or g.N
-            chunks = next(c for c in (8, 4, 2, 1) if g.N % c == 0 and n_kv % c == 0 and (c == 1 or g.keep_prob == 1.0))
+            chunks = next(c for c in ((args.chunks,) if args.chunks else (16, 8, 4, 2, 1))
+                          if g.N % c == 0 and n_kv % c == 0 and (c == 1 or g.keep_prob == 1.0))
             step_buf = torch.empty(swa.swa_step_host_buffer_size(p, chunks), dtype=torch.uint8, device=dev)
 
         def e2e_step():
@@ -457,6 +458,8 @@ def main(argv=None):
     ap.add_argument("--keep-prob", type=float, default=None, help="override the workload's keep_prob")
     ap.add_argument("--dropout-gen", action="store_true",
                     help="dropout workloads: generate the keep mask in the kernels from a seed / offset")
+    ap.add_argument("--chunks", type=int, default=None,
+                    help="head groups of the end-to-end host step (default: the largest of 16, 8, 4, 2, 1 that divides)")
     ap.add_argument("--heads", type=int, default=None,
                     help="override the workload's head count N (smaller profiling captures)")
     args = ap.parse_args(argv)

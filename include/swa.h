@@ -204,8 +204,10 @@ SWA_API swa_status_t swa_backward_noalloc(const swa_params_t *p, const void *q, 
  * addition of this library; the pages' operators take device tensors).  The
  * heads are split into `chunks` equal groups; each group is copied to its own
  * compact device tensors inside `device_buffer`, computed (swa_forward, then
- * swa_backward, on `stream`) and copied back, and the copies of the next and
- * the previous group run on two internal streams while a group computes.
+ * swa_backward) and copied back, and the copies of the next and the previous
+ * group run on two internal streams while a group computes.  Consecutive
+ * groups compute on two further internal streams in turn, so one group's
+ * kernels may start while the previous group's last CTAs still run.
  * Heads are independent, so the results equal those of one swa_forward +
  * swa_backward on device copies of the same tensors, bit for bit.
  *   q, k, v, dy   host, p->dtype, shapes and layout as for swa_forward /
