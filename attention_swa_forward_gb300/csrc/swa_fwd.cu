@@ -186,8 +186,18 @@ __global__ void __launch_bounds__(224, 1)
     if (g.stall & kStallForward)
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s.never, 0, a.err, kErrFwdSoftmax));
     bool s_ready = false;  // S(it) known complete from a probe issued during the previous tile
+    // Keep bits read from the mask are fetched one tile ahead, so their
+    // global-load latency is not on the softmax's path.
+    uint32_t next_bits[4] = {0u, 0u, 0u, 0u};
+    if (DM == 1 && n_kv > 0 && row_valid) load_keep_bits(a.mask, sq, w.n, i, kv_t0 * kTileN, next_bits);
     for (int it = 0; ok && it < n_kv; ++it) {
       const int sb = it & 1;
+      uint32_t bits[4] = {~0u, ~0u, ~0u, ~0u};
+      if (DM == 1) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) bits[u] = next_bits[u];
+        if (it + 1 < n_kv && row_valid) load_keep_bits(a.mask, sq, w.n, i, (kv_t0 + it + 1) * kTileN, next_bits);
+      }
       // warp-uniform outcome: the tcgen05.ld below is warp-collective
       if (!s_ready && !__all_sync(0xFFFFFFFFu, mbar_wait(&s.s_full[sb], (it >> 1) & 1, a.err, kErrFwdSoftmax))) {
         ok = false;
@@ -256,13 +266,7 @@ __global__ void __launch_bounds__(224, 1)
         m_use = m_new;
       }
       const float msub = (m_use == -INFINITY) ? 0.f : m_use;
-      uint32_t bits[4] = {~0u, ~0u, ~0u, ~0u};
-      if (DM == 1) {
-        bits[0] = bits[1] = bits[2] = bits[3] = 0u;
-        if (row_valid) load_keep_bits(a.mask, sq, w.n, i, j0, bits);
-      } else if (DM == 2) {
-        gen_keep_words<4>(g, stat_index(g, sq, w.b, w.n, i), j0 >> 4, bits);
-      }
+      if (DM == 2) gen_keep_words<4>(g, stat_index(g, sq, w.b, w.n, i), j0 >> 4, bits);
       // p = exp2(.), the row sum of p (before dropout), then P = p*z packed
       // to bf16 pairs in place: xr[t/2] receives the pair (t, t+1)
       float r8[8];
