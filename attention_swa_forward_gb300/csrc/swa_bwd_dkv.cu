@@ -189,7 +189,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // over all of them in TMEM.
   const int n_it = g.group * n_q;
 
-  if (threadIdx.x == 0) {
+  // The producer's lane initialises the barriers and issues the loads of K,
+  // V and the first Q and dY tiles before the CTA-wide barrier, so their
+  // latency runs while TMEM is allocated.
+  if (warp == 8 && lane == 0) {
     mbar_init(&bar[kBarKvFull], 1);
     for (int st = 0; st < kQS; ++st) {
       mbar_init(&bar[kBarQFull + (st)], 1);
@@ -214,6 +217,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar[kBarDrainKv], 1);
     mbar_init(&bar[kBarNever], 1);
     fence_mbar_init();
+    if (n_q > 0) {
+      tma_prefetch_desc(&mq);
+      tma_prefetch_desc(&mk);
+      tma_prefetch_desc(&mv);
+      tma_prefetch_desc(&mdy);
+      mbar_arrive_expect_tx(&bar[kBarKvFull], 2 * kTileBytes);
+      tma_rows<D>(s.k(), &mk, &bar[kBarKvFull], g, w.b, w.n, sq.kv_start, j0);
+      tma_rows<D>(s.v(), &mv, &bar[kBarKvFull], g, w.b, w.n, sq.kv_start, j0);
+      const int i0 = q_t0 * kTileM, qn = w.n * g.group;  // step 0
+      mbar_arrive_expect_tx(&bar[kBarQFull], kTileBytes);
+      tma_rows<D>(s.q(0), &mq, &bar[kBarQFull], g, w.b, qn, sq.q_start, i0);
+      mbar_arrive_expect_tx(&bar[kBarDyFull], kTileBytes);
+      tma_rows<D>(s.dy(0), &mdy, &bar[kBarDyFull], g, w.b, qn, sq.q_start, i0);
+    }
   }
   if (warp == 9) {
     tmem_alloc(s.tmem_slot, kTmemCols);
@@ -227,15 +244,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 8) {
     // -------------------------------------------------- producer (warp) --
     if (n_q > 0) {
-      if (lane == 0) {
-        tma_prefetch_desc(&mq);
-        tma_prefetch_desc(&mk);
-        tma_prefetch_desc(&mv);
-        tma_prefetch_desc(&mdy);
-        mbar_arrive_expect_tx(&bar[kBarKvFull], 2 * kTileBytes);
-        tma_rows<D>(s.k(), &mk, &bar[kBarKvFull], g, w.b, w.n, sq.kv_start, j0);
-        tma_rows<D>(s.v(), &mv, &bar[kBarKvFull], g, w.b, w.n, sq.kv_start, j0);
-      }
       int q_issued = 0, dy_issued = 0;
       for (int it = 0; it < n_it; ++it) {
         const int i0 = (q_t0 + it % n_q) * kTileM;
@@ -245,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it >= kQS &&
             !__all_sync(0xFFFFFFFFu, mbar_wait(&bar[kBarQEmpty + (qs)], ((it / kQS) - 1) & 1, a.err, kErrBwdLoad)))
           break;
-        if (lane == 0) {
+        if (lane == 0 && it > 0) {  // Q(0) went out before the CTA-wide barrier
           mbar_arrive_expect_tx(&bar[kBarQFull + (qs)], kTileBytes);
           tma_rows<D>(s.q(qs), &mq, &bar[kBarQFull + (qs)], g, w.b, qn, sq.q_start, i0);
         }
@@ -256,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it >= 2 &&
             !__all_sync(0xFFFFFFFFu, mbar_wait(&bar[kBarDyEmpty + (st)], ((it >> 1) - 1) & 1, a.err, kErrBwdLoad)))
           break;
-        if (lane == 0) {
+        if (lane == 0 && it > 0) {  // so did dY(0)
           mbar_arrive_expect_tx(&bar[kBarDyFull + (st)], kTileBytes);
           tma_rows<D>(s.dy(st), &mdy, &bar[kBarDyFull + (st)], g, w.b, qn, sq.q_start, i0);
         }

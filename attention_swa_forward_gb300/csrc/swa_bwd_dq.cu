@@ -78,7 +78,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   int kv_t0, n_kv;
   key_tiles_of_query_tile(g, sq, w.tile, &kv_t0, &n_kv);
 
-  if (threadIdx.x == 0) {
+  // The producer's lane initialises the barriers and issues the loads of Q,
+  // dY and the first K and V tiles before the CTA-wide barrier, so their
+  // latency runs while TMEM is allocated.
+  if (warp == 8 && lane == 0) {
     mbar_init(&s.qdy_full, 1);
     for (int b = 0; b < 3; ++b) {
       mbar_init(&s.k_full[b], 1);
@@ -101,6 +104,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.drain_dq, 1);
     mbar_init(&s.never, 1);
     fence_mbar_init();
+    if (n_kv > 0) {
+      tma_prefetch_desc(&mq);
+      tma_prefetch_desc(&mk);
+      tma_prefetch_desc(&mv);
+      tma_prefetch_desc(&mdy);
+      mbar_arrive_expect_tx(&s.qdy_full, 2 * kTileBytes);
+      tma_rows<D>(s.q, &mq, &s.qdy_full, g, w.b, w.n, sq.q_start, q0);
+      tma_rows<D>(s.dy, &mdy, &s.qdy_full, g, w.b, w.n, sq.q_start, q0);
+      mbar_arrive_expect_tx(&s.k_full[0], kTileBytes);
+      tma_rows<D>(s.k[0], &mk, &s.k_full[0], g, w.b, hk, sq.kv_start, kv_t0 * kTileN);
+      mbar_arrive_expect_tx(&s.v_full[0], kTileBytes);
+      tma_rows<D>(s.v[0], &mv, &s.v_full[0], g, w.b, hk, sq.kv_start, kv_t0 * kTileN);
+    }
   }
   if (warp == 9) {
     tmem_alloc(&s.tmem_base, kTmemCols);
@@ -114,15 +130,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 8) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0 && n_kv > 0) {
-      tma_prefetch_desc(&mq);
-      tma_prefetch_desc(&mk);
-      tma_prefetch_desc(&mv);
-      tma_prefetch_desc(&mdy);
-      mbar_arrive_expect_tx(&s.qdy_full, 2 * kTileBytes);
-      tma_rows<D>(s.q, &mq, &s.qdy_full, g, w.b, w.n, sq.q_start, q0);
-      tma_rows<D>(s.dy, &mdy, &s.qdy_full, g, w.b, w.n, sq.q_start, q0);
-      int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
+      int k_issued = 1, v_issued = 1;  // Q, dY, K(0) and V(0) went out before the CTA-wide barrier
+      for (int j = 1; j < n_kv; ++j) {
         const int jr = (kv_t0 + j) * kTileN;
         const int kb = j % 3, vb = j & 1;
         // K(j) reuses the stage of K(j-3), free once dQ(j-3) is done

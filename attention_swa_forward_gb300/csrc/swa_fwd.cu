@@ -64,7 +64,10 @@ __global__ void __launch_bounds__(224, 1)
   int kv_t0, n_kv;
   key_tiles_of_query_tile(g, sq, w.tile, &kv_t0, &n_kv);
 
-  if (threadIdx.x == 0) {
+  // The producer's lane initialises the barriers and issues the loads of Q
+  // and the first K tile before the CTA-wide barrier, so their latency runs
+  // while TMEM is allocated.
+  if (warp == 4 && lane == 0) {
     mbar_init(&s.q_full, 1);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.k_full[i], 1);
@@ -83,6 +86,15 @@ __global__ void __launch_bounds__(224, 1)
     mbar_init(&s.drain_pv, 1);
     mbar_init(&s.never, 1);
     fence_mbar_init();
+    if (n_kv > 0) {
+      tma_prefetch_desc(&mq);
+      tma_prefetch_desc(&mk);
+      tma_prefetch_desc(&mv);
+      mbar_arrive_expect_tx(&s.q_full, kTileBytes);
+      tma_rows<D>(s.q, &mq, &s.q_full, g, w.b, w.n, sq.q_start, q0);
+      mbar_arrive_expect_tx(&s.k_full[0], kTileBytes);
+      tma_rows<D>(s.k[0], &mk, &s.k_full[0], g, w.b, hk, sq.kv_start, kv_t0 * kTileN);
+    }
   }
   if (warp == 5) {
     tmem_alloc(&s.tmem_base, kTmemCols);
@@ -96,20 +108,17 @@ __global__ void __launch_bounds__(224, 1)
   if (warp == 4) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0 && n_kv > 0) {
-      tma_prefetch_desc(&mq);
-      tma_prefetch_desc(&mk);
-      tma_prefetch_desc(&mv);
-      mbar_arrive_expect_tx(&s.q_full, kTileBytes);
-      tma_rows<D>(s.q, &mq, &s.q_full, g, w.b, w.n, sq.q_start, q0);
-      int k_issued = 0, v_issued = 0;
+      int k_issued = 1, v_issued = 0;  // Q and K(0) went out before the CTA-wide barrier
       for (int it = 0; it < n_kv; ++it) {
         const int st = it % kStages;
         const uint32_t use = it / kStages;
         const int j0 = (kv_t0 + it) * kTileN;
-        if (it >= kStages && !mbar_wait(&s.k_empty[st], (use - 1) & 1, a.err, kErrFwdLoad)) break;
-        mbar_arrive_expect_tx(&s.k_full[st], kTileBytes);
-        tma_rows<D>(s.k[st], &mk, &s.k_full[st], g, w.b, hk, sq.kv_start, j0);
-        ++k_issued;
+        if (it > 0) {
+          if (it >= kStages && !mbar_wait(&s.k_empty[st], (use - 1) & 1, a.err, kErrFwdLoad)) break;
+          mbar_arrive_expect_tx(&s.k_full[st], kTileBytes);
+          tma_rows<D>(s.k[st], &mk, &s.k_full[st], g, w.b, hk, sq.kv_start, j0);
+          ++k_issued;
+        }
         if (it >= kStages && !mbar_wait(&s.v_empty[st], (use - 1) & 1, a.err, kErrFwdLoad)) break;
         mbar_arrive_expect_tx(&s.v_full[st], kTileBytes);
         tma_rows<D>(s.v[st], &mv, &s.v_full[st], g, w.b, hk, sq.kv_start, j0);
