@@ -551,6 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bar[kBarDsFull + (st)]);
     }
     if (ok && n_q > 0) ok = compute_wait(&bar[kBarMmaDone], 0, a.err);  // every MMA done
+    // The eight compute warps agree on whether to write the epilogue: its
+    // staging barrier below must see all eight or none.
+    ok = named_barrier_and(1, kComputeThreads, ok);
     if (ok) {
       tc_fence_after_sync();
       // epilogue: thread r owns key row j0 + r; warps 0-3 write dV, 4-7 dK
@@ -558,6 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t dcol = h == 0 ? kColDV : kColDK;
       const float mul = h == 0 ? 1.f : g.scale;
       void* dbase = h == 0 ? a.dv : a.dk;
+      // dV is staged in the V buffer and dK in the K buffer (every MMA is done)
+      uint8_t* stage = h == 0 ? s.v() : s.k();
       const int64_t dst = kv_elem(g, sq, w.b, w.n, j);
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
@@ -573,10 +578,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int t = 0; t < 32; ++t) o[t] = 0.f;
         }
-        if (kv_valid) {
+        if (g.out_f32) {
+          if (kv_valid) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              if (ch * 32 + q4 * 8 < g.D) store8<F16>(dbase, dst + ch * 32 + q4 * 8, &o[q4 * 8], true);
+          }
+        } else {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
-            if (ch * 32 + q4 * 8 < g.D) store8<F16>(dbase, dst + ch * 32 + q4 * 8, &o[q4 * 8], g.out_f32);
+            if (ch * 32 + q4 * 8 < g.D) st_chunk_sw128(stage, r, ch * 4 + q4, pack8<F16>(&o[q4 * 8]));
+        }
+      }
+      if (!g.out_f32) {
+        // each warp store writes whole rows (one row per thread would touch
+        // 32 rows, 32 cache lines, per store); warps 0-3 store dV, 4-7 dK
+        named_barrier_sync(1, kComputeThreads);
+        constexpr int kChunks = D / 8;
+        constexpr int kRowsPerStore = 32 / kChunks;
+        const int c = lane % kChunks;
+        for (int rr = wq * kRowsPerStore + lane / kChunks; rr < kTileN; rr += 4 * kRowsPerStore) {
+          const int gj = j0 + rr;
+          if (gj < sq.kv_len && c * 8 < g.D)
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(dbase) + kv_elem(g, sq, w.b, w.n, gj) + c * 8) =
+                ld_chunk_sw128(stage, rr, c);
         }
       }
     }

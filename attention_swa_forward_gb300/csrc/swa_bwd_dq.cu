@@ -343,6 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&s.ds_full[b]);
     }
     if (ok && n_kv > 0) ok = compute_wait(&s.ds_free[(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1, a.err);  // every MMA done
+    // The eight compute warps agree on whether to write the epilogue: its
+    // staging barrier below must see all eight or none.
+    ok = named_barrier_and(1, kComputeThreads, ok);
     if (ok) {
       tc_fence_after_sync();
       // epilogue: dQ = scale * acc, row r, columns [h*D/2, h*D/2 + D/2)
@@ -362,10 +365,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int t = 0; t < 32; ++t) o[t] = 0.f;
         }
-        if (row_valid) {
+        if (g.out_f32) {
+          if (row_valid) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              if (h * kCols + ch * 32 + q4 * 8 < g.D) store8<F16>(a.dq, dst + ch * 32 + q4 * 8, &o[q4 * 8], true);
+          }
+        } else {
+          // staged in the Q buffer (every S is done) for whole-row stores below
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
-            if (h * kCols + ch * 32 + q4 * 8 < g.D) store8<F16>(a.dq, dst + ch * 32 + q4 * 8, &o[q4 * 8], g.out_f32);
+            if (h * kCols + ch * 32 + q4 * 8 < g.D)
+              st_chunk_sw128(s.q, r, (h * kCols + ch * 32) / 8 + q4, pack8<F16>(&o[q4 * 8]));
+        }
+      }
+      if (!g.out_f32) {
+        // each warp store writes whole rows (one row per thread would touch
+        // 32 rows, 32 cache lines, per store)
+        named_barrier_sync(1, kComputeThreads);
+        constexpr int kChunks = D / 8;
+        constexpr int kRowsPerStore = 32 / kChunks;
+        const int c = lane % kChunks;
+        for (int rr = warp * kRowsPerStore + lane / kChunks; rr < kTileM; rr += 8 * kRowsPerStore) {
+          const int gi = q0 + rr;
+          if (gi < sq.q_len && c * 8 < g.D)
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + q_elem(g, sq, w.b, w.n, gi) + c * 8) =
+                ld_chunk_sw128(s.q, rr, c);
         }
       }
     }

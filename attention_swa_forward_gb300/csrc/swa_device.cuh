@@ -170,6 +170,10 @@ __device__ __forceinline__ void st_chunk_sw128(uint8_t* tile, int r, int c, uint
   *reinterpret_cast<uint4*>(dst) = v;
 }
 
+__device__ __forceinline__ uint4 ld_chunk_sw128(const uint8_t* tile, int r, int c) {
+  return *reinterpret_cast<const uint4*>(tile + (c >> 3) * kAtomBytes + r * 128 + ((((c & 7) ^ r) & 7) << 4));
+}
+
 template <bool F16>
 __device__ __forceinline__ uint4 pack8(const float* x) {
   uint4 v;
