@@ -300,6 +300,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
   return d;
 }
 
+// The descriptor of the same matrix `bytes` further on in shared memory: the
+// start address is stored divided by 16 in the low 14 bits, and shared
+// addresses stay below 256 KB, so the field never carries into the rest.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // Instruction descriptor for kind::f16 with fp32 D and A / B both bf16
 // (f16 = false) or both fp16 (f16 = true): the two operands of one MMA
 // always share their type.

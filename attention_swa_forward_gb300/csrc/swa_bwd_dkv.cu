@@ -311,12 +311,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t k_addr = smem_u32(s.k()), v_addr = smem_u32(s.v());
       const int nk = d_steps(g);
       auto issue_ss = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {  // 128 x 128 x D, both K-major
+        const uint64_t da = sdesc_sw128(a_addr, 16, 1024), db = sdesc_sw128(b_addr, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           if (kk >= nk) break;
           const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-          umma_bf16_ss(tmem + d_col, sdesc_sw128(a_addr + off, 16, 1024), sdesc_sw128(b_addr + off, 16, 1024), kIdT,
-                       kk > 0);
+          umma_bf16_ss(tmem + d_col, sdesc_advance(da, off), sdesc_advance(db, off), kIdT, kk > 0);
         }
       };
       bool ok = mbar_wait(&bar[kBarKvFull], 0, a.err, kErrBwdMma) && mbar_wait(&bar[kBarQFull + (0)], 0, a.err, kErrBwdMma);
@@ -359,18 +359,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bar[kBarPtFull + (st)], (it >> 1) & 1, a.err, kErrBwdMma)) break;
         tc_fence_after_sync();
         const uint32_t ra = tmem + region(it);
-        const uint32_t dy_addr = smem_u32(s.dy(st)), q_addr = smem_u32(s.q(qs));
+        const uint64_t d_dy = sdesc_sw128(smem_u32(s.dy(st)), kAtomBytes, 1024);
+        const uint64_t d_q = sdesc_sw128(smem_u32(s.q(qs)), kAtomBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk)  // dV += P^T dY  (K dim = query rows)
           umma_bf16_ts(tmem + kColDV, ra + (kk >> 2) * 64 + (kk & 3) * 8,
-                       sdesc_sw128(dy_addr + kk * 2048, kAtomBytes, 1024), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
+                       sdesc_advance(d_dy, kk * 2048), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar[kBarDyEmpty + (st)]);  // dP^T(it) read dY(it) too; it finished before P^T(it) existed
         if (!mbar_wait(&bar[kBarDsFull + (st)], (it >> 1) & 1, a.err, kErrBwdMma)) break;
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk)  // dK += dS^T Q
           umma_bf16_ts(tmem + kColDK, ra + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
-                       sdesc_sw128(q_addr + kk * 2048, kAtomBytes, 1024), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
+                       sdesc_advance(d_q, kk * 2048), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar[kBarQEmpty + (qs)]);  // likewise S^T(it) for Q(it)
         umma_commit(&bar[kBarRegionFree + (st)]);
         if (it == n_it - 1) umma_commit(&bar[kBarMmaDone]);

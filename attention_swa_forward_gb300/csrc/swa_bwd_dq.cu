@@ -169,13 +169,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j > 0 && !mbar_wait(&s.s_loaded, (j - 1) & 1, a.err, kErrBwdMma)) break;
           if (!mbar_wait(&s.k_full[j % 3], (j / 3) & 1, a.err, kErrBwdMma)) break;
           tc_fence_after_sync();
-          const uint32_t k_addr = smem_u32(s.k[j % 3]);
+          const uint64_t dq_ = sdesc_sw128(q_addr, 16, 1024), dk_ = sdesc_sw128(smem_u32(s.k[j % 3]), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             if (kk >= nk) break;
             const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-            umma_bf16_ss(tmem + kColS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), kIdS,
-                         kk > 0);
+            umma_bf16_ss(tmem + kColS, sdesc_advance(dq_, off), sdesc_advance(dk_, off), kIdS, kk > 0);
           }
           umma_commit(&s.s_full);
         }
@@ -188,13 +187,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j > 0 && !mbar_wait(&s.dp_loaded, (j - 1) & 1, a.err, kErrBwdMma)) break;
           if (!mbar_wait(&s.v_full[j & 1], (j >> 1) & 1, a.err, kErrBwdMma)) break;
           tc_fence_after_sync();
-          const uint32_t v_addr = smem_u32(s.v[j & 1]);
+          const uint64_t ddy = sdesc_sw128(dy_addr, 16, 1024), dv_ = sdesc_sw128(smem_u32(s.v[j & 1]), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             if (kk >= nk) break;
             const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-            umma_bf16_ss(tmem + kColDP, sdesc_sw128(dy_addr + off, 16, 1024), sdesc_sw128(v_addr + off, 16, 1024),
-                         kIdS, kk > 0);
+            umma_bf16_ss(tmem + kColDP, sdesc_advance(ddy, off), sdesc_advance(dv_, off), kIdS, kk > 0);
           }
           umma_commit(&s.dp_full);
           umma_commit(&s.v_empty[j & 1]);
@@ -211,11 +209,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = j & 1;
         if (!mbar_wait(&s.ds_full[b], (j >> 1) & 1, a.err, kErrBwdMma)) break;
         tc_fence_after_sync();
-        const uint32_t k_addr = smem_u32(s.k[j % 3]);
+        const uint64_t dk_ = sdesc_sw128(smem_u32(s.k[j % 3]), kAtomBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)  // dQ += dS(j) K_j  (A = dS in TMEM, K dim = keys)
-          umma_bf16_ts(tmem + kColDQ, tmem + kColDS + b * 64 + kk * 8,
-                       sdesc_sw128(k_addr + kk * 2048, kAtomBytes, 1024), kIdQ, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + kColDQ, tmem + kColDS + b * 64 + kk * 8, sdesc_advance(dk_, kk * 2048), kIdQ,
+                       (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&s.ds_free[b]);
         // K(j) was also read by S(j), which finished before dS(j) existed
         umma_commit(&s.k_empty[j % 3]);

@@ -145,13 +145,12 @@ __global__ void __launch_bounds__(224, 1)
         if (it >= 2 && !mbar_wait(&s.s_free[sb], ((it >> 1) - 1) & 1, a.err, kErrFwdMma)) break;
         if (!mbar_wait(&s.k_full[st], (it / kStages) & 1, a.err, kErrFwdMma)) break;
         tc_fence_after_sync();
-        const uint32_t k_addr = smem_u32(s.k[st]);
+        const uint64_t dq_ = sdesc_sw128(q_addr, 16, 1024), dk_ = sdesc_sw128(smem_u32(s.k[st]), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           if (kk >= nk) break;
           const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-          umma_bf16_ss(tmem + sb * kTileN, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                       kIdS, kk > 0);
+          umma_bf16_ss(tmem + sb * kTileN, sdesc_advance(dq_, off), sdesc_advance(dk_, off), kIdS, kk > 0);
         }
         umma_commit(&s.s_full[sb]);
         umma_commit(&s.k_empty[st]);
@@ -168,11 +167,11 @@ __global__ void __launch_bounds__(224, 1)
         if (!mbar_wait(&s.p_full[pb], (it >> 1) & 1, a.err, kErrFwdMma)) break;
         if (!mbar_wait(&s.v_full[st], (it / kStages) & 1, a.err, kErrFwdMma)) break;
         tc_fence_after_sync();
-        const uint32_t v_addr = smem_u32(s.v[st]);
+        const uint64_t dv_ = sdesc_sw128(smem_u32(s.v[st]), kAtomBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)  // O += P V  (A = P in TMEM)
-          umma_bf16_ts(tmem + kColO, tmem + kColP + pb * 64 + kk * 8, sdesc_sw128(v_addr + kk * 2048, kAtomBytes, 1024),
-                       kIdO, (it > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + kColO, tmem + kColP + pb * 64 + kk * 8, sdesc_advance(dv_, kk * 2048), kIdO,
+                       (it > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&s.o_done[pb]);
         umma_commit(&s.v_empty[st]);
       }
