@@ -128,6 +128,7 @@ swa_status_t make_plan(const swa_params_t* p, Plan& plan) {
   g.scale = static_cast<float>(p->scale);
   g.scale_log2 = static_cast<float>(p->scale * kLog2e);
   g.inv_keep = static_cast<float>(1.0 / p->keep_prob);
+  g.keep = static_cast<float>(p->keep_prob);
   if (p->dtype != SWA_DTYPE_BF16 && p->dtype != SWA_DTYPE_FP16 && p->dtype != SWA_DTYPE_FP32)
     return fail(SWA_ERR_PARAM_INVALID, "dtype should be 0 (bf16), 1 (fp16) or 2 (fp32), got %d", p->dtype);
   // fp32: the kernels run on bf16 copies of the inputs made in the workspace

@@ -6,6 +6,9 @@
 //   S^T  = K Q^T                    P^T = exp2(S^T*scale*log2e - lse2)  (recomputed)
 //   dP^T = V dY^T                   dS^T = P^T * (dP^T * z/keep - D)
 //   dV  += (P * z/keep)^T dY        dK  += dS^T Q  (x scale at the end)
+// With dropout the 1/keep factor leaves the per-element work: the tiles carry
+// (P*z)^T and P^T * (z*dP^T - keep*D), and the epilogues multiply dV by 1/keep
+// and dK by scale/keep.
 // lse2 = softmax_max*log2e + log2(softmax_sum) and D = rowsum(dY*O) come from
 // the preprocess kernel.  dQ is computed by the query-major pass
 // (swa_bwd_dq.cu), so nothing here accumulates through global memory.
@@ -280,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t si = ws_stat_index(g, sq, w.b, qn, i);
             l2 = a.lse2[si];
             dd = a.dsum[si];
+            if constexpr (DROP) dd *= g.keep;  // the compute warps form P * (z dP - keep D)
             if constexpr (DM == 1) load_keep_bits(a.mask, sq, qn, i, j0, bits);
           }
           s.lse2(st)[c] = l2;
@@ -480,35 +484,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!compute_wait(&bar[kBarDpFull], it & 1, a.err)) { ok = false; break; }
       tc_fence_after_sync();
       {
-        // this thread's keep bits of the tile: bit t = (query cbase + t, key r)
+        // this thread's keep bits of the tile: bit t = (query cbase + t, key r).
+        // The stage holds them query-major (word wq of query c: keys
+        // 32 wq .. 32 wq + 31); lane l fetches query cbase + l's word and a
+        // warp transpose hands lane k the bits of key 32 wq + k.
         uint32_t km[2] = {~0u, ~0u};
         if constexpr (DROP) {
-          km[0] = km[1] = 0u;
-#pragma unroll
-          for (int t = 0; t < 64; ++t) km[t >> 5] |= ((s.keep(st)[(cbase + t) * 4 + (wq)] >> lane) & 1u) << (t & 31);
+          km[0] = warp_transpose_bits(s.keep(st)[(cbase + lane) * 4 + wq], lane);
+          km[1] = warp_transpose_bits(s.keep(st)[(cbase + 32 + lane) * 4 + wq], lane);
         }
-        // dS^T = P^T * (dP^T * z / keep - D) for the 32 query columns of one half
+        // dS^T = P^T * (dP^T * z / keep - D) for the 32 query columns of one
+        // half.  With dropout the loop forms P^T * (z dP^T - keep D), 1/keep
+        // times dS^T, and the dK epilogue takes the 1/keep (the staged D
+        // already holds keep D).
         auto ds_half = [&](int half, const uint32_t (&d)[32], uint32_t* dk) {
 #pragma unroll
           for (int t4 = 0; t4 < 8; ++t4) {
             const int tb = half * 32 + t4 * 4;
             const float4 d4 = *reinterpret_cast<const float4*>(&s.dsum(st)[cbase + tb]);
             const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-            float dsv[4];
-            if constexpr (DROP) {
+            float dp[4], dsv[4];
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int t = tb + u;
-                float dp = __uint_as_float(d[t4 * 4 + u]);
-                dp = ((km[t >> 5] >> (t & 31)) & 1u) ? dp * g.inv_keep : 0.f;
-                dsv[u] = p[t] * (dp - dv4[u]);
-              }
-            } else {
-#pragma unroll
-              for (int u = 0; u < 4; u += 2)  // packed pairs
-                fmulsub2(dsv[u], dsv[u + 1], p[tb + u], p[tb + u + 1], __uint_as_float(d[t4 * 4 + u]),
-                         __uint_as_float(d[t4 * 4 + u + 1]), dv4[u], dv4[u + 1]);
+            for (int u = 0; u < 4; ++u) {
+              const int t = tb + u;
+              dp[u] = __uint_as_float(d[t4 * 4 + u]);
+              if constexpr (DROP) dp[u] = ((km[t >> 5] >> (t & 31)) & 1u) ? dp[u] : 0.f;
             }
+#pragma unroll
+            for (int u = 0; u < 4; u += 2)  // packed pairs
+              fmulsub2(dsv[u], dsv[u + 1], p[tb + u], p[tb + u + 1], dp[u], dp[u + 1], dv4[u], dv4[u + 1]);
             dk[t4 * 2] = pack2<F16>(dsv[0], dsv[1]);
             dk[t4 * 2 + 1] = pack2<F16>(dsv[2], dsv[3]);
           }
@@ -518,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t d[32];  // dP^T columns [cbase, cbase + 32): read before P^T goes over them
           tmem_ld_32x32b_x32(col, d);
           tmem_ld_wait(d);
-          // P^T * z / keep first, so dV can start
+          // P^T * z first, so dV can start (the dV epilogue takes the 1/keep)
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             uint32_t pk[16];
@@ -527,8 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int t = half * 32 + 2 * t2;
               float p0 = p[t], p1 = p[t + 1];
               if constexpr (DROP) {
-                p0 = ((km[t >> 5] >> (t & 31)) & 1u) ? p0 * g.inv_keep : 0.f;
-                p1 = ((km[(t + 1) >> 5] >> ((t + 1) & 31)) & 1u) ? p1 * g.inv_keep : 0.f;
+                p0 = ((km[t >> 5] >> (t & 31)) & 1u) ? p0 : 0.f;
+                p1 = ((km[(t + 1) >> 5] >> ((t + 1) & 31)) & 1u) ? p1 : 0.f;
               }
               pk[t2] = pack2<F16>(p0, p1);
             }
@@ -560,7 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // epilogue: thread r owns key row j0 + r; warps 0-3 write dV, 4-7 dK
       const bool kv_valid = j < sq.kv_len;
       const uint32_t dcol = h == 0 ? kColDV : kColDK;
-      const float mul = h == 0 ? 1.f : g.scale;
+      // the 1/keep of dropout left out of P^T z and dS^T (exactly 1 without dropout)
+      const float mul = h == 0 ? g.inv_keep : g.scale * g.inv_keep;
       void* dbase = h == 0 ? a.dv : a.dk;
       // dV is staged in the V buffer and dK in the K buffer (every MMA is done)
       uint8_t* stage = h == 0 ? s.v() : s.k();

@@ -4,6 +4,8 @@
 // "反向公式", the dQ row of the formulas):
 //   S  = Q K^T,  P = exp2(S*scale*log2e - lse2),  dP = dY V^T,
 //   dS = P * (dP * z/keep - D),  dQ += dS K,  dQ = scale * dQ at the end.
+// With dropout the tiles carry P * (z*dP - keep*D), 1/keep times dS, and the
+// epilogue multiplies by scale/keep instead.
 // dQ accumulates in TMEM over the key tiles of the band and is written once:
 // no accumulation through global memory (the measured fp32 reduce-add ceiling
 // of the L2 would otherwise bound the backward), and the result is
@@ -237,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t si = ws_stat_index(g, sq, w.b, w.n, i);
       lse2 = a.lse2[si];
       drow = a.dsum[si];
+      if constexpr (DM != 0) drow *= g.keep;  // the loop forms P * (z dP - keep D)
     }
     // keep bits of this thread's 64 key columns of key tile j (two words)
     auto fetch_bits = [&](int j, uint32_t& kb0, uint32_t& kb1) {
@@ -313,23 +316,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait(d1);
         tc_fence_before_sync();
         mbar_arrive(&s.dp_loaded);
+        // dS = P * (dP - D), packed pairs; with dropout P * (z dP - keep D),
+        // 1/keep times dS, the epilogue taking the 1/keep
 #pragma unroll
         for (int t2 = 0; t2 < 32; ++t2) {
-          float dv[2];
+          const int t = 2 * t2;
+          float dp0 = __uint_as_float(t < 32 ? d0[t] : d1[t - 32]);
+          float dp1 = __uint_as_float(t + 1 < 32 ? d0[t + 1] : d1[t - 31]);
           if (DM != 0) {
-#pragma unroll
-            for (int uu = 0; uu < 2; ++uu) {
-              const int t = 2 * t2 + uu;
-              float dp = __uint_as_float(t < 32 ? d0[t] : d1[t - 32]);
-              const bool keep = ((t < 32 ? kb0 : kb1) >> (t & 31)) & 1u;
-              dp = keep ? dp * g.inv_keep : 0.f;
-              dv[uu] = p[t] * (dp - drow);
-            }
-          } else {  // dS = P * (dP - D), packed pair
-            const int t = 2 * t2;
-            fmulsub2(dv[0], dv[1], p[t], p[t + 1], __uint_as_float(t < 32 ? d0[t] : d1[t - 32]),
-                     __uint_as_float(t + 1 < 32 ? d0[t + 1] : d1[t - 31]), drow, drow);
+            dp0 = (((t < 32 ? kb0 : kb1) >> (t & 31)) & 1u) ? dp0 : 0.f;
+            dp1 = (((t + 1 < 32 ? kb0 : kb1) >> ((t + 1) & 31)) & 1u) ? dp1 : 0.f;
           }
+          float dv[2];
+          fmulsub2(dv[0], dv[1], p[t], p[t + 1], dp0, dp1, drow, drow);
           dk[t2] = pack2<F16>(dv[0], dv[1]);
         }
       }
@@ -346,7 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = named_barrier_and(1, kComputeThreads, ok);
     if (ok) {
       tc_fence_after_sync();
-      // epilogue: dQ = scale * acc, row r, columns [h*D/2, h*D/2 + D/2)
+      // epilogue: dQ = scale / keep * acc, row r, columns [h*D/2, h*D/2 + D/2)
+      const float mul = g.scale * g.inv_keep;
       constexpr int kCols = D / 2;
       const int64_t dst = q_elem(g, sq, w.b, w.n, i) + h * kCols;
 #pragma unroll
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_32x32b_x32(tmem + lane_off + kColDQ + h * kCols + ch * 32, t32);
           tmem_ld_wait(t32);
 #pragma unroll
-          for (int t = 0; t < 32; ++t) o[t] = __uint_as_float(t32[t]) * g.scale;
+          for (int t = 0; t < 32; ++t) o[t] = __uint_as_float(t32[t]) * mul;
         } else {
 #pragma unroll
           for (int t = 0; t < 32; ++t) o[t] = 0.f;

@@ -174,6 +174,24 @@ __device__ __forceinline__ uint4 ld_chunk_sw128(const uint8_t* tile, int r, int 
   return *reinterpret_cast<const uint4*>(tile + (c >> 3) * kAtomBytes + r * 128 + ((((c & 7) ^ r) & 7) << 4));
 }
 
+// 32 x 32 bit-matrix transpose across a warp (all 32 lanes converged).  On
+// entry lane l holds row l of the matrix (bit k = element (l, k)); on exit
+// lane k holds column k (bit l = element (l, k)).  Transposing swaps each bit
+// of the row index with the same bit of the column index; stage j swaps bit j,
+// which trades the two off-diagonal j x j blocks of every 2j x 2j block
+// between lane pairs l, l ^ j.
+__device__ __forceinline__ uint32_t warp_transpose_bits(uint32_t x, int lane) {
+  constexpr uint32_t kLowCols[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int s = 0; s < 5; ++s) {
+    const int j = 16 >> s;
+    const uint32_t m = kLowCols[s];  // the columns whose bit j is clear
+    const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, x, j);
+    x = (lane & j) ? ((x & ~m) | ((y >> j) & m)) : ((x & m) | ((y << j) & ~m));
+  }
+  return x;
+}
+
 template <bool F16>
 __device__ __forceinline__ uint4 pack8(const float* x) {
   uint4 v;

@@ -98,6 +98,7 @@ struct Geometry {
   float scale;        // score scale
   float scale_log2;   // scale * log2(e)
   float inv_keep;     // 1 / keep_prob
+  float keep;         // keep_prob
   int32_t has_mask;   // dropout active (a drop_mask, or generated from seed / offset)
   int32_t drop_gen;   // 1: keep bits generated from (seed, offset) instead of read
   uint32_t seed_lo, seed_hi, off_lo;
