@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = 0; u < 4; ++u) {
               const int t = tb + u;
               dp[u] = __uint_as_float(d[t4 * 4 + u]);
-              if constexpr (DROP) dp[u] = ((km[t >> 5] >> (t & 31)) & 1u) ? dp[u] : 0.f;
+              if constexpr (DROP) dp[u] = keep_or_zero(dp[u], km[t >> 5], t & 31);
             }
 #pragma unroll
             for (int u = 0; u < 4; u += 2)  // packed pairs
@@ -531,8 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int t = half * 32 + 2 * t2;
               float p0 = p[t], p1 = p[t + 1];
               if constexpr (DROP) {
-                p0 = ((km[t >> 5] >> (t & 31)) & 1u) ? p0 : 0.f;
-                p1 = ((km[(t + 1) >> 5] >> ((t + 1) & 31)) & 1u) ? p1 : 0.f;
+                p0 = keep_or_zero(p0, km[t >> 5], t & 31);
+                p1 = keep_or_zero(p1, km[(t + 1) >> 5], (t + 1) & 31);
               }
               pk[t2] = pack2<F16>(p0, p1);
             }

@@ -174,6 +174,13 @@ __device__ __forceinline__ uint4 ld_chunk_sw128(const uint8_t* tile, int r, int 
   return *reinterpret_cast<const uint4*>(tile + (c >> 3) * kAtomBytes + r * 128 + ((((c & 7) ^ r) & 7) << 4));
 }
 
+// x where bit b of w is set, +0 where it is clear: the bit, moved to the
+// sign position and sign-extended, masks x (no predicate, no select).
+__device__ __forceinline__ float keep_or_zero(float x, uint32_t w, int b) {
+  const uint32_t m = static_cast<uint32_t>(static_cast<int32_t>(w << (31 - b)) >> 31);
+  return __uint_as_float(__float_as_uint(x) & m);
+}
+
 // 32 x 32 bit-matrix transpose across a warp (all 32 lanes converged).  On
 // entry lane l holds row l of the matrix (bit k = element (l, k)); on exit
 // lane k holds column k (bit l = element (l, k)).  Transposing swaps each bit
