@@ -170,27 +170,37 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
     uint8_t* d = base + static_cast<size_t>(c) * L.chunk_bytes;
     cudaStream_t comp = s_comp[c & 1];
     const swa_stream_t comp_h = reinterpret_cast<swa_stream_t>(comp);
-    cudaEvent_t in_done = nullptr, comp_done = nullptr;
-    if ((e = event(&in_done)) != cudaSuccess || (e = event(&comp_done)) != cudaSuccess) break;
+    // The forward needs q, k, v only: it starts while dy is still being
+    // copied.  out and the statistics are final after the forward and go
+    // back while the backward runs.  (This shortens the pipeline's fill by
+    // the first chunk's dy and its drain by the last chunk's out.)
+    cudaEvent_t qkv_done = nullptr, dy_done = nullptr, fwd_done = nullptr, comp_done = nullptr;
+    if ((e = event(&qkv_done)) != cudaSuccess || (e = event(&dy_done)) != cudaSuccess ||
+        (e = event(&fwd_done)) != cudaSuccess || (e = event(&comp_done)) != cudaSuccess)
+      break;
     if ((e = copy_in(L.q, c, d + L.q_off, q, s_in)) != cudaSuccess) break;
     if ((e = copy_in(L.kv, c, d + L.k_off, k, s_in)) != cudaSuccess) break;
     if ((e = copy_in(L.kv, c, d + L.v_off, v, s_in)) != cudaSuccess) break;
+    if ((e = cudaEventRecord(qkv_done, s_in)) != cudaSuccess) break;
     if ((e = copy_in(L.q, c, d + L.dy_off, dy, s_in)) != cudaSuccess) break;
-    if ((e = cudaEventRecord(in_done, s_in)) != cudaSuccess) break;
-    if ((e = cudaStreamWaitEvent(comp, in_done, 0)) != cudaSuccess) break;
+    if ((e = cudaEventRecord(dy_done, s_in)) != cudaSuccess) break;
+    if ((e = cudaStreamWaitEvent(comp, qkv_done, 0)) != cudaSuccess) break;
     st = swa_forward(&L.sub, d + L.q_off, d + L.k_off, d + L.v_off, nullptr, d + L.out_off,
                      reinterpret_cast<float*>(d + L.smax_off), reinterpret_cast<float*>(d + L.ssum_off),
                      d + L.fws_off, L.fws_bytes, comp_h);
     if (st != SWA_OK) break;
+    if ((e = cudaEventRecord(fwd_done, comp)) != cudaSuccess) break;
+    if ((e = cudaStreamWaitEvent(s_out, fwd_done, 0)) != cudaSuccess) break;
+    if ((e = copy_out(L.q, c, out, d + L.out_off, s_out)) != cudaSuccess) break;
+    if ((e = copy_out(L.st, c, softmax_max, d + L.smax_off, s_out)) != cudaSuccess) break;
+    if ((e = copy_out(L.st, c, softmax_sum, d + L.ssum_off, s_out)) != cudaSuccess) break;
+    if ((e = cudaStreamWaitEvent(comp, dy_done, 0)) != cudaSuccess) break;
     st = swa_backward(&L.sub, d + L.q_off, d + L.k_off, d + L.v_off, d + L.dy_off, d + L.out_off,
                       reinterpret_cast<const float*>(d + L.smax_off), reinterpret_cast<const float*>(d + L.ssum_off),
                       nullptr, d + L.dq_off, d + L.dk_off, d + L.dv_off, d + L.bws_off, L.bws_bytes, comp_h);
     if (st != SWA_OK) break;
     if ((e = cudaEventRecord(comp_done, comp)) != cudaSuccess) break;
     if ((e = cudaStreamWaitEvent(s_out, comp_done, 0)) != cudaSuccess) break;
-    if ((e = copy_out(L.q, c, out, d + L.out_off, s_out)) != cudaSuccess) break;
-    if ((e = copy_out(L.st, c, softmax_max, d + L.smax_off, s_out)) != cudaSuccess) break;
-    if ((e = copy_out(L.st, c, softmax_sum, d + L.ssum_off, s_out)) != cudaSuccess) break;
     if ((e = copy_out(L.q, c, dq, d + L.dq_off, s_out)) != cudaSuccess) break;
     if ((e = copy_out(L.kv, c, dk, d + L.dk_off, s_out)) != cudaSuccess) break;
     if ((e = copy_out(L.kv, c, dv, d + L.dv_off, s_out)) != cudaSuccess) break;
