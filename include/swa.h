@@ -188,7 +188,11 @@ SWA_API swa_status_t swa_backward(const swa_params_t *p, const void *q, const vo
  * SWA_ERR_WORKSPACE.  Every call looks up the array's device address in the
  * current context (cudaGetSymbolAddress), so an address never outlives its
  * context; the first lookup on a device may load the library's device code,
- * so make the first call before any stream capture.  All calls on a device
+ * so make the first call before any stream capture.  The library carries its
+ * own copy of the CUDA runtime (linked statically): do not reset the device
+ * (cudaDeviceReset, or a primary-context reset through the driver) between
+ * calls while the library stays loaded, since whether its runtime then
+ * reloads its device code is not specified.  All calls on a device
  * share the array and
  * each call clears what must start at zero, so calls whose kernels overlap on
  * the GPU (concurrent streams, other threads) race and must be serialised by
