@@ -43,7 +43,19 @@ namespace {
 constexpr int kThreads = 352;
 constexpr int kComputeThreads = 256;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColDV = 256;
+
+// TMEM plan: kRegions 128-column regions, each holding one query tile's S^T,
+// then dP^T, then P^T / dS^T; dV and dK after them.  At D = 128 the two
+// accumulators take 256 columns and two regions fit; at D <= 64 a third
+// region fits, so S^T(i+1) waits for dK(i-2) to release its region instead
+// of dK(i-1).
+template <int D>
+struct DkvTmem {
+  static constexpr int kRegions = D <= 64 ? 3 : 2;
+  static constexpr uint32_t kColDV = kRegions * 128u;
+  static constexpr uint32_t kColDK = kColDV + D;
+  static_assert(kColDK + D <= kTmemCols, "TMEM plan");
+};
 constexpr size_t kMaxSmem = 232448;
 
 // mbarrier slots
@@ -55,11 +67,11 @@ enum : int {
   kBarDyEmpty = 9,     // [2]
   kBarStatFull = 11,   // [2]
   kBarGenFull = 13,    // [2] generated keep bits of the tile in that stage written (compute threads)
-  kBarSFull = 15,      // [2] per region: the two issuers hand off there, so no waiter is a phase behind
-  kBarPtFull = 17,     // [2]
-  kBarDsFull = 19,     // [2]
-  kBarRegionFree = 21, // [2]
-  kBarSLoaded = 23,
+  kBarSFull = 15,      // [3] per region: the two issuers hand off there, so no waiter is a phase behind
+  kBarPtFull = 18,     // [3]
+  kBarDsFull = 21,     // [3]
+  kBarRegionFree = 24, // [3]
+  kBarSLoaded = 27,
   kBarDpFull,
   kBarMmaDone,
   kBarDrainSdp,
@@ -162,7 +174,11 @@ struct DkvSmem {
 __device__ __forceinline__ bool compute_wait(uint64_t* bar, uint32_t parity, int* err) {
   return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, err, kErrBwdCompute));
 }
-__device__ __forceinline__ uint32_t region(int it) { return (it & 1) * 128u; }
+// Region of step it, and the phase parity of its per-region barriers.
+template <int R>
+__device__ __forceinline__ int region_of(int it) { return it % R; }
+template <int R>
+__device__ __forceinline__ uint32_t region_phase(int it) { return static_cast<uint32_t>((it / R) & 1); }
 
 template <int D, int DM, bool F16, int CAP>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -176,7 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const DkvSmem<D, DROP> s(smem_raw);
   uint64_t* const bar = s.bar;
-  constexpr uint32_t kColDK = kColDV + D;
+  constexpr int kR = DkvTmem<D>::kRegions;
+  constexpr uint32_t kColDV = DkvTmem<D>::kColDV, kColDK = DkvTmem<D>::kColDK;
+  auto region = [](int it) { return static_cast<uint32_t>(region_of<kR>(it)) * 128u; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Geometry& g = a.g;
   const Item w = resolve_item(tab, a.g, static_cast<int>(blockIdx.x), a.g.N_kv);  // w.n: key/value head
@@ -206,11 +224,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar[kBarDyEmpty + (st)], 1);
       mbar_init(&bar[kBarStatFull + (st)], 32);
       mbar_init(&bar[kBarGenFull + (st)], kComputeThreads);
-      mbar_init(&bar[kBarSFull + (st)], 1);
     }
     mbar_init(&bar[kBarSLoaded], kComputeThreads);
     mbar_init(&bar[kBarDpFull], 1);
-    for (int r = 0; r < 2; ++r) {
+    for (int r = 0; r < kR; ++r) {
+      mbar_init(&bar[kBarSFull + (r)], 1);
       mbar_init(&bar[kBarPtFull + (r)], kComputeThreads);
       mbar_init(&bar[kBarDsFull + (r)], kComputeThreads);
       mbar_init(&bar[kBarRegionFree + (r)], 1);
@@ -261,8 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_rows<D>(s.q(qs), &mq, &bar[kBarQFull + (qs)], g, w.b, qn, sq.q_start, i0);
         }
         ++q_issued;
-        // dY and the statistics reuse stage (it & 1) once dV(it - 2) is done,
-        // which also means the compute warps are through with tile it - 2
+        // dY reuses stage (it & 1) once dV(it - 2), its last reader, is done
         const int st = it & 1;
         if (it >= 2 &&
             !__all_sync(0xFFFFFFFFu, mbar_wait(&bar[kBarDyEmpty + (st)], ((it >> 1) - 1) & 1, a.err, kErrBwdLoad)))
@@ -272,25 +289,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_rows<D>(s.dy(st), &mdy, &bar[kBarDyFull + (st)], g, w.b, qn, sq.q_start, i0);
         }
         ++dy_issued;
-        // per-query statistics (and keep bits) of this tile: 4 rows per lane
+        // per-query statistics (and keep bits) of this tile, 4 rows per lane:
+        // loaded into registers first, then written into stage (it & 1) once
+        // the compute warps have stored dS^T(it - 2).  That is their last read
+        // of the stage (D is read while dS^T is formed, after dV(it - 2) may
+        // already have finished), and the barrier cannot run a phase ahead:
+        // its next phase needs a tile whose statistics are not written yet.
+        float l2[4], dd[4];
+        uint32_t bits[4][4];
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int i = i0 + lane * 4 + k4;
+          l2[k4] = INFINITY;
+          dd[k4] = 0.f;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) bits[k4][q4] = 0u;
+          if (i < sq.q_len) {
+            const int64_t si = ws_stat_index(g, sq, w.b, qn, i);
+            l2[k4] = a.lse2[si];
+            dd[k4] = a.dsum[si];
+            if constexpr (DROP) dd[k4] *= g.keep;  // the compute warps form P * (z dP - keep D)
+            if constexpr (DM == 1) load_keep_bits(a.mask, sq, qn, i, j0, bits[k4]);
+          }
+        }
+        if (it >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait(&bar[kBarDsFull + region_of<kR>(it - 2)],
+                                                         region_phase<kR>(it - 2), a.err, kErrBwdLoad)))
+          break;
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
           const int c = lane * 4 + k4;
-          const int i = i0 + c;
-          float l2 = INFINITY, dd = 0.f;
-          uint32_t bits[4] = {0u, 0u, 0u, 0u};
-          if (i < sq.q_len) {
-            const int64_t si = ws_stat_index(g, sq, w.b, qn, i);
-            l2 = a.lse2[si];
-            dd = a.dsum[si];
-            if constexpr (DROP) dd *= g.keep;  // the compute warps form P * (z dP - keep D)
-            if constexpr (DM == 1) load_keep_bits(a.mask, sq, qn, i, j0, bits);
-          }
-          s.lse2(st)[c] = l2;
-          s.dsum(st)[c] = dd;
+          s.lse2(st)[c] = l2[k4];
+          s.dsum(st)[c] = dd[k4];
           if constexpr (DM == 1) {
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) s.keep(st)[(c) * 4 + (q4)] = bits[q4];
+            for (int q4 = 0; q4 < 4; ++q4) s.keep(st)[(c) * 4 + (q4)] = bits[k4][q4];
           }
         }
         mbar_arrive(&bar[kBarStatFull + (st)]);
@@ -338,13 +370,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_ss(region(it), v_addr, smem_u32(s.dy(st)));  // dP^T = V dY^T
         umma_commit(&bar[kBarDpFull]);
         if (it + 1 < n_it) {
-          // S^T(it+1) into the other region, once dK(it-1) has read it
-          if (it >= 1 && !mbar_wait(&bar[kBarRegionFree + ((it - 1) & 1)], ((it - 1) >> 1) & 1, a.err, kErrBwdMma)) break;
+          // S^T(it+1) into its region, once dK(it+1-kR) has read it
+          if (it + 1 >= kR && !mbar_wait(&bar[kBarRegionFree + region_of<kR>(it + 1 - kR)],
+                                         region_phase<kR>(it + 1 - kR), a.err, kErrBwdMma))
+            break;
           const int nq = (it + 1) % kQS;
           if (!mbar_wait(&bar[kBarQFull + (nq)], ((it + 1) / kQS) & 1, a.err, kErrBwdMma)) break;
           tc_fence_after_sync();
           issue_ss(region(it + 1), k_addr, smem_u32(s.q(nq)));
-          umma_commit(&bar[kBarSFull + ((it + 1) & 1)]);
+          umma_commit(&bar[kBarSFull + region_of<kR>(it + 1)]);
         }
       }
       umma_commit(&bar[kBarDrainSdp]);
@@ -360,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // query columns [64h, 64h+64) of the tile hold P^T in columns
         // [64h, 64h+32) and dS^T in [64h+32, 64h+64), two bf16 per column.
         // P^T is stored first, so dV(it) runs while dS^T is computed.
-        if (!mbar_wait(&bar[kBarPtFull + (st)], (it >> 1) & 1, a.err, kErrBwdMma)) break;
+        if (!mbar_wait(&bar[kBarPtFull + region_of<kR>(it)], region_phase<kR>(it), a.err, kErrBwdMma)) break;
         tc_fence_after_sync();
         const uint32_t ra = tmem + region(it);
         const uint64_t d_dy = sdesc_sw128(smem_u32(s.dy(st)), kAtomBytes, 1024);
@@ -370,14 +404,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16_ts(tmem + kColDV, ra + (kk >> 2) * 64 + (kk & 3) * 8,
                        sdesc_advance(d_dy, kk * 2048), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar[kBarDyEmpty + (st)]);  // dP^T(it) read dY(it) too; it finished before P^T(it) existed
-        if (!mbar_wait(&bar[kBarDsFull + (st)], (it >> 1) & 1, a.err, kErrBwdMma)) break;
+        if (!mbar_wait(&bar[kBarDsFull + region_of<kR>(it)], region_phase<kR>(it), a.err, kErrBwdMma)) break;
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk)  // dK += dS^T Q
           umma_bf16_ts(tmem + kColDK, ra + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
                        sdesc_advance(d_q, kk * 2048), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar[kBarQEmpty + (qs)]);  // likewise S^T(it) for Q(it)
-        umma_commit(&bar[kBarRegionFree + (st)]);
+        umma_commit(&bar[kBarRegionFree + region_of<kR>(it)]);
         if (it == n_it - 1) umma_commit(&bar[kBarMmaDone]);
       }
       umma_commit(&bar[kBarDrainKv]);
@@ -426,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i0 = (q_t0 + it % n_q) * kTileM;
       const bool full = tile_fully_visible(g, sq, i0, j0);
       const uint32_t col = tmem + lane_off + region(it) + cbase;
-      if (!compute_wait(&bar[kBarSFull + (st)], (it >> 1) & 1, a.err)) { ok = false; break; }
+      if (!compute_wait(&bar[kBarSFull + region_of<kR>(it)], region_phase<kR>(it), a.err)) { ok = false; break; }
       if (!compute_wait(&bar[kBarStatFull + (st)], (it >> 1) & 1, a.err)) { ok = false; break; }
       tc_fence_after_sync();
       // ---- S^T -> P^T (registers)
@@ -476,7 +510,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- next tile's generated keep bits, into the stage tile it-1 used
       // once every thread is through with tile it-1 (its ds_full)
       if (DM == 2 && it + 1 < n_it) {
-        if (it >= 1 && !compute_wait(&bar[kBarDsFull + ((it - 1) & 1)], ((it - 1) >> 1) & 1, a.err)) { ok = false; break; }
+        if (it >= 1 &&
+            !compute_wait(&bar[kBarDsFull + region_of<kR>(it - 1)], region_phase<kR>(it - 1), a.err)) {
+          ok = false;
+          break;
+        }
         gen_tile_bits(it + 1);
       }
       // ---- dP^T -> dS^T; P^T*z/keep and dS^T packed bf16 into the same columns
@@ -540,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st_wait();
           tc_fence_before_sync();
-          mbar_arrive(&bar[kBarPtFull + (st)]);
+          mbar_arrive(&bar[kBarPtFull + region_of<kR>(it)]);
           ds_half(0, d, dk);
         }
         {
@@ -553,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&bar[kBarDsFull + (st)]);
+      mbar_arrive(&bar[kBarDsFull + region_of<kR>(it)]);
     }
     if (ok && n_q > 0) ok = compute_wait(&bar[kBarMmaDone], 0, a.err);  // every MMA done
     // The eight compute warps agree on whether to write the epilogue: its
