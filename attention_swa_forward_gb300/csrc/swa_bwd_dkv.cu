@@ -21,12 +21,13 @@
 //              and each tile's per-query lse2 / D (and dropout bits) into shared
 //   warp  9    tcgen05 issuer of S^T and dP^T (SS)
 //   warp 10    tcgen05 issuer of dV and dK (TS)
-// TMEM: two 128-column regions R0, R1, dV [256,256+D), dK [256+D,256+2D).
-// Query tile i lives in R(i%2): S^T(i) is computed there; once every thread has
-// it in registers, dP^T(i) is computed over it; each thread then stores its
-// P^T / dS^T (bf16) into the very columns it read, and dV / dK take them as
-// the TMEM A operand.  Issue order per tile: dP^T(i), S^T(i+1) (into the other
-// region, once dK(i-1) has finished reading it), dV(i), dK(i): the tensor pipe
+// TMEM: R 128-column regions (R = 2 at D = 128, 3 at D <= 64), then dV and
+// dK (DkvTmem).  Query tile i lives in region i % R: S^T(i) is computed there;
+// once every thread has it in registers, dP^T(i) is computed over it; each
+// thread then stores its P^T / dS^T (bf16) into the very columns it read, and
+// dV / dK take them as the TMEM A operand.  Issue order per tile: dP^T(i),
+// S^T(i+1) (into its region, once dK(i+1-R) has finished reading it), dV(i),
+// dK(i): the tensor pipe
 // always has the next GEMM queued while the compute warps work.  Two issuing
 // threads keep it fed: its queue is shallow, so every barrier wait of a
 // single issuer between GEMMs left it idle.
