@@ -610,8 +610,6 @@ swa_status_t swa_workspace_status(const void* workspace, swa_stream_t stream) {
   int32_t word = 0;
   e = cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "reading the workspace header");
-  if (word == swa::kErrSmemAlign)
-    return fail(SWA_ERR_CUDA, "a kernel found its dynamic shared memory not 1024-byte aligned and did no work");
   if (word != 0) return fail(SWA_ERR_TIMEOUT, "a kernel gave up a bounded wait (code %d)", word);
   return SWA_OK;
 }

@@ -83,7 +83,6 @@ enum : int32_t {
   kErrBwdLoad = 11,
   kErrBwdMma = 12,
   kErrBwdCompute = 13,
-  kErrSmemAlign = 21,  // dynamic shared memory base not 1024-byte aligned
 };
 
 struct Geometry {
