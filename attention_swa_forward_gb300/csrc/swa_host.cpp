@@ -2,7 +2,8 @@
 // and outputs live in host memory, with the host <-> device copies overlapped
 // with the computation.
 //
-// The heads are split into `chunks` equal groups.  Each group is a complete
+// The heads are split into `chunks` equal groups (the first and the last
+// split once more in two, see StepPlan).  Each group is a complete
 // smaller problem (heads are independent in every step of the method), so it
 // is copied into its own compact device tensors, computed by swa_forward and
 // swa_backward, and copied back.  Chunk c+1's inputs travel host -> device on
@@ -96,6 +97,45 @@ swa_status_t make_layout(const swa_params_t* p, int chunks, Layout& L) {
   return SWA_OK;
 }
 
+// The pipeline's units: head groups of N / chunks heads, except that the
+// first and the last group are each split into two halves when 2 * chunks
+// divides N and N_kv.  The pipeline's fill (the first unit's inputs) and
+// drain (the last unit's results) then move half as many bytes.  Units are
+// packed back to back in the device buffer.
+struct Unit {
+  const Layout* L;
+  int group;   // head group index within L's split
+  size_t off;  // byte offset of the unit's region in the device buffer
+};
+struct StepPlan {
+  Layout full, half;
+  std::vector<Unit> units;
+  size_t total = 0;
+};
+
+swa_status_t make_step_plan(const swa_params_t* p, int chunks, StepPlan& P) {
+  swa_status_t st = make_layout(p, chunks, P.full);
+  if (st != SWA_OK) return st;
+  const int64_t n_kv = p->N_kv == 0 ? p->N : p->N_kv;
+  const bool taper = chunks >= 2 && p->N % (2 * chunks) == 0 && n_kv % (2 * chunks) == 0;
+  if (taper && (st = make_layout(p, 2 * chunks, P.half)) != SWA_OK) return st;
+  P.units.clear();
+  size_t o = 0;
+  for (int c = 0; c < chunks; ++c) {
+    if (taper && (c == 0 || c == chunks - 1)) {
+      for (int k = 0; k < 2; ++k) {
+        P.units.push_back(Unit{&P.half, 2 * c + k, o});
+        o += P.half.chunk_bytes;
+      }
+    } else {
+      P.units.push_back(Unit{&P.full, c, o});
+      o += P.full.chunk_bytes;
+    }
+  }
+  P.total = o;
+  return SWA_OK;
+}
+
 cudaError_t copy_in(const Span& s, int c, void* dev, const void* host, cudaStream_t st) {
   return cudaMemcpy2DAsync(dev, s.width, static_cast<const uint8_t*>(host) + s.host_offset(c), s.pitch, s.width,
                            s.rows, cudaMemcpyHostToDevice, st);
@@ -115,24 +155,24 @@ extern "C" {
 
 swa_status_t swa_step_host_buffer_size(const swa_params_t* p, int chunks, size_t* bytes) {
   if (!bytes) return swa::set_error(SWA_ERR_PARAM_NULLPTR, "bytes is NULL");
-  Layout L;
-  swa_status_t st = make_layout(p, chunks, L);
+  StepPlan P;
+  swa_status_t st = make_step_plan(p, chunks, P);
   if (st != SWA_OK) return st;
-  *bytes = L.total;
+  *bytes = P.total;
   return SWA_OK;
 }
 
 swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, const void* k, const void* v,
                            const void* dy, void* out, float* softmax_max, float* softmax_sum, void* dq, void* dk,
                            void* dv, void* device_buffer, size_t device_bytes, swa_stream_t stream) {
-  Layout L;
-  swa_status_t st = make_layout(p, chunks, L);
+  StepPlan P;
+  swa_status_t st = make_step_plan(p, chunks, P);
   if (st != SWA_OK) return st;
   if (!q || !k || !v || !dy || !out || !softmax_max || !softmax_sum || !dq || !dk || !dv)
     return swa::set_error(SWA_ERR_PARAM_NULLPTR, "a required host pointer is NULL");
-  if (!device_buffer || device_bytes < L.total || (reinterpret_cast<uintptr_t>(device_buffer) & 255u))
+  if (!device_buffer || device_bytes < P.total || (reinterpret_cast<uintptr_t>(device_buffer) & 255u))
     return swa::set_error(SWA_ERR_WORKSPACE, "device_buffer must be >= %zu bytes and 256-byte aligned (got %zu)",
-                          L.total, device_bytes);
+                          P.total, device_bytes);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   // Two copy streams, two compute streams and their events, released by the
   // driver once their work has run (cudaStreamDestroy / cudaEventDestroy on
@@ -166,9 +206,11 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
     return cuda_fail(e, "setting up the copy streams");
   }
   uint8_t* base = static_cast<uint8_t*>(device_buffer);
-  for (int c = 0; c < chunks; ++c) {
-    uint8_t* d = base + static_cast<size_t>(c) * L.chunk_bytes;
-    cudaStream_t comp = s_comp[c & 1];
+  for (size_t u = 0; u < P.units.size(); ++u) {
+    const Layout& L = *P.units[u].L;
+    const int c = P.units[u].group;
+    uint8_t* d = base + P.units[u].off;
+    cudaStream_t comp = s_comp[u & 1];
     const swa_stream_t comp_h = reinterpret_cast<swa_stream_t>(comp);
     // The forward needs q, k, v only: it starts while dy is still being
     // copied.  out and the statistics are final after the forward and go
@@ -229,15 +271,15 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
 
 swa_status_t swa_step_host_status(const swa_params_t* p, int chunks, const void* device_buffer,
                                   swa_stream_t stream) {
-  Layout L;
-  swa_status_t st = make_layout(p, chunks, L);
+  StepPlan P;
+  swa_status_t st = make_step_plan(p, chunks, P);
   if (st != SWA_OK) return st;
   if (!device_buffer) return swa::set_error(SWA_ERR_PARAM_NULLPTR, "device_buffer is NULL");
   const uint8_t* base = static_cast<const uint8_t*>(device_buffer);
-  for (int c = 0; c < chunks; ++c) {
-    const uint8_t* d = base + static_cast<size_t>(c) * L.chunk_bytes;
-    if ((st = swa_workspace_status(d + L.fws_off, stream)) != SWA_OK) return st;
-    if ((st = swa_workspace_status(d + L.bws_off, stream)) != SWA_OK) return st;
+  for (const Unit& un : P.units) {
+    const uint8_t* d = base + un.off;
+    if ((st = swa_workspace_status(d + un.L->fws_off, stream)) != SWA_OK) return st;
+    if ((st = swa_workspace_status(d + un.L->bws_off, stream)) != SWA_OK) return st;
   }
   return SWA_OK;
 }

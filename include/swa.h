@@ -206,10 +206,14 @@ SWA_API swa_status_t swa_backward_noalloc(const swa_params_t *p, const void *q, 
 
 /* Forward + backward of one problem whose tensors live in HOST memory (an
  * addition of this library; the pages' operators take device tensors).  The
- * heads are split into `chunks` equal groups; each group is copied to its own
- * compact device tensors inside `device_buffer`, computed (swa_forward, then
- * swa_backward) and copied back, and the copies of the next and the previous
- * group run on two internal streams while a group computes.  Consecutive
+ * heads are split into `chunks` equal groups; when 2 * chunks divides N and
+ * N_kv, the first and the last group are split once more into two halves, so
+ * that less is copied before the first computation and after the last.  Each
+ * group is copied to its own compact device tensors inside `device_buffer`,
+ * computed (swa_forward, then swa_backward) and copied back, and the copies
+ * of the next and the previous group run on two internal streams while a
+ * group computes.  A group's forward starts once its q, k and v are in, and
+ * its out and statistics go back while its backward runs.  Consecutive
  * groups compute on two further internal streams in turn, so one group's
  * kernels may start while the previous group's last CTAs still run.
  * Heads are independent, so the results equal those of one swa_forward +

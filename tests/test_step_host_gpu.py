@@ -24,6 +24,10 @@ CASES = {
                                    cu_seqlens_kv=[130, 130, 400], scale=0.125, sparse_mode=0), (1, 4)),
     "bnsd_fp32_d72": (dict(layout="BNSD", B=1, N=4, D=72, S_q=200, S_kv=260, scale=72 ** -0.5, sparse_mode=4,
                            pre_tokens=50, next_tokens=80, dtype="fp32"), (2,)),
+    # 3 and 6 chunks of 12 heads: halved first and last groups around full
+    # ones (6 heads -> units of 2, 2, 4, 2, 2; 12 -> 1, 1, 2, 2, 2, 2, 1, 1)
+    "bnsd_n12_tapered": (dict(layout="BNSD", B=1, N=12, D=64, S_q=256, S_kv=256, scale=0.125, sparse_mode=4,
+                              pre_tokens=90, next_tokens=30), (3, 6)),
     "bnsd_gendrop": (dict(layout="BNSD", B=1, N=2, D=64, S_q=256, S_kv=256, scale=0.125, sparse_mode=4,
                           pre_tokens=64, next_tokens=0, keep_prob=0.8, dropout_gen=1, dropout_seed=9,
                           dropout_offset=1), (1,)),
