@@ -3,7 +3,7 @@
 // with the computation.
 //
 // The heads are split into `chunks` equal groups (the first and the last
-// split once more in two, see StepPlan).  Each group is a complete
+// split further into halves, see StepPlan).  Each group is a complete
 // smaller problem (heads are independent in every step of the method), so it
 // is copied into its own compact device tensors, computed by swa_forward and
 // swa_backward, and copied back.  Chunk c+1's inputs travel host -> device on
@@ -97,40 +97,53 @@ swa_status_t make_layout(const swa_params_t* p, int chunks, Layout& L) {
   return SWA_OK;
 }
 
-// The pipeline's units: head groups of N / chunks heads, except that the
-// first and the last group are each split into two halves when 2 * chunks
-// divides N and N_kv.  The pipeline's fill (the first unit's inputs) and
-// drain (the last unit's results) then move half as many bytes.  Units are
-// packed back to back in the device buffer.
+// The pipeline's units: head groups of N / chunks heads, except at the two
+// ends.  The first group is split in halves, its first half again, and so on
+// for `levels` levels (while 2^levels * chunks divides N and N_kv, at most 3),
+// and the last group the same way mirrored: with 8 groups of 4 heads the units
+// hold 1, 1, 2, 4, ..., 4, 2, 1, 1 heads.  The pipeline's fill (the first
+// unit's inputs) and drain (the last unit's results) then move a fraction of
+// a group's bytes while the middle groups stay large.  Units are packed back
+// to back in the device buffer.
 struct Unit {
   const Layout* L;
   int group;   // head group index within L's split
   size_t off;  // byte offset of the unit's region in the device buffer
 };
+constexpr int kMaxLevels = 3;
 struct StepPlan {
-  Layout full, half;
+  Layout split[kMaxLevels + 1];  // split[l]: chunks * 2^l equal groups
   std::vector<Unit> units;
   size_t total = 0;
 };
 
 swa_status_t make_step_plan(const swa_params_t* p, int chunks, StepPlan& P) {
-  swa_status_t st = make_layout(p, chunks, P.full);
+  swa_status_t st = make_layout(p, chunks, P.split[0]);
   if (st != SWA_OK) return st;
   const int64_t n_kv = p->N_kv == 0 ? p->N : p->N_kv;
-  const bool taper = chunks >= 2 && p->N % (2 * chunks) == 0 && n_kv % (2 * chunks) == 0;
-  if (taper && (st = make_layout(p, 2 * chunks, P.half)) != SWA_OK) return st;
+  int levels = 0;
+  while (chunks >= 2 && levels < kMaxLevels) {
+    const int64_t g = int64_t{chunks} << (levels + 1);
+    if (p->N % g != 0 || n_kv % g != 0) break;
+    if ((st = make_layout(p, static_cast<int>(g), P.split[levels + 1])) != SWA_OK) return st;
+    ++levels;
+  }
   P.units.clear();
   size_t o = 0;
-  for (int c = 0; c < chunks; ++c) {
-    if (taper && (c == 0 || c == chunks - 1)) {
-      for (int k = 0; k < 2; ++k) {
-        P.units.push_back(Unit{&P.half, 2 * c + k, o});
-        o += P.half.chunk_bytes;
-      }
-    } else {
-      P.units.push_back(Unit{&P.full, c, o});
-      o += P.full.chunk_bytes;
-    }
+  auto add = [&](int l, int group) {
+    P.units.push_back(Unit{&P.split[l], group, o});
+    o += P.split[l].chunk_bytes;
+  };
+  if (levels == 0) {
+    for (int c = 0; c < chunks; ++c) add(0, c);
+  } else {
+    // first group: split[levels] groups 0 and 1, then group 1 of each coarser split
+    add(levels, 0);
+    for (int l = levels; l >= 1; --l) add(l, 1);
+    for (int c = 1; c < chunks - 1; ++c) add(0, c);
+    // last group, mirrored: group 2^l * chunks - 2 of each finer split, then the last one
+    for (int l = 1; l <= levels; ++l) add(l, (chunks << l) - 2);
+    add(levels, (chunks << levels) - 1);
   }
   P.total = o;
   return SWA_OK;

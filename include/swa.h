@@ -206,8 +206,9 @@ SWA_API swa_status_t swa_backward_noalloc(const swa_params_t *p, const void *q, 
 
 /* Forward + backward of one problem whose tensors live in HOST memory (an
  * addition of this library; the pages' operators take device tensors).  The
- * heads are split into `chunks` equal groups; when 2 * chunks divides N and
- * N_kv, the first and the last group are split once more into two halves, so
+ * heads are split into `chunks` equal groups; the first group is split into
+ * halves, its first half again, and so on while 2^l * chunks divides N and
+ * N_kv (at most three levels), and the last group the same way mirrored, so
  * that less is copied before the first computation and after the last.  Each
  * group is copied to its own compact device tensors inside `device_buffer`,
  * computed (swa_forward, then swa_backward) and copied back, and the copies

@@ -198,9 +198,11 @@ def test_fp32_workspace_holds_bf16_copies(lib):
 def test_step_host_buffer_sizes(lib):
     """swa_step_host's device buffer: per pipeline unit, compact copies of q,
     k, v, dy, out, dq, dk, dv and the statistics plus that unit's workspaces.
-    A unit is a group of N / chunks heads, except that the first and the last
-    group are split into two halves when 2 * chunks divides N and N_kv; the
-    chunk count must divide N and N_kv, and dropout needs one chunk."""
+    A unit is a group of N / chunks heads, except at the ends: the first group
+    is split in halves, its first half again, and so on while 2^l * chunks
+    divides N and N_kv (at most three levels), and the last group the same way
+    mirrored; the chunk count must divide N and N_kv, and dropout needs one
+    chunk."""
     g = Geometry("BNSD", 2, 8, 64, S_q=256, S_kv=256, N_kv=4, sparse_mode=0)
     p = swa.Params(g)
     r256 = lambda x: (x + 255) // 256 * 256
@@ -212,14 +214,14 @@ def test_step_host_buffer_sizes(lib):
         fws, bws = _size(sub)[1], _size(sub, backward=True)[1]
         return 4 * r256(qb) + 4 * r256(kb) + 2 * r256(sb) + r256(fws) + r256(bws)
 
-    # 1 chunk: one unit; 2 chunks: 2*2 = 4 divides N = 8 and N_kv = 4, so both
-    # groups are halved (four units of a 4-way split); 4 chunks: 8 does not
-    # divide N_kv, so four units of the 4-way split
+    # 1 chunk: one unit; 2 chunks: 2*2 = 4 divides N = 8 and N_kv = 4 (8 does
+    # not divide N_kv), so one level: both groups halved, four units of the
+    # 4-way split; 4 chunks: 8 does not divide N_kv, so four plain groups
     expect = {1: unit_bytes(1), 2: 4 * unit_bytes(4), 4: 4 * unit_bytes(4)}
     for chunks, want in expect.items():
         assert swa.swa_step_host_buffer_size(p, chunks) == want, chunks
-    # three chunks of N = 12, N_kv = 12: halved first and last group (four
-    # units of a 6-way split) plus one full group of the 3-way split
+    # three chunks of N = 12: 6 and 12 divide N, so two levels; units of
+    # 1, 1, 2, 4, 2, 1, 1 heads (12-, 6-, 3-, 6- and 12-way splits)
     g3 = Geometry("BNSD", 1, 12, 64, S_q=128, S_kv=128, sparse_mode=0)
 
     def unit3(groups):
@@ -229,7 +231,7 @@ def test_step_host_buffer_sizes(lib):
         fws, bws = _size(sub)[1], _size(sub, backward=True)[1]
         return 8 * r256(qb) + 2 * r256(sb) + r256(fws) + r256(bws)
 
-    assert swa.swa_step_host_buffer_size(swa.Params(g3), 3) == 4 * unit3(6) + unit3(3)
+    assert swa.swa_step_host_buffer_size(swa.Params(g3), 3) == 4 * unit3(12) + 2 * unit3(6) + unit3(3)
     n = ctypes.c_size_t(0)
     assert swa.lib().swa_step_host_buffer_size(p.ref(), 3, ctypes.byref(n)) == swa.SWA_ERR_PARAM_INVALID
     assert swa.lib().swa_step_host_buffer_size(p.ref(), 0, ctypes.byref(n)) == swa.SWA_ERR_PARAM_INVALID

@@ -24,8 +24,8 @@ CASES = {
                                    cu_seqlens_kv=[130, 130, 400], scale=0.125, sparse_mode=0), (1, 4)),
     "bnsd_fp32_d72": (dict(layout="BNSD", B=1, N=4, D=72, S_q=200, S_kv=260, scale=72 ** -0.5, sparse_mode=4,
                            pre_tokens=50, next_tokens=80, dtype="fp32"), (2,)),
-    # 3 and 6 chunks of 12 heads: halved first and last groups around full
-    # ones (6 heads -> units of 2, 2, 4, 2, 2; 12 -> 1, 1, 2, 2, 2, 2, 1, 1)
+    # 3 and 6 chunks of 12 heads: split end groups around full ones (units
+    # of 1, 1, 2, 4, 2, 1, 1 and of 1, 1, 2, 2, 2, 2, 1, 1 heads)
     "bnsd_n12_tapered": (dict(layout="BNSD", B=1, N=12, D=64, S_q=256, S_kv=256, scale=0.125, sparse_mode=4,
                               pre_tokens=90, next_tokens=30), (3, 6)),
     "bnsd_gendrop": (dict(layout="BNSD", B=1, N=2, D=64, S_q=256, S_kv=256, scale=0.125, sparse_mode=4,
