@@ -72,7 +72,8 @@ enum : int {
   kBarPtFull = 18,     // [3]
   kBarDsFull = 21,     // [3]
   kBarRegionFree = 24, // [3]
-  kBarSLoaded = 27,
+  kBarDsHalf = 27,     // [3] the first 32-query half of each thread's dS^T columns stored
+  kBarSLoaded = 30,
   kBarDpFull,
   kBarMmaDone,
   kBarDrainSdp,
@@ -232,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar[kBarSFull + (r)], 1);
       mbar_init(&bar[kBarPtFull + (r)], kComputeThreads);
       mbar_init(&bar[kBarDsFull + (r)], kComputeThreads);
+      mbar_init(&bar[kBarDsHalf + (r)], kComputeThreads);
       mbar_init(&bar[kBarRegionFree + (r)], 1);
     }
     mbar_init(&bar[kBarMmaDone], 1);
@@ -405,12 +407,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16_ts(tmem + kColDV, ra + (kk >> 2) * 64 + (kk & 3) * 8,
                        sdesc_advance(d_dy, kk * 2048), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar[kBarDyEmpty + (st)]);  // dP^T(it) read dY(it) too; it finished before P^T(it) existed
+        // dK += dS^T Q in two parts: k-steps 0, 1, 4, 5 read the first
+        // 32-query half of each warp's 64 dS^T columns, stored before the
+        // second (DsHalf); k-steps 2, 3, 6, 7 the second (DsFull)
+        auto dk_steps = [&](int k0) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int kk = k0 + (e & 1) + (e >> 1) * 4;
+            umma_bf16_ts(tmem + kColDK, ra + (kk >> 2) * 64 + 32 + (kk & 3) * 8, sdesc_advance(d_q, kk * 2048),
+                         kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
+          }
+        };
+        if (!mbar_wait(&bar[kBarDsHalf + region_of<kR>(it)], region_phase<kR>(it), a.err, kErrBwdMma)) break;
+        tc_fence_after_sync();
+        dk_steps(0);
         if (!mbar_wait(&bar[kBarDsFull + region_of<kR>(it)], region_phase<kR>(it), a.err, kErrBwdMma)) break;
         tc_fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < kTileM / 16; ++kk)  // dK += dS^T Q
-          umma_bf16_ts(tmem + kColDK, ra + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
-                       sdesc_advance(d_q, kk * 2048), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
+        dk_steps(2);
         umma_commit(&bar[kBarQEmpty + (qs)]);  // likewise S^T(it) for Q(it)
         umma_commit(&bar[kBarRegionFree + region_of<kR>(it)]);
         if (it == n_it - 1) umma_commit(&bar[kBarMmaDone]);
@@ -586,9 +599,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t d[32];  // dP^T columns [cbase + 32, cbase + 64), where dS^T goes
           tmem_ld_32x32b_x32(col + 32, d);
           tmem_ld_wait(d);
+          // dP^T is in registers: the first half of dS^T goes out now, so dK
+          // can start on it while the second half is formed
+          tmem_st_32x32b_x16(col + 32, dk);
+          tmem_st_wait();
+          tc_fence_before_sync();
+          mbar_arrive(&bar[kBarDsHalf + region_of<kR>(it)]);
           ds_half(1, d, dk + 16);
         }
-        tmem_st_32x32b_x32(col + 32, dk);
+        tmem_st_32x32b_x16(col + 48, dk + 16);
       }
       tmem_st_wait();
       tc_fence_before_sync();
