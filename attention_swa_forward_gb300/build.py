@@ -12,8 +12,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libswa.so")
-SOURCES = ["swa_api.cpp", "swa_fwd.cu", "swa_bwd_dkv.cu", "swa_bwd_dq.cu", "swa_aux.cu", "swa_noalloc.cu",
-           "swa_host.cpp"]
+SOURCES = ["swa_api.cpp", "swa_fwd.cu", "swa_fwd_pair.cu", "swa_bwd_dkv.cu", "swa_bwd_dq.cu", "swa_aux.cu",
+           "swa_noalloc.cu", "swa_host.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I", INCLUDE, "-I", CSRC]

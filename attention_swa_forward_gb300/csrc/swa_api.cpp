@@ -28,6 +28,7 @@ namespace {
 
 thread_local std::string t_last_error = "no error";
 std::atomic<int32_t> g_stall{0};  // swa_debug_stall: read into Geometry::stall by every call
+std::atomic<int32_t> g_fwd_pairs{0};  // swa_debug_forward_pairs: 0 by size, 1 always, 2 never
 thread_local cudaEvent_t t_ev[6] = {};  // start/stop around: forward, dK/dV pass, dQ pass
 
 swa_status_t fail(swa_status_t st, const char* fmt, ...) {
@@ -477,11 +478,32 @@ swa_status_t swa_forward(const swa_params_t* p, const void* q, const void* k, co
 
   e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
-  const std::vector<SeqDesc> descs = build_descs(plan, true);
+  std::vector<SeqDesc> descs = build_descs(plan, true);
+  // D <= 64: TMEM holds two query tiles' S, O and P, and one CTA takes a pair
+  // of consecutive query tiles (swa_fwd_pair.cu), when the pairs still fill
+  // every SM at least once; smaller problems keep one CTA per query tile
+  bool pair = false;
+  if (plan.g.D <= 64) {
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the SM count");
+    int64_t items = 0;
+    for (const SeqDesc& d : descs) items += static_cast<int64_t>(d.tiles) * d.heads;
+    const int32_t mode = g_fwd_pairs.load(std::memory_order_relaxed);
+    pair = mode == 1 || (mode == 0 && items >= 2 * static_cast<int64_t>(sms));
+  }
+  if (pair)
+    for (SeqDesc& d : descs) d.tiles = (d.tiles + 1) / 2;
   if (t_ev[0]) cudaEventRecord(t_ev[0], s);
   e = run_tables(
-      descs, [&](const SeqTable<kSmallTable>& t) { return launch_forward(a, t, mq, mk, mv, s); },
-      [&](const SeqTable<kLargeTable>& t) { return launch_forward(a, t, mq, mk, mv, s); });
+      descs,
+      [&](const SeqTable<kSmallTable>& t) {
+        return pair ? launch_forward_pair(a, t, mq, mk, mv, s) : launch_forward(a, t, mq, mk, mv, s);
+      },
+      [&](const SeqTable<kLargeTable>& t) {
+        return pair ? launch_forward_pair(a, t, mq, mk, mv, s) : launch_forward(a, t, mq, mk, mv, s);
+      });
   if (t_ev[1]) cudaEventRecord(t_ev[1], s);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return SWA_OK;
@@ -652,6 +674,9 @@ swa_status_t swa_debug_schedule(const swa_params_t* p, int32_t pass, int32_t* it
 }
 
 void swa_debug_stall(int32_t kernels) { g_stall.store(kernels & 7, std::memory_order_relaxed); }
+void swa_debug_forward_pairs(int32_t mode) {
+  g_fwd_pairs.store(mode >= 0 && mode <= 2 ? mode : 0, std::memory_order_relaxed);
+}
 
 void swa_set_timing_events(void* const* events) {
   for (int i = 0; i < 6; ++i) t_ev[i] = events ? static_cast<cudaEvent_t>(events[i]) : nullptr;

@@ -155,6 +155,11 @@ swa_status_t set_error(swa_status_t st, const char* fmt, ...);
 template <int CAP>
 cudaError_t launch_forward(const FwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, cudaStream_t stream);
+// D <= 64: one CTA per pair of query tiles; the table's entries count pairs
+// (tiles = ceil(query tiles / 2)).
+template <int CAP>
+cudaError_t launch_forward_pair(const FwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq,
+                                const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t stream);
 template <int CAP>
 cudaError_t launch_backward_dkv(const BwdArgs& a, const SeqTable<CAP>& tab, const CUtensorMap& mq,
                                 const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdy,

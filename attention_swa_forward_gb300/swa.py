@@ -103,6 +103,8 @@ def lib() -> ctypes.CDLL:
             L.swa_debug_schedule.restype = st
             L.swa_debug_stall.argtypes = [ctypes.c_int32]
             L.swa_debug_stall.restype = None
+            L.swa_debug_forward_pairs.argtypes = [ctypes.c_int32]
+            L.swa_debug_forward_pairs.restype = None
             L.swa_last_error.argtypes = []
             L.swa_last_error.restype = ctypes.c_char_p
             _lib = L
@@ -113,7 +115,7 @@ def exported_symbols():
     return ["swa_params_default", "swa_forward_workspace_size", "swa_forward", "swa_backward_workspace_size",
             "swa_backward", "swa_backward_noalloc", "swa_workspace_status", "swa_set_timing_events",
             "swa_last_error", "swa_dropout_mask", "swa_step_host_buffer_size", "swa_step_host",
-            "swa_step_host_status", "swa_debug_schedule", "swa_debug_stall"]
+            "swa_step_host_status", "swa_debug_schedule", "swa_debug_stall", "swa_debug_forward_pairs"]
 
 
 def _check(status: int):
@@ -247,6 +249,12 @@ def swa_debug_stall(kernels: int):
     """Test hook: kernels (bit 0 forward, 1 key-major, 2 query-major) whose
     compute warps first wait on a barrier nothing completes; 0 turns it off."""
     lib().swa_debug_stall(int(kernels))
+
+
+def swa_debug_forward_pairs(mode: int):
+    """Test hook: forward kernel choice at D <= 64 (0 by size, 1 always one
+    CTA per pair of query tiles, 2 never)."""
+    lib().swa_debug_forward_pairs(int(mode))
 
 
 # ------------------------------------------------------- torch convenience --

@@ -296,10 +296,17 @@ SWA_API void swa_set_timing_events(void *const *events);
  * memory and returns, and swa_workspace_status then reports
  * SWA_ERR_TIMEOUT: it exercises the bounded-wait failure path without a
  * fault.  The outputs of such a call are undefined.  Process-wide; 0 turns
- * it off. */
+ * it off.
+ *
+ * swa_debug_forward_pairs: how later forward calls with D <= 64 pick their
+ * kernel.  0 (the default): one CTA per pair of query tiles when the pairs
+ * fill every SM at least once, else one CTA per query tile; 1: always pairs;
+ * 2: never.  Both kernels compute the same results; the switch lets tests
+ * reach each on small problems.  Process-wide. */
 SWA_API swa_status_t swa_debug_schedule(const swa_params_t *p, int32_t pass, int32_t *items, int64_t capacity,
                                         int64_t *count);
 SWA_API void swa_debug_stall(int32_t kernels);
+SWA_API void swa_debug_forward_pairs(int32_t mode);
 
 /* Text describing the last non-OK status returned on this thread. */
 SWA_API const char *swa_last_error(void);

@@ -88,8 +88,13 @@ def _gpu(geom, inp, mask=None):
             (("out", out), ("smax", smax), ("ssum", ssum), ("dq", dq), ("dk", dk), ("dv", dv))}
 
 
-@pytest.mark.parametrize("name", sorted(CASES))
-def test_generated_dropout_parity(name):
+# every case with the forward's default kernel choice; the D <= 64 cases also
+# with the forward forced onto one CTA per pair of query tiles
+_RUNS = [(n, 0) for n in sorted(CASES)] + [(n, 1) for n in sorted(CASES) if CASES[n]["D"] <= 64]
+
+
+@pytest.mark.parametrize("name,pairs", _RUNS, ids=[n + ("-pairs" if p else "") for n, p in _RUNS])
+def test_generated_dropout_parity(name, pairs):
     geom = Geometry(**CASES[name])
     inp = draw(geom, 6000 + sum(map(ord, name)))
     assert inp.drop_mask is None  # the seed / offset stand for the mask
@@ -97,9 +102,13 @@ def test_generated_dropout_parity(name):
     mask = orc.generate_keep_mask(pr, geom.dropout_seed, geom.dropout_offset)
     out, smax, ssum = orc.forward(pr, inp.q, inp.k, inp.v, mask)
     dq, dk, dv = orc.backward(pr, inp.q, inp.k, inp.v, inp.dy, mask)
-    res = _gpu(geom, inp)
+    swa.swa_debug_forward_pairs(pairs)
+    try:
+        res = _gpu(geom, inp)
+    finally:
+        swa.swa_debug_forward_pairs(0)
     dt = out_dtype(geom)
-    label = f"generated dropout {name}"
+    label = f"generated dropout {name}" + (" (query tile pairs)" if pairs else "")
     check_tensor(label, "out", res["out"], out, dt, TOL_OUT)
     check_stat(label, "softmax_max", res["smax"], smax)
     check_stat(label, "softmax_sum", res["ssum"], ssum)

@@ -187,6 +187,31 @@ def test_small_parity(name):
     check_grads(res, dq, dk, dv, name, dt)
 
 
+@pytest.mark.parametrize("name", sorted(n for n, kw in SMALL.items() if kw["D"] <= 64))
+def test_small_parity_pair_forward(name):
+    """The D <= 64 cases with the forward forced onto one CTA per pair of query
+    tiles (the size rule picks that kernel only when the pairs fill every SM):
+    every output, the gradients computed from its out and statistics
+    included, against the oracle."""
+    geom = Geometry(**SMALL[name])
+    inp = draw(geom, 5000 + sum(map(ord, name)))
+    pr = to_problem(geom)
+    swa.swa_debug_forward_pairs(1)
+    try:
+        res = as_np(run_gpu(inp))
+    finally:
+        swa.swa_debug_forward_pairs(0)
+    dt = out_dtype(geom)
+    ops = (inp.q, inp.k, inp.v, inp.dy)
+    if dt == "fp32":  # computed on the bf16 roundings of fp32 inputs
+        ops = tuple(t.to(torch.bfloat16).to(torch.float32) for t in ops)
+    out, smax, ssum = orc.forward(pr, *ops[:3], inp.drop_mask)
+    dq, dk, dv = orc.backward(pr, *ops, inp.drop_mask)
+    label = f"{name} (query tile pairs)"
+    check_forward(res, out, smax, ssum, label, dt)
+    check_grads(res, dq, dk, dv, label, dt)
+
+
 def test_repeat_calls_are_deterministic_forward():
     geom = Geometry(**SMALL["bnsd_band_d128_ragged"])
     inp = draw(geom, 77)
