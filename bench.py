@@ -68,6 +68,17 @@ def flops(g: Geometry) -> dict:
     return {"pairs": p, "fwd": 4.0 * g.D * p, "bwd": 10.0 * g.D * p, "total": 14.0 * g.D * p}
 
 
+def forward_kernel_name(g: Geometry, dev) -> str:
+    """The forward kernel the library launches: at D <= 64 one CTA per pair
+    of query tiles when the pairs fill every SM at least once, otherwise one
+    CTA per query tile (the rule swa_forward applies)."""
+    if g.D > 64:
+        return "swa_fwd_kernel"
+    tiles = g.N * sum(-(-lq // 128) for lq, _ in g.seq_lens())
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return "swa_fwd_pair_kernel" if tiles >= 2 * sms else "swa_fwd_kernel"
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -410,7 +421,7 @@ def run_swa(args, name: str):
     # dY V^T, dS K).  Only 14*D per pair counts toward the metric.
     pairs_d = fl["pairs"] * g.D
     kernels = {
-        "swa_fwd_kernel": {"ms": fwd_ms, "tflops": 4.0 * pairs_d / (fwd_ms / 1e3) / 1e12},
+        forward_kernel_name(g, dev): {"ms": fwd_ms, "tflops": 4.0 * pairs_d / (fwd_ms / 1e3) / 1e12},
         "swa_bwd_dkv_kernel": {"ms": dkv_ms, "tflops": 8.0 * pairs_d / (dkv_ms / 1e3) / 1e12},
         "swa_bwd_dq_kernel": {"ms": dq_ms, "tflops": 6.0 * pairs_d / (dq_ms / 1e3) / 1e12},
     }
