@@ -639,21 +639,24 @@ swa_status_t swa_workspace_status(const void* workspace, swa_stream_t stream) {
 swa_status_t swa_debug_schedule(const swa_params_t* p, int32_t pass, int32_t* items, int64_t capacity,
                                 int64_t* count) {
   if (!count) return fail(SWA_ERR_PARAM_NULLPTR, "count is NULL");
-  if (pass != 0 && pass != 1) return fail(SWA_ERR_PARAM_INVALID, "pass should be 0 or 1, got %d", pass);
+  if (pass < 0 || pass > 2) return fail(SWA_ERR_PARAM_INVALID, "pass should be 0, 1 or 2, got %d", pass);
   Plan plan;
   swa_status_t st = make_plan(p, plan);
   if (st != SWA_OK) return st;
-  const bool query_side = pass == 0;
+  const bool query_side = pass != 1;
   const int nh = query_side ? plan.g.N : plan.g.N_kv;
-  const std::vector<SeqDesc> descs = build_descs(plan, query_side);
+  std::vector<SeqDesc> descs = build_descs(plan, query_side);
+  if (pass == 2)  // the forward's pairs of query tiles (as swa_forward sets them up at D <= 64)
+    for (SeqDesc& d : descs) d.tiles = (d.tiles + 1) / 2;
   int64_t n = 0;
   int32_t launch = 0;
   auto emit = [&](const auto& tab) -> cudaError_t {
     for (int k = 0; k < tab.n_items; ++k) {
       const Item it = resolve_item(tab, plan.g, k, nh);
       int t0, cnt;
-      if (query_side) key_tiles_of_query_tile(plan.g, it.s, it.tile, &t0, &cnt);
-      else query_tiles_of_key_tile(plan.g, it.s, it.tile, &t0, &cnt);
+      if (pass == 0) key_tiles_of_query_tile(plan.g, it.s, it.tile, &t0, &cnt);
+      else if (pass == 1) query_tiles_of_key_tile(plan.g, it.s, it.tile, &t0, &cnt);
+      else key_tiles_of_query_pair(plan.g, it.s, it.tile, &t0, &cnt);
       if (items && n < capacity) {
         int32_t* r = items + 6 * n;
         r[0] = launch;

@@ -78,17 +78,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const HalfRange ra = half_range(g, sq, 2 * w.tile), rb = half_range(g, sq, 2 * w.tile + 1);
   const bool has_b = (2 * w.tile + 1) * kTileM < sq.q_len;
   // the key tiles either half visits: [u0, u0 + n_u)
-  int u0 = 0, n_u = 0;
-  if (ra.n > 0 && rb.n > 0) {
-    u0 = min(ra.t0, rb.t0);
-    n_u = max(ra.t0 + ra.n, rb.t0 + rb.n) - u0;
-  } else if (ra.n > 0) {
-    u0 = ra.t0;
-    n_u = ra.n;
-  } else if (rb.n > 0) {
-    u0 = rb.t0;
-    n_u = rb.n;
-  }
+  int u0, n_u;
+  key_tiles_of_query_pair(g, sq, w.tile, &u0, &n_u);
   auto uses = [&](int h, int j) {
     const HalfRange& r = h ? rb : ra;
     return j >= r.t0 && j < r.t0 + r.n;

@@ -77,6 +77,28 @@ SWA_HD void key_tiles_of_query_tile(const Geometry& g, const SeqInfo& s, int til
   }
 }
 
+// Key tiles [*u0, *u0 + *n) that query tiles 2p and 2p + 1 of sequence s
+// visit between them (the forward at D <= 64 takes the two in one CTA; the
+// second may not exist).  A tile with no visible key adds nothing; the union
+// of two runs is taken from the first start to the last end.
+SWA_HD void key_tiles_of_query_pair(const Geometry& g, const SeqInfo& s, int p, int* u0, int* n) {
+  int ta = 0, na = 0, tb = 0, nb = 0;
+  if (2 * p * kTileM < s.q_len) key_tiles_of_query_tile(g, s, 2 * p, &ta, &na);
+  if ((2 * p + 1) * kTileM < s.q_len) key_tiles_of_query_tile(g, s, 2 * p + 1, &tb, &nb);
+  *u0 = 0;
+  *n = 0;
+  if (na > 0 && nb > 0) {
+    *u0 = ta < tb ? ta : tb;
+    *n = (ta + na > tb + nb ? ta + na : tb + nb) - *u0;
+  } else if (na > 0) {
+    *u0 = ta;
+    *n = na;
+  } else if (nb > 0) {
+    *u0 = tb;
+    *n = nb;
+  }
+}
+
 // Query tiles [*t0, *t0 + *n) that see key tile `tile` of sequence s:
 // i - pre <= j <= i + next  <=>  j - next <= i <= j + pre.
 SWA_HD void query_tiles_of_key_tile(const Geometry& g, const SeqInfo& s, int tile, int* t0, int* n) {

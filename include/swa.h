@@ -276,11 +276,16 @@ SWA_API void swa_set_timing_events(void *const *events);
  * FlashAttentionVarLenScore doc (preTokens / nextTokens as the left and right
  * edges): a 128-row query tile touches one run of 128-row key tiles and a
  * key tile one run of query tiles; tiles outside the runs are skipped.
- *   pass 0   forward and query-major dQ pass: one item per query tile of
- *            each (batch, query head); partners are key tiles
+ *   pass 0   query-major dQ pass (and the forward one CTA per query tile):
+ *            one item per query tile of each (batch, query head); partners
+ *            are key tiles
  *   pass 1   key-major dK / dV pass: one item per key tile of each (batch,
  *            key/value head); partners are query tiles, walked for every
  *            query head of the group
+ *   pass 2   the forward one CTA per pair of query tiles (D <= 64, when the
+ *            pairs fill every SM): one item per pair p (query tiles 2p and
+ *            2p + 1) of each (batch, query head); partners are the key tiles
+ *            from the first start to the last end of the two tiles' runs
  *   items    host, 6 int32 per item in launch order: launch index, batch,
  *            head, tile, first partner tile, partner tile count; at most
  *            `capacity` items are written (items may be NULL to count)

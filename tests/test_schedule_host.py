@@ -1,7 +1,8 @@
 """The band / varlen tile schedule, checked on the host against brute force.
 
-swa_debug_schedule returns the work items the kernels of one pass receive,
-computed by the same code the kernels run.  Brute force from the BAND
+swa_debug_schedule returns the work items the kernels of one pass receive
+(query tiles, key tiles, or the forward's pairs of query tiles), computed by
+the same code the kernels run.  Brute force from the BAND
 inequality (FlashAttentionVarLenScore doc, preTokens / nextTokens as the
 window's left and right edges: query i sees key j iff
 i - pre <= j <= i + next, local indices) gives, for every 128-row tile of
@@ -122,6 +123,43 @@ def test_schedule_covers_every_visible_tile_once(name, pass_):
         assert launches[-1] + 1 == (n_entries + table - 1) // table
 
 
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_pair_schedule_covers_every_query_tile_once(name):
+    # pass 2, the forward one CTA per pair of query tiles: pair p of each
+    # (batch, head) holds query tiles 2p and 2p + 1 (the second only if it
+    # exists), every tile in exactly one pair; the pair's key tiles run from
+    # the first start to the last end of its tiles' brute-force partner runs
+    geom = Geometry(**CASES[name])
+    items = swa.swa_debug_schedule(swa.Params(geom), 2)
+    expect_pairs, covered = {}, {}
+    for b, (lq, lk) in enumerate(geom.seq_lens()):
+        if lq == 0:
+            continue
+        q_to_k, _ = _partner_sets(geom, lq, lk)
+        tiles = len(q_to_k)
+        for h in range(geom.N):
+            for t in range(tiles):
+                covered[(b, h, t)] = 0
+            for p in range((tiles + 1) // 2):
+                runs = [_as_run(q_to_k[t]) for t in (2 * p, 2 * p + 1) if t < tiles and q_to_k[t]]
+                if runs:
+                    u0 = min(r[0] for r in runs)
+                    expect_pairs[(b, h, p)] = (u0, max(r[0] + r[1] for r in runs) - u0)
+                else:
+                    expect_pairs[(b, h, p)] = (0, 0)
+    got = {}
+    for launch, b, h, p, t0, n in items.tolist():
+        assert (b, h, p) not in got, ("pair listed twice", (b, h, p))
+        got[(b, h, p)] = (t0 if n else 0, n)
+        for t in (2 * p, 2 * p + 1):
+            if (b, h, t) in covered:
+                covered[(b, h, t)] += 1
+    assert set(got) == set(expect_pairs)
+    assert all(c == 1 for c in covered.values()), [k_ for k_, c in covered.items() if c != 1][:5]
+    bad = [k_ for k_ in expect_pairs if got[k_] != expect_pairs[k_]]
+    assert not bad, [(k_, got[k_], expect_pairs[k_]) for k_ in bad[:5]]
+
+
 @pytest.mark.parametrize("name", ["tnd_600", "tnd_40_mixed_skipped", "tnd_rect_nomask"])
 @pytest.mark.parametrize("pass_", [0, 1], ids=["query_tiles", "key_tiles"])
 def test_tnd_entries_heaviest_first(name, pass_):
@@ -142,5 +180,5 @@ def test_tnd_entries_heaviest_first(name, pass_):
 def test_schedule_rejects_bad_pass(lib):
     geom = Geometry(**CASES["bnsd_band"])
     with pytest.raises(swa.SwaError) as e:
-        swa.swa_debug_schedule(swa.Params(geom), 2)
+        swa.swa_debug_schedule(swa.Params(geom), 3)
     assert e.value.status == swa.SWA_ERR_PARAM_INVALID
