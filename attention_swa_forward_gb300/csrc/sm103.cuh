@@ -35,6 +35,16 @@ __device__ __forceinline__ bool elect_one_lane() {
 // records an error code in a device word and gives up instead of hanging.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s; real waits are microseconds
 
+// ------------------------------------------- programmatic dependent launch --
+// Wait until the grids this one depends on in stream order have completed
+// and their memory is visible; a no-op for a normally launched grid.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let a dependent grid launched with programmatic stream serialization start
+// once every CTA of this grid has signalled (or exited).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------- mbarrier --
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

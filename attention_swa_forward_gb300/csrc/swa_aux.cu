@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(256) swa_prep_kernel(const PrepArgs a) {
   constexpr int kPer = DP / 32;  // 2 or 4 elements per lane
   const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  griddep_wait();  // dY, O and the statistics come from earlier grids
+  griddep_launch_dependents();
   if (blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0;  // fresh error word for this backward call
   if (row >= a.rows) return;
   const int D = a.g.D;
@@ -76,6 +78,8 @@ __global__ void __launch_bounds__(256) swa_prep_wide_kernel(const PrepArgs a) {
   constexpr int kSteps = 4;
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  griddep_wait();  // dY, O and the statistics come from earlier grids
+  griddep_launch_dependents();
   if (blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0;  // fresh error word for this backward call
   const int64_t row0 = warp * (kRowsPerStep * kSteps) + lane / kLanesPerRow;
   const int col = (lane % kLanesPerRow) * 8;
@@ -177,24 +181,23 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream) {
     const int64_t rows_per_block = 8 * (32 / (a.g.D / 8)) * 4;  // 8 warps x rows per step x 4 steps
     const unsigned gr = static_cast<unsigned>((a.rows + rows_per_block - 1) / rows_per_block);
     if (a.g.D == 64) {
-      if (a.g.f16) swa_prep_wide_kernel<64, true><<<gr, 256, 0, stream>>>(a);
-      else swa_prep_wide_kernel<64, false><<<gr, 256, 0, stream>>>(a);
+      if (a.g.f16) return launch_pdl(swa_prep_wide_kernel<64, true>, dim3(gr), dim3(256), 0, stream, a);
+      return launch_pdl(swa_prep_wide_kernel<64, false>, dim3(gr), dim3(256), 0, stream, a);
     } else {
-      if (a.g.f16) swa_prep_wide_kernel<128, true><<<gr, 256, 0, stream>>>(a);
-      else swa_prep_wide_kernel<128, false><<<gr, 256, 0, stream>>>(a);
+      if (a.g.f16) return launch_pdl(swa_prep_wide_kernel<128, true>, dim3(gr), dim3(256), 0, stream, a);
+      return launch_pdl(swa_prep_wide_kernel<128, false>, dim3(gr), dim3(256), 0, stream, a);
     }
-    return cudaGetLastError();
   }
   const int64_t threads = a.rows * 32;
   const int block = 256;
   const int64_t grid = (threads + block - 1) / block;
   const unsigned gr = static_cast<unsigned>(grid);
   if (a.g.D <= 64) {
-    if (a.g.f16) swa_prep_kernel<64, true><<<gr, block, 0, stream>>>(a);
-    else swa_prep_kernel<64, false><<<gr, block, 0, stream>>>(a);
+    if (a.g.f16) return launch_pdl(swa_prep_kernel<64, true>, dim3(gr), dim3(block), 0, stream, a);
+    return launch_pdl(swa_prep_kernel<64, false>, dim3(gr), dim3(block), 0, stream, a);
   } else {
-    if (a.g.f16) swa_prep_kernel<128, true><<<gr, block, 0, stream>>>(a);
-    else swa_prep_kernel<128, false><<<gr, block, 0, stream>>>(a);
+    if (a.g.f16) return launch_pdl(swa_prep_kernel<128, true>, dim3(gr), dim3(block), 0, stream, a);
+    return launch_pdl(swa_prep_kernel<128, false>, dim3(gr), dim3(block), 0, stream, a);
   }
   return cudaGetLastError();
 }

@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kColDV = DkvTmem<D>::kColDV, kColDK = DkvTmem<D>::kColDK;
   auto region = [](int it) { return static_cast<uint32_t>(region_of<kR>(it)) * 128u; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_launch_dependents();  // the query-major pass reads nothing this grid writes
   const Geometry& g = a.g;
   const Item w = resolve_item(tab, a.g, static_cast<int>(blockIdx.x), a.g.N_kv);  // w.n: key/value head
   const SeqInfo sq = w.s;
@@ -267,6 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 8) {
     // -------------------------------------------------- producer (warp) --
+    // the per-query statistics below come from the preprocess grid; every
+    // lane waits for it (so this grid also completes only after it has)
+    griddep_wait();
     if (n_q > 0) {
       int q_issued = 0, dy_issued = 0;
       for (int it = 0; it < n_it; ++it) {
@@ -685,8 +689,8 @@ cudaError_t launch_dkv_t(const BwdArgs& a, const SeqTable<CAP>& tab, const CUten
   static std::atomic<uint64_t> smem_set{0};
   const cudaError_t e = set_smem_limit(swa_bwd_dkv_kernel<D, DM, F16, CAP>, smem, smem_set);
   if (e != cudaSuccess) return e;
-  swa_bwd_dkv_kernel<D, DM, F16, CAP><<<tab.n_items, kThreads, smem, stream>>>(a, tab, mq, mk, mv, mdy);
-  return cudaGetLastError();
+  return launch_pdl(swa_bwd_dkv_kernel<D, DM, F16, CAP>, dim3(tab.n_items), dim3(kThreads), smem, stream, a, tab, mq,
+                    mk, mv, mdy);
 }
 
 }  // namespace

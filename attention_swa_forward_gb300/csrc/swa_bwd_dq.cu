@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   DqSmem<D>& s = *reinterpret_cast<DqSmem<D>*>(align1024(smem_raw));
   constexpr int kTileBytes = DqSmem<D>::kTileBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_launch_dependents();
   const Geometry& g = a.g;
   const Item w = resolve_item(tab, a.g, static_cast<int>(blockIdx.x), a.g.N);
   const int hk = w.n / a.g.group;  // the key/value head this query head reads
@@ -234,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_valid = i < sq.q_len;
     int wlo, whi;
     key_window(g, sq, i, wlo, whi);
+    griddep_wait();  // lse2 and D come from the preprocess grid, which ran before the previous grid ended
     float lse2 = INFINITY, drow = 0.f;
     if (row_valid) {
       const int64_t si = ws_stat_index(g, sq, w.b, w.n, i);
@@ -408,8 +410,8 @@ cudaError_t launch_dq_t(const BwdArgs& a, const SeqTable<CAP>& tab, const CUtens
   static std::atomic<uint64_t> smem_set{0};
   const cudaError_t e = set_smem_limit(swa_bwd_dq_kernel<D, DM, F16, CAP>, smem, smem_set);
   if (e != cudaSuccess) return e;
-  swa_bwd_dq_kernel<D, DM, F16, CAP><<<tab.n_items, kThreads, smem, stream>>>(a, tab, mq, mk, mv, mdy);
-  return cudaGetLastError();
+  return launch_pdl(swa_bwd_dq_kernel<D, DM, F16, CAP>, dim3(tab.n_items), dim3(kThreads), smem, stream, a, tab, mq,
+                    mk, mv, mdy);
 }
 
 }  // namespace

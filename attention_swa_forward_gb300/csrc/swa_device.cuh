@@ -2,6 +2,8 @@
 // addressing of BNSD / TND rows, the BAND window, tile loads, dropout bits and
 // writing a bf16 row into a 128-byte-swizzled shared-memory tile.
 #pragma once
+#include <utility>
+
 #include "sm103.cuh"
 #include "swa_internal.h"
 #include "swa_sched.h"
@@ -9,6 +11,25 @@
 namespace swa {
 
 constexpr int kAtomBytes = 128 * 128;  // one atom column: 128 rows x 128 bytes
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous grid on the stream finishes; it calls griddep_wait before
+// reading what that grid (or an earlier one) wrote.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
