@@ -476,9 +476,11 @@ swa_status_t swa_forward(const swa_params_t* p, const void* q, const void* k, co
   a.ssum = softmax_sum;
   a.err = static_cast<int32_t*>(workspace);
 
-  e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
-  if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
   std::vector<SeqDesc> descs = build_descs(plan, true);
+  if (descs.empty()) {  // nothing to launch; otherwise the first launch clears the status word itself
+    e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
+  }
   // D <= 64: TMEM holds two query tiles' S, O and P, and one CTA takes a pair
   // of consecutive query tiles (swa_fwd_pair.cu), when the pairs still fill
   // every SM at least once; smaller problems keep one CTA per query tile
@@ -496,14 +498,13 @@ swa_status_t swa_forward(const swa_params_t* p, const void* q, const void* k, co
   if (pair)
     for (SeqDesc& d : descs) d.tiles = (d.tiles + 1) / 2;
   if (t_ev[0]) cudaEventRecord(t_ev[0], s);
-  e = run_tables(
-      descs,
-      [&](const SeqTable<kSmallTable>& t) {
-        return pair ? launch_forward_pair(a, t, mq, mk, mv, s) : launch_forward(a, t, mq, mk, mv, s);
-      },
-      [&](const SeqTable<kLargeTable>& t) {
-        return pair ? launch_forward_pair(a, t, mq, mk, mv, s) : launch_forward(a, t, mq, mk, mv, s);
-      });
+  int launches = 0;
+  auto one = [&](const auto& t) {
+    FwdArgs at = a;
+    at.clear_err = launches++ == 0 ? 1 : 0;
+    return pair ? launch_forward_pair(at, t, mq, mk, mv, s) : launch_forward(at, t, mq, mk, mv, s);
+  };
+  e = run_tables(descs, one, one);
   if (t_ev[1]) cudaEventRecord(t_ev[1], s);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return SWA_OK;

@@ -54,6 +54,13 @@ __global__ void __launch_bounds__(224, 1)
   FwdSmem<D>& s = *reinterpret_cast<FwdSmem<D>*>(align1024(smem_raw));
   constexpr int kTileBytes = FwdSmem<D>::kTileBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // q, k, v, the outputs and the status word may belong to the previous grid
+  // on the stream (this kernel is launched with programmatic serialization):
+  // wait for it before touching any of them.  No early trigger: the next
+  // grid starts when this one ends (backward CTAs made resident during the
+  // forward's last wave slowed the whole step)
+  griddep_wait();
+  if (a.clear_err && blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0;
   const Geometry& g = a.g;
   const Item w = resolve_item(tab, a.g, static_cast<int>(blockIdx.x), a.g.N);
   const int hk = w.n / a.g.group;  // the key/value head this query head reads
@@ -393,8 +400,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, const SeqTable<CAP>& tab, const CUten
   static std::atomic<uint64_t> smem_set{0};
   const cudaError_t e = set_smem_limit(swa_fwd_kernel<D, DM, F16, CAP>, smem, smem_set);
   if (e != cudaSuccess) return e;
-  swa_fwd_kernel<D, DM, F16, CAP><<<tab.n_items, 224, smem, stream>>>(a, tab, mq, mk, mv);
-  return cudaGetLastError();
+  return launch_pdl(swa_fwd_kernel<D, DM, F16, CAP>, dim3(tab.n_items), dim3(224), smem, stream, a, tab, mq, mk, mv);
 }
 
 }  // namespace

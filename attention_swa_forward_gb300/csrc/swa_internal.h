@@ -118,6 +118,7 @@ struct FwdArgs {
   float* smax;
   float* ssum;
   int32_t* err;
+  int32_t clear_err;  // 1: block 0 clears *err on entry (the first launch of a forward call)
 };
 
 struct BwdArgs {
