@@ -7,11 +7,15 @@
 // smaller problem (heads are independent in every step of the method), so it
 // is copied into its own compact device tensors, computed by swa_forward and
 // swa_backward, and copied back.  Chunk c+1's inputs travel host -> device on
-// one stream and chunk c-1's results device -> host on another while chunk c
+// one stream and chunk c-1's results device -> host on others while chunk c
 // computes.  Consecutive chunks compute on two internal streams in turn, so
 // the kernels of chunk c+1 can start on the SMs that chunk c's last wave of
 // CTAs leaves idle: smaller chunks (a shorter pipeline fill and drain of the
-// copies) then cost no kernel efficiency.  A head group of a BNSD tensor is
+// copies) then cost no kernel efficiency.  Each compute stream has its own
+// device -> host stream: a chunk's results queue behind its own backward,
+// not behind the other stream's chunk, so the device -> host direction of
+// the link (the one that drains last) is not left idle while a ready chunk
+// waits.  A head group of a BNSD tensor is
 // one contiguous block per batch, and of a TND tensor one block per row, so
 // every copy is a single 2-D copy (rows = batches or tokens, pitch = the full
 // row).
@@ -187,15 +191,16 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
     return swa::set_error(SWA_ERR_WORKSPACE, "device_buffer must be >= %zu bytes and 256-byte aligned (got %zu)",
                           P.total, device_bytes);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  // Two copy streams, two compute streams and their events, released by the
-  // driver once their work has run (cudaStreamDestroy / cudaEventDestroy on
-  // pending work).
-  cudaStream_t s_in = nullptr, s_out = nullptr, s_comp[2] = {nullptr, nullptr};
+  // One host -> device stream, two compute streams with a device -> host
+  // stream each, and their events, released by the driver once their work has
+  // run (cudaStreamDestroy / cudaEventDestroy on pending work).
+  cudaStream_t s_in = nullptr, s_outs[2] = {nullptr, nullptr}, s_comp[2] = {nullptr, nullptr};
   std::vector<cudaEvent_t> ev;
   auto release = [&]() {
     for (cudaEvent_t e : ev) cudaEventDestroy(e);
     if (s_in) cudaStreamDestroy(s_in);
-    if (s_out) cudaStreamDestroy(s_out);
+    for (cudaStream_t x : s_outs)
+      if (x) cudaStreamDestroy(x);
     for (cudaStream_t x : s_comp)
       if (x) cudaStreamDestroy(x);
   };
@@ -205,14 +210,14 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
     return r;
   };
   cudaError_t e = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking);
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&s_outs[i], cudaStreamNonBlocking);
   for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&s_comp[i], cudaStreamNonBlocking);
   cudaEvent_t start = nullptr, done = nullptr;
   if (e == cudaSuccess) e = event(&start);
   if (e == cudaSuccess) e = event(&done);
   // nothing may start before what the caller queued earlier (which may still use the buffer)
   if (e == cudaSuccess) e = cudaEventRecord(start, cs);
-  for (cudaStream_t x : {s_in, s_out, s_comp[0], s_comp[1]})
+  for (cudaStream_t x : {s_in, s_outs[0], s_outs[1], s_comp[0], s_comp[1]})
     if (e == cudaSuccess) e = cudaStreamWaitEvent(x, start, 0);
   if (e != cudaSuccess) {
     release();
@@ -223,7 +228,7 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
     const Layout& L = *P.units[u].L;
     const int c = P.units[u].group;
     uint8_t* d = base + P.units[u].off;
-    cudaStream_t comp = s_comp[u & 1];
+    cudaStream_t comp = s_comp[u & 1], s_out = s_outs[u & 1];
     const swa_stream_t comp_h = reinterpret_cast<swa_stream_t>(comp);
     // The forward needs q, k, v only: it starts while dy is still being
     // copied.  out and the statistics are final after the forward and go
@@ -262,7 +267,7 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
   }
   // The caller's stream completes only after the last result has reached the
   // host, and, after a failure part-way, only after every copy already
-  // enqueued on either copy stream has run: host memory is never written
+  // enqueued on any copy stream has run: host memory is never written
   // once the caller has seen the stream finish.
   cudaEvent_t in_end = nullptr, comp_end[2] = {nullptr, nullptr};
   cudaError_t e_end = event(&in_end);
@@ -273,8 +278,12 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
     if (e_end == cudaSuccess) e_end = cudaEventRecord(comp_end[i], s_comp[i]);
     if (e_end == cudaSuccess) e_end = cudaStreamWaitEvent(cs, comp_end[i], 0);
   }
-  if (e_end == cudaSuccess) e_end = cudaEventRecord(done, s_out);
+  cudaEvent_t done2 = nullptr;
+  if (e_end == cudaSuccess) e_end = event(&done2);
+  if (e_end == cudaSuccess) e_end = cudaEventRecord(done, s_outs[0]);
   if (e_end == cudaSuccess) e_end = cudaStreamWaitEvent(cs, done, 0);
+  if (e_end == cudaSuccess) e_end = cudaEventRecord(done2, s_outs[1]);
+  if (e_end == cudaSuccess) e_end = cudaStreamWaitEvent(cs, done2, 0);
   if (e == cudaSuccess) e = e_end;
   release();
   if (st != SWA_OK) return st;

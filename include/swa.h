@@ -212,11 +212,12 @@ SWA_API swa_status_t swa_backward_noalloc(const swa_params_t *p, const void *q, 
  * that less is copied before the first computation and after the last.  Each
  * group is copied to its own compact device tensors inside `device_buffer`,
  * computed (swa_forward, then swa_backward) and copied back, and the copies
- * of the next and the previous group run on two internal streams while a
- * group computes.  A group's forward starts once its q, k and v are in, and
- * its out and statistics go back while its backward runs.  Consecutive
- * groups compute on two further internal streams in turn, so one group's
- * kernels may start while the previous group's last CTAs still run.
+ * of the next and the previous group run on internal streams while a group
+ * computes.  A group's forward starts once its q, k and v are in, and its
+ * out and statistics go back while its backward runs.  Consecutive groups
+ * compute on two further internal streams in turn, so one group's kernels
+ * may start while the previous group's last CTAs still run; each of those
+ * has its own device -> host stream.
  * Heads are independent, so the results equal those of one swa_forward +
  * swa_backward on device copies of the same tensors, bit for bit.
  *   q, k, v, dy   host, p->dtype, shapes and layout as for swa_forward /
