@@ -106,3 +106,49 @@ def test_grouped_heads_are_repeated_heads(D):
         # for margin
         tol = 2.0 ** -8 * (per_head.abs().sum(dim=2) + got.abs()) + 1e-6
         assert torch.all((got - summed).abs() <= tol), n
+
+
+PAIR_CASES = {
+    "band": dict(layout="BNSD", B=2, N=2, D=64, S_q=700, S_kv=700, scale=0.125, sparse_mode=4, pre_tokens=300,
+                 next_tokens=40),
+    "mask_dropout": dict(layout="BNSD", B=1, N=3, D=64, S_q=520, S_kv=520, scale=0.125, sparse_mode=4, pre_tokens=256,
+                         next_tokens=256, keep_prob=0.9),
+    "gen_dropout_tnd": dict(layout="TND", B=3, N=2, D=64, cu_seqlens_q=[300, 300, 750], cu_seqlens_kv=[300, 300, 750],
+                            scale=0.125, sparse_mode=4, pre_tokens=90, next_tokens=10, keep_prob=0.85, dropout_gen=1,
+                            dropout_seed=5, dropout_offset=2),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PAIR_CASES))
+def test_pair_forward_is_one_tile_forward(name):
+    """At D <= 64 the forward over pairs of query tiles computes every row
+    with the same operations in the same order as one CTA per tile."""
+    geom = Geometry(**PAIR_CASES[name])
+    inp = draw(geom, 75)
+    res = []
+    for mode in (1, 2):  # always pairs, never pairs
+        swa.swa_debug_forward_pairs(mode)
+        try:
+            res.append(run(geom, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask))
+        finally:
+            swa.swa_debug_forward_pairs(0)
+    same(res[0], res[1], label=name)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_fp32_storage_of_bf16_values_is_the_bf16_path(D):
+    """fp32 inputs are rounded to bf16 once and computed like bf16 inputs in
+    fp32: inputs that already are bf16 values give the bf16 path's results,
+    once the fp32 outputs are rounded to bf16 (round to nearest even)."""
+    kw = dict(layout="BNSD", B=1, N=2, D=D, S_q=333, S_kv=333, scale=D ** -0.5, sparse_mode=4, pre_tokens=150,
+              next_tokens=20, keep_prob=0.9)
+    g16 = Geometry(**kw)
+    g32 = Geometry(**kw, dtype="fp32")
+    inp = draw(g16, 76)
+    r16 = run(g16, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask)
+    f = lambda x: x.to(torch.float32)
+    r32 = run(g32, f(inp.q), f(inp.k), f(inp.v), f(inp.dy), inp.drop_mask)
+    for n in ("out", "dq", "dk", "dv"):
+        assert r32[n].dtype == torch.float32
+        assert torch.equal(r32[n].to(torch.bfloat16), r16[n]), n
+    same(r16, r32, names=("smax", "ssum"))
