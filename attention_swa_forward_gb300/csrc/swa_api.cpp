@@ -29,7 +29,7 @@ namespace {
 thread_local std::string t_last_error = "no error";
 std::atomic<int32_t> g_stall{0};  // swa_debug_stall: read into Geometry::stall by every call
 std::atomic<int32_t> g_fwd_pairs{0};  // swa_debug_forward_pairs: 0 by size, 1 always, 2 never
-thread_local cudaEvent_t t_ev[6] = {};  // start/stop around: forward, dK/dV pass, dQ pass
+thread_local cudaEvent_t t_ev[8] = {};  // start/stop around: forward, dK/dV pass, dQ pass, preprocess
 
 swa_status_t fail(swa_status_t st, const char* fmt, ...) {
   char buf[512];
@@ -570,7 +570,9 @@ swa_status_t swa_backward(const swa_params_t* p, const void* q, const void* k, c
   pa.ssum = softmax_sum;
   pa.lse2 = lse2;
   pa.dsum = dsum;
+  if (t_ev[6]) cudaEventRecord(t_ev[6], s);
   cudaError_t e = launch_prep(pa, s);
+  if (t_ev[7]) cudaEventRecord(t_ev[7], s);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
 
   BwdArgs a{};
@@ -683,7 +685,7 @@ void swa_debug_forward_pairs(int32_t mode) {
 }
 
 void swa_set_timing_events(void* const* events) {
-  for (int i = 0; i < 6; ++i) t_ev[i] = events ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+  for (int i = 0; i < 8; ++i) t_ev[i] = events ? static_cast<cudaEvent_t>(events[i]) : nullptr;
 }
 
 const char* swa_last_error(void) { return t_last_error.c_str(); }

@@ -217,14 +217,14 @@ _timing_handles = None
 
 
 def swa_set_timing_events(events=None):
-    """Six raw cudaEvent_t handles (ints): forward, dK/dV and dQ start/stop pairs;
-    None stops recording."""
+    """Eight raw cudaEvent_t handles (ints): forward, dK/dV, dQ and preprocess
+    start/stop pairs; None stops recording."""
     global _timing_handles
     if events is None:
         _timing_handles = None
         lib().swa_set_timing_events(None)
         return
-    _timing_handles = (ctypes.c_void_p * 6)(*events)
+    _timing_handles = (ctypes.c_void_p * 8)(*events)
     lib().swa_set_timing_events(_timing_handles)
 
 

@@ -320,7 +320,7 @@ def run_swa(args, name: str):
     swa.check_workspace(ws_b)
 
     # ---- timed region: K steps, kernel events around the main kernels
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
     for quad in evs:  # materialise the event handles on this stream
         for e in quad:
             e.record(stream)
@@ -348,6 +348,7 @@ def run_swa(args, name: str):
     fwd_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     dkv_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
     dq_ms = sum(e[4].elapsed_time(e[5]) for e in evs) / args.steps
+    prep_ms = sum(e[6].elapsed_time(e[7]) for e in evs) / args.steps
     sec_max = max_over_ranks(sec, ws, dev)
     value = whole_job_value(fl["total"], ws, sec_max)
 
@@ -437,10 +438,20 @@ def run_swa(args, name: str):
     achieved = kernels[dom]["tflops"]
     for kd in kernels.values():
         kd["frac"] = kd["tflops"] / peak
+    # the memory-bound preprocess: reads dY and O and the two statistics,
+    # writes lse2 and D (algorithmic bytes per launch)
+    # (16-bit dY and O: fp32 inputs reach it as bf16 copies)
+    rows = g.B * g.N * g.S_q if g.layout == "BNSD" else g.T_q * g.N
+    prep_bytes = rows * (2 * g.D * 2 + 4 * 4)
+    hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    prep_gbs = prep_bytes / (prep_ms / 1e3) / 1e9
+    memory_bound = {"kernel": "swa_prep_wide_kernel" if g.D in (64, 128) else "swa_prep_kernel", "bound": "hbm",
+                    "ms": prep_ms, "bytes": prep_bytes, "achieved": prep_gbs, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": prep_gbs / hbm_peak, "peak_source": f"{source} hbm_gbs"}
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{source} {peak_key} (timed region {region_s:.2f} s of back-to-back steps)",
-                "kernels": kernels}
+                "kernels": kernels, "memory_bound": memory_bound}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": sec_max * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -260,12 +260,13 @@ SWA_API swa_status_t swa_dropout_mask(const swa_params_t *p, uint8_t *mask, size
  * (SWA_ERR_CUDA if the stream itself failed). */
 SWA_API swa_status_t swa_workspace_status(const void *workspace, swa_stream_t stream);
 
-/* Measurement support.  `events` is NULL (stop recording) or an array of six
- * cudaEvent_t handles owned by the caller: {forward start, forward stop,
- * dK/dV start, dK/dV stop, dQ start, dQ stop}.  Later calls on this thread
- * record each pair on their stream immediately around the corresponding
- * attention kernel launch (swa_forward's forward kernel; swa_backward's
- * key-major dK/dV kernel and query-major dQ kernel).  No other effect. */
+/* Measurement support.  `events` is NULL (stop recording) or an array of
+ * eight cudaEvent_t handles owned by the caller: {forward start, forward
+ * stop, dK/dV start, dK/dV stop, dQ start, dQ stop, preprocess start,
+ * preprocess stop}.  Later calls on this thread record each pair on their
+ * stream immediately around the corresponding kernel launch (swa_forward's
+ * forward kernel; swa_backward's key-major dK/dV kernel, query-major dQ
+ * kernel and D / lse2 preprocess).  No other effect. */
 SWA_API void swa_set_timing_events(void *const *events);
 
 /* Test and inspection support (additions of this library; the pages have no
