@@ -73,6 +73,7 @@ def _load():
             lib.orc_backward_dq_rows.argtypes = [P, vp, vp, vp, vp, vp, i64, vp, vp]
             lib.orc_backward_dkv_cols.argtypes = [P, vp, vp, vp, vp, vp, i64, vp, vp, vp]
             lib.orc_key_ranges.argtypes = [P, i64, vp, vp, vp]
+            lib.orc_rounding_budget.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.orc_philox4x32_10.argtypes = [vp, vp, vp]
             lib.orc_philox4x32_10.restype = None
             lib.orc_generate_keep_mask.argtypes = [P, ctypes.c_uint64, ctypes.c_uint64, vp]
@@ -252,6 +253,24 @@ def backward_dkv_cols(pr: Problem, q, k, v, dy, drop_mask, cols):
     lib.orc_backward_dkv_cols(c.ref(), _ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(m), len(sel), _ptr(sel), _ptr(dk),
                               _ptr(dv))
     return dk, dv
+
+
+def rounding_budget(pr: Problem, q, k, v, dy, drop_mask=None):
+    """Test support: per element, the sums of absolute values that bound the
+    drift of out, dQ, dK and dV when the products' operands P~ (forward,
+    dV) and dS (dQ, dK) are rounded to a float of unit roundoff u: the error
+    is at most u times the budget, to first order.  Returns (out_b, dq_b,
+    dk_b, dv_b) as float64 in the layouts of out / q and k / v."""
+    lib = _load()
+    c = _Call(pr)
+    q, k, v, dy, m = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dy), _as_u8(drop_mask)
+    out_b = np.zeros(_q_shape(pr), dtype=np.float64)
+    dq_b = np.zeros(_q_shape(pr), dtype=np.float64)
+    dk_b = np.zeros(_kv_shape(pr), dtype=np.float64)
+    dv_b = np.zeros(_kv_shape(pr), dtype=np.float64)
+    lib.orc_rounding_budget(c.ref(), _ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(m), _ptr(out_b), _ptr(dq_b),
+                            _ptr(dk_b), _ptr(dv_b))
+    return out_b, dq_b, dk_b, dv_b
 
 
 def key_ranges(pr: Problem, rows):

@@ -432,6 +432,105 @@ int orc_backward_dkv_cols(const orc_params *p, const double *q, const double *k,
   return 0;
 }
 
+/* ------------------------------------------------- rounding budgets -- */
+
+/* Test support, not part of what the method computes: sums of absolute
+ * values that bound how far an evaluation of the same definitions may drift
+ * when it rounds the operands of its matrix products to a float of unit
+ * roundoff u.  Rounding every P~_ij = P_ij z_ij / keep (forward and dV) or
+ * dS_ij (dQ and dK) to such a float moves, element by element over d, at
+ * most by u times
+ *   out_b[i] = sum_j |P~_ij| |v_j|,      dv_b[j] = sum_i |P~_ij| |dY_i|,
+ *   dq_b[i]  = |scale| sum_j |dS_ij| |k_j|,  dk_b[j] = |scale| sum_i |dS_ij| |q_i|
+ * (to first order: the error of a sum of rounded terms), with P and dS as
+ * in the exact backward (the VarLen doc's forward formula; the PyPTO
+ * article's backward formulas). */
+static void budget_row(const orc_params *p, const orc_seq *s, int64_t b, int64_t n, int64_t i, const row_data *r,
+                       const double *q, const double *k, const double *v, const double *dy, const uint8_t *mask,
+                       double *out_b, double *dq_b) {
+  const int64_t D = p->D;
+  int64_t lo, hi;
+  for (int64_t d = 0; d < D; ++d) { out_b[d] = 0.0; dq_b[d] = 0.0; }
+  if (!key_range(p, s, i, &lo, &hi)) return;
+  const double *qi = q + row_q(p, s, b, n, i);
+  const double *dyi = dy + row_q(p, s, b, n, i);
+  const int64_t h = kv_head(p, n);
+  for (int64_t j = lo; j <= hi; ++j) {
+    const double *kj = k + row_kv(p, s, b, h, j);
+    const double *vj = v + row_kv(p, s, b, h, j);
+    const double pij = prob(r, p->scale * dot(qi, kj, D));
+    const double z = keep_bit(s, mask, n, i, j) / p->keep_prob;
+    const double dsij = pij * (dot(dyi, vj, D) * z - r->Di);
+    for (int64_t d = 0; d < D; ++d) {
+      out_b[d] += fabs(pij * z) * fabs(vj[d]);
+      dq_b[d] += fabs(p->scale) * fabs(dsij) * fabs(kj[d]);
+    }
+  }
+}
+
+static void budget_col(const orc_params *p, const orc_seq *s, int64_t b, int64_t h, int64_t j, const row_data *rows,
+                       const double *q, const double *k, const double *v, const double *dy, const uint8_t *mask,
+                       double *dk_b, double *dv_b) {
+  const int64_t D = p->D, G = p->N / p->N_kv;
+  int64_t lo, hi;
+  for (int64_t d = 0; d < D; ++d) { dk_b[d] = 0.0; dv_b[d] = 0.0; }
+  if (!query_range(p, s, j, &lo, &hi)) return;
+  const double *kj = k + row_kv(p, s, b, h, j);
+  const double *vj = v + row_kv(p, s, b, h, j);
+  for (int64_t gi = 0; gi < G; ++gi) {
+    const int64_t n = h * G + gi;
+    for (int64_t i = lo; i <= hi; ++i) {
+      const double *qi = q + row_q(p, s, b, n, i);
+      const double *dyi = dy + row_q(p, s, b, n, i);
+      const row_data *r = &rows[gi * s->q_len + i];
+      const double pij = prob(r, p->scale * dot(qi, kj, D));
+      const double z = keep_bit(s, mask, n, i, j) / p->keep_prob;
+      const double dsij = pij * (dot(dyi, vj, D) * z - r->Di);
+      for (int64_t d = 0; d < D; ++d) {
+        dv_b[d] += fabs(pij * z) * fabs(dyi[d]);
+        dk_b[d] += fabs(p->scale) * fabs(dsij) * fabs(qi[d]);
+      }
+    }
+  }
+}
+
+/* The four budgets over the whole problem (fp64, the layouts of out / q and
+ * of k / v), from the oracle's own forward (exact mode). */
+int orc_rounding_budget(const orc_params *p, const double *q, const double *k, const double *v, const double *dy,
+                        const uint8_t *mask, double *out_b, double *dq_b, double *dk_b, double *dv_b) {
+  const int64_t D = p->D, G = p->N / p->N_kv;
+  int64_t max_sq = 0;
+  for (int64_t b = 0; b < p->B; ++b) { orc_seq s = seq_of(p, b); if (s.q_len > max_sq) max_sq = s.q_len; }
+  row_data *rows = (row_data *)malloc(sizeof(row_data) * (size_t)(G * (max_sq > 0 ? max_sq : 1)));
+  for (int64_t b = 0; b < p->B; ++b) {
+    orc_seq s = seq_of(p, b);
+    for (int64_t h = 0; h < p->N_kv; ++h) {
+      for (int64_t gi = 0; gi < G; ++gi) {
+        const int64_t n = h * G + gi;
+        row_data *rg = rows + gi * s.q_len;
+#pragma omp parallel
+        {
+          double *o = (double *)malloc(sizeof(double) * D);
+#pragma omp for schedule(dynamic, 8)
+          for (int64_t i = 0; i < s.q_len; ++i)
+            rg[i] = backward_row_data(p, &s, b, n, i, q, k, v, dy, mask, NULL, NULL, NULL, o);
+          free(o);
+        }
+#pragma omp parallel for schedule(dynamic, 8)
+        for (int64_t i = 0; i < s.q_len; ++i)
+          budget_row(p, &s, b, n, i, &rg[i], q, k, v, dy, mask, out_b + row_q(p, &s, b, n, i),
+                     dq_b + row_q(p, &s, b, n, i));
+      }
+#pragma omp parallel for schedule(dynamic, 8)
+      for (int64_t j = 0; j < s.kv_len; ++j)
+        budget_col(p, &s, b, h, j, rows, q, k, v, dy, mask, dk_b + row_kv(p, &s, b, h, j),
+                   dv_b + row_kv(p, &s, b, h, j));
+    }
+  }
+  free(rows);
+  return 0;
+}
+
 /* ------------------------------------------------ generated dropout -- */
 
 /* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as

@@ -676,3 +676,71 @@ def test_edge_probe_exposes_one_pair_window_errors(name):
             kv_t, kv_b = dv_t.reshape(-1, D)[keys, 4:], dv_b.reshape(-1, D)[keys, 4:]
             gate = TOL_ABS + half_ulp(kv_t, "bf16")
             assert np.all(np.max(np.abs(kv_b - kv_t) - 3 * gate, axis=1) > 0), (name, edge, delta, "dv")
+
+
+# ------------------------------------------------------- rounding budgets --
+# orc_rounding_budget is test support: the per-element sums of absolute
+# values that bound the drift of out / dQ / dK / dV when the products'
+# operands are rounded to 16 bits (the tolerance of the GPU cases outside
+# the workloads' regime).  Its pins: equality where every term has one sign
+# (closed forms), the triangle inequality, and invariance / linearity in dY.
+
+def test_budget_equals_result_when_every_term_is_positive():
+    """v > 0 makes every term of out_i = sum_j P~_ij v_j positive, dY > 0
+    every term of dV_j = sum_i P~_ij dY_i: there the budgets are the results
+    (with dropout, so the z / keep weights are in both)."""
+    g = Geometry(layout="BNSD", B=1, N=2, D=16, S_q=70, S_kv=70, scale=0.25, sparse_mode=4, pre_tokens=20,
+                 next_tokens=5, keep_prob=0.8)
+    inp = draw(g, 501)
+    pr = to_problem(g)
+    v = inp.v.double().abs().numpy() + 0.01
+    dy = inp.dy.double().abs().numpy() + 0.01
+    out, _, _ = orc.forward(pr, inp.q, inp.k, v, inp.drop_mask)
+    _, _, dv = orc.backward(pr, inp.q, inp.k, v, dy, inp.drop_mask)
+    out_b, _, _, dv_b = orc.rounding_budget(pr, inp.q, inp.k, v, dy, inp.drop_mask)
+    np.testing.assert_allclose(out_b, out, rtol=1e-12, atol=0.0)
+    np.testing.assert_allclose(dv_b, dv, rtol=1e-12, atol=0.0)
+
+
+def test_dq_budget_is_exact_for_two_keys_of_opposite_sign():
+    """D = 1 and every query sees keys i - 1 and i (BAND(1, 0)).  The two
+    dS of a row sum to zero (sum_j P_ij (dP_ij - D_i) = 0), so
+    dQ_i = scale dS_{i,i-1} (k_{i-1} - k_i); with k alternating in sign,
+    |dQ_i| = |scale| |dS_{i,i-1}| (|k_{i-1}| + |k_i|), which is its budget."""
+    S = 40
+    g = Geometry(layout="BNSD", B=1, N=1, D=1, S_q=S, S_kv=S, scale=0.7, sparse_mode=4, pre_tokens=1, next_tokens=0)
+    pr = to_problem(g)
+    rng = np.random.default_rng(7)
+    sign = np.where(np.arange(S) % 2 == 0, 1.0, -1.0).reshape(1, 1, S, 1)
+    q = rng.normal(size=(1, 1, S, 1))
+    k = (np.abs(rng.normal(size=(1, 1, S, 1))) + 0.1) * sign
+    v = rng.normal(size=(1, 1, S, 1))
+    dy = rng.normal(size=(1, 1, S, 1))
+    dq, _, _ = orc.backward(pr, q, k, v, dy)
+    _, dq_b, _, _ = orc.rounding_budget(pr, q, k, v, dy)
+    assert np.max(np.abs(dq)) > 1e-3  # not a trivial zero
+    np.testing.assert_allclose(dq_b, np.abs(dq), rtol=1e-10, atol=1e-15)
+
+
+def test_budget_bounds_the_result_and_ignores_signs():
+    """Every budget is at least the absolute result (triangle inequality),
+    on a grouped-head BAND case with dropout; dY -> -dY flips dS and
+    P~ dY but not their absolute values, and 2 dY doubles the three
+    backward budgets while the forward's, which has no dY, stays."""
+    g = Geometry(layout="BNSD", B=1, N=4, N_kv=2, D=32, S_q=150, S_kv=150, scale=0.2, sparse_mode=4, pre_tokens=60,
+                 next_tokens=10, keep_prob=0.8)
+    inp = draw(g, 502)
+    pr = to_problem(g)
+    out, _, _ = orc.forward(pr, inp.q, inp.k, inp.v, inp.drop_mask)
+    dq, dk, dv = orc.backward(pr, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask)
+    b = orc.rounding_budget(pr, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask)
+    for got, bud in zip((out, dq, dk, dv), b):
+        assert np.all(bud >= np.abs(got) * (1.0 - 1e-12) - 1e-15)
+        assert np.max(bud - np.abs(got)) > 0.0  # strict somewhere: the terms do cancel
+    bn = orc.rounding_budget(pr, inp.q, inp.k, inp.v, -inp.dy, inp.drop_mask)
+    b2 = orc.rounding_budget(pr, inp.q, inp.k, inp.v, 2 * inp.dy, inp.drop_mask)
+    for x, y in zip(b, bn):
+        np.testing.assert_allclose(x, y, rtol=1e-12, atol=0.0)
+    for x, y in zip(b[1:], b2[1:]):
+        np.testing.assert_allclose(2.0 * x, y, rtol=1e-12, atol=0.0)
+    np.testing.assert_allclose(b[0], b2[0], rtol=1e-12, atol=0.0)
