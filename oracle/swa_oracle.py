@@ -74,6 +74,7 @@ def _load():
             lib.orc_backward_dkv_cols.argtypes = [P, vp, vp, vp, vp, vp, i64, vp, vp, vp]
             lib.orc_key_ranges.argtypes = [P, i64, vp, vp, vp]
             lib.orc_rounding_budget.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+            lib.orc_rounding_error.argtypes = [P, vp, vp, vp, vp, vp, ctypes.c_double, vp, vp, vp, vp]
             lib.orc_philox4x32_10.argtypes = [vp, vp, vp]
             lib.orc_philox4x32_10.restype = None
             lib.orc_generate_keep_mask.argtypes = [P, ctypes.c_uint64, ctypes.c_uint64, vp]
@@ -271,6 +272,25 @@ def rounding_budget(pr: Problem, q, k, v, dy, drop_mask=None):
     lib.orc_rounding_budget(c.ref(), _ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(m), _ptr(out_b), _ptr(dq_b),
                             _ptr(dk_b), _ptr(dv_b))
     return out_b, dq_b, dk_b, dv_b
+
+
+def rounding_error(pr: Problem, q, k, v, dy, drop_mask=None, u: float = 2.0 ** -8):
+    """Test support: per element, first-order error bounds of an evaluation
+    that rounds P~ (forward and dV), dS (dQ and dK) and the stored output O
+    to a float of unit roundoff ``u`` and computes everything else exactly:
+    u times the rounding budgets, plus for dQ and dK the effect of the error
+    of D_i = dY_i . O_i formed from that O.  Returns (out_e, dq_e, dk_e,
+    dv_e) as float64."""
+    lib = _load()
+    c = _Call(pr)
+    q, k, v, dy, m = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dy), _as_u8(drop_mask)
+    out_e = np.zeros(_q_shape(pr), dtype=np.float64)
+    dq_e = np.zeros(_q_shape(pr), dtype=np.float64)
+    dk_e = np.zeros(_kv_shape(pr), dtype=np.float64)
+    dv_e = np.zeros(_kv_shape(pr), dtype=np.float64)
+    lib.orc_rounding_error(c.ref(), _ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(m), float(u), _ptr(out_e), _ptr(dq_e),
+                           _ptr(dk_e), _ptr(dv_e))
+    return out_e, dq_e, dk_e, dv_e
 
 
 def key_ranges(pr: Problem, rows):

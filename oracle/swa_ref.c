@@ -531,6 +531,96 @@ int orc_rounding_budget(const orc_params *p, const double *q, const double *k, c
   return 0;
 }
 
+/* First-order error bounds of an evaluation that rounds P~ (the forward's
+ * and dV's operand), dS (dQ's and dK's) and the stored output O to a float
+ * of unit roundoff u, and computes everything else exactly (test support):
+ *   out_e = u out_b,   dv_e = u dv_b,
+ *   dq_e[i] = u dq_b[i] + |scale| dD_i sum_j P_ij |k_j|,
+ *   dk_e[j] = u dk_b[j] + |scale| sum_i dD_i P_ij |q_i|,
+ * where dD_i = u sum_d |dY_id| (out_b[i,d] + |O_id|) bounds the error of
+ * D_i = dY_i . O_i formed from that O (its operand-rounding error plus its
+ * own rounding), and dS_ij moves by -P_ij times it. */
+static double row_dD(const orc_params *p, const orc_seq *s, int64_t b, int64_t n, int64_t i, const row_data *r,
+                     const double *q, const double *k, const double *v, const double *dy, const uint8_t *mask,
+                     double u, double *o, double *ob, double *scratch) {
+  const int64_t D = p->D;
+  double m, l;
+  forward_row(p, s, b, n, i, q, k, v, mask, o, &m, &l);
+  budget_row(p, s, b, n, i, r, q, k, v, dy, mask, ob, scratch);
+  const double *dyi = dy + row_q(p, s, b, n, i);
+  double acc = 0.0;
+  for (int64_t d = 0; d < D; ++d) acc += fabs(dyi[d]) * (ob[d] + fabs(o[d]));
+  return u * acc;
+}
+
+int orc_rounding_error(const orc_params *p, const double *q, const double *k, const double *v, const double *dy,
+                       const uint8_t *mask, double u, double *out_e, double *dq_e, double *dk_e, double *dv_e) {
+  const int64_t D = p->D, G = p->N / p->N_kv;
+  orc_rounding_budget(p, q, k, v, dy, mask, out_e, dq_e, dk_e, dv_e);
+  const int64_t nq = total_q_rows(p) * p->N, nk = (p->layout == 0 ? p->B * p->S_kv : p->T_kv) * p->N_kv;
+  for (int64_t t = 0; t < nq * D; ++t) { out_e[t] *= u; dq_e[t] *= u; }
+  for (int64_t t = 0; t < nk * D; ++t) { dk_e[t] *= u; dv_e[t] *= u; }
+  int64_t max_sq = 0;
+  for (int64_t b = 0; b < p->B; ++b) { orc_seq s = seq_of(p, b); if (s.q_len > max_sq) max_sq = s.q_len; }
+  const size_t nrows = (size_t)(G * (max_sq > 0 ? max_sq : 1));
+  row_data *rows = (row_data *)malloc(sizeof(row_data) * nrows);
+  double *dD = (double *)malloc(sizeof(double) * nrows);
+  for (int64_t b = 0; b < p->B; ++b) {
+    orc_seq s = seq_of(p, b);
+    for (int64_t h = 0; h < p->N_kv; ++h) {
+      for (int64_t gi = 0; gi < G; ++gi) {
+        const int64_t n = h * G + gi;
+        row_data *rg = rows + gi * s.q_len;
+        double *dg = dD + gi * s.q_len;
+#pragma omp parallel
+        {
+          double *o = (double *)malloc(sizeof(double) * D);
+          double *ob = (double *)malloc(sizeof(double) * D);
+          double *sc = (double *)malloc(sizeof(double) * D);
+#pragma omp for schedule(dynamic, 8)
+          for (int64_t i = 0; i < s.q_len; ++i) {
+            rg[i] = backward_row_data(p, &s, b, n, i, q, k, v, dy, mask, NULL, NULL, NULL, o);
+            dg[i] = row_dD(p, &s, b, n, i, &rg[i], q, k, v, dy, mask, u, o, ob, sc);
+          }
+          free(o); free(ob); free(sc);
+        }
+        /* dQ_i moves by -scale dD_i sum_j P_ij k_j */
+#pragma omp parallel for schedule(dynamic, 8)
+        for (int64_t i = 0; i < s.q_len; ++i) {
+          int64_t lo, hi;
+          if (!key_range(p, &s, i, &lo, &hi)) continue;
+          const double *qi = q + row_q(p, &s, b, n, i);
+          double *e = dq_e + row_q(p, &s, b, n, i);
+          for (int64_t j = lo; j <= hi; ++j) {
+            const double *kj = k + row_kv(p, &s, b, h, j);
+            const double pij = prob(&rg[i], p->scale * dot(qi, kj, D));
+            for (int64_t d = 0; d < D; ++d) e[d] += fabs(p->scale) * dg[i] * pij * fabs(kj[d]);
+          }
+        }
+      }
+      /* dK_j moves by -scale sum_i dD_i P_ij q_i, over the group's query heads */
+#pragma omp parallel for schedule(dynamic, 8)
+      for (int64_t j = 0; j < s.kv_len; ++j) {
+        int64_t lo, hi;
+        if (!query_range(p, &s, j, &lo, &hi)) continue;
+        const double *kj = k + row_kv(p, &s, b, h, j);
+        double *e = dk_e + row_kv(p, &s, b, h, j);
+        for (int64_t gi = 0; gi < G; ++gi) {
+          const int64_t n = h * G + gi;
+          for (int64_t i = lo; i <= hi; ++i) {
+            const double *qi = q + row_q(p, &s, b, n, i);
+            const double pij = prob(&rows[gi * s.q_len + i], p->scale * dot(qi, kj, D));
+            for (int64_t d = 0; d < D; ++d) e[d] += fabs(p->scale) * dD[gi * s.q_len + i] * pij * fabs(qi[d]);
+          }
+        }
+      }
+    }
+  }
+  free(rows);
+  free(dD);
+  return 0;
+}
+
 /* ------------------------------------------------ generated dropout -- */
 
 /* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as

@@ -744,3 +744,48 @@ def test_budget_bounds_the_result_and_ignores_signs():
     for x, y in zip(b[1:], b2[1:]):
         np.testing.assert_allclose(2.0 * x, y, rtol=1e-12, atol=0.0)
     np.testing.assert_allclose(b[0], b2[0], rtol=1e-12, atol=0.0)
+
+
+def test_rounding_error_bound_composition():
+    """The composed bounds are linear in the unit roundoff, and the forward's
+    and dV's are u times their budgets (no D term there)."""
+    g = Geometry(layout="BNSD", B=1, N=4, N_kv=2, D=32, S_q=150, S_kv=150, scale=0.2, sparse_mode=4, pre_tokens=60,
+                 next_tokens=10, keep_prob=0.8)
+    inp = draw(g, 503)
+    pr = to_problem(g)
+    args = (pr, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask)
+    u = 2.0 ** -8
+    e1, e2 = orc.rounding_error(*args, u=u), orc.rounding_error(*args, u=2 * u)
+    for x, y in zip(e1, e2):
+        np.testing.assert_allclose(2.0 * x, y, rtol=1e-12, atol=0.0)
+    b = orc.rounding_budget(*args)
+    np.testing.assert_allclose(e1[0], u * b[0], rtol=1e-12, atol=0.0)
+    np.testing.assert_allclose(e1[3], u * b[3], rtol=1e-12, atol=0.0)
+    for j in (1, 2):  # dQ and dK carry the D term on top of u times their budgets
+        assert np.all(e1[j] >= u * b[j] * (1.0 - 1e-12))
+        assert np.max(e1[j] - u * b[j]) > 0.0
+
+
+def test_rounding_error_d_term_matches_a_perturbed_output():
+    """The D term through the oracle's own backward: with q, k > 0, shifting
+    the given O by sign(dY) u (out_b + |O|) moves D_i by exactly dD_i, and
+    the given-stats backward then moves dQ and dK by exactly the D terms of
+    their bounds (dS_ij moves by -P_ij dD_i, and every P_ij k_j and P_ij q_i
+    is positive)."""
+    S, D = 90, 16
+    g = Geometry(layout="BNSD", B=1, N=2, D=D, S_q=S, S_kv=S, scale=0.3, sparse_mode=4, pre_tokens=25, next_tokens=4)
+    pr = to_problem(g)
+    rng = np.random.default_rng(11)
+    q = rng.uniform(0.1, 1.0, size=(1, 2, S, D))
+    k = rng.uniform(0.1, 1.0, size=(1, 2, S, D))
+    v = rng.normal(size=(1, 2, S, D))
+    dy = rng.normal(size=(1, 2, S, D))
+    u = 2.0 ** -8
+    out, smax, ssum = orc.forward(pr, q, k, v)
+    out_b, dq_b, dk_b, _ = orc.rounding_budget(pr, q, k, v, dy)
+    _, dq_e, dk_e, _ = orc.rounding_error(pr, q, k, v, dy, u=u)
+    shifted = out + np.sign(dy) * u * (out_b + np.abs(out))
+    dq0, dk0, _ = orc.backward(pr, q, k, v, dy, None, given_out=out, given_max=smax, given_sum=ssum)
+    dq1, dk1, _ = orc.backward(pr, q, k, v, dy, None, given_out=shifted, given_max=smax, given_sum=ssum)
+    np.testing.assert_allclose(np.abs(dq1 - dq0), dq_e - u * dq_b, rtol=1e-7, atol=1e-15)
+    np.testing.assert_allclose(np.abs(dk1 - dk0), dk_e - u * dk_b, rtol=1e-7, atol=1e-15)

@@ -27,7 +27,8 @@ from attention_swa_forward_gb300 import build as B
 from attention_swa_forward_gb300 import swa
 from attention_swa_forward_gb300.workloads import Geometry, draw
 from oracle import swa_oracle as orc
-from tests.helpers import TOL_GRAD, TOL_OUT, check_stat, check_tensor, out_dtype, to_problem
+from tests.helpers import (TOL_ABS, TOL_GRAD, TOL_OUT, check_stat, check_tensor, half_ulp, out_dtype, rel_l2,
+                           to_problem)
 
 N_CASES = 64
 
@@ -135,3 +136,71 @@ def test_random_geometry_parity(seed, built):
     check_stat(label, "softmax_sum", res["ssum"], ssum)
     for name, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
         check_tensor(label, name, res[name], ref, dt, TOL_GRAD)
+
+
+# ------------------------------------------------- outside that regime --
+# Scales up to 2.5 D^-0.5, keep_prob down to 0.5 and key ranges of any
+# length.  There the products' 16-bit operands (P~ for out and dV, dS for
+# dQ and dK) carry rounding errors up to u = 2^-8 of each term, D_i is
+# formed from the stored, rounded O, and the sums of those terms' absolute
+# values can far exceed the results.  The element gate adds the oracle's
+# first-order bound of those roundings (orc_rounding_error, u = 2^-8) to
+# the flat one.
+
+EXTREME = {
+    # the two draws outside the regime that missed the flat gate
+    "gqa_39_keys_scale_1.9_keep_0.7": dict(layout="BNSD", B=2, N=6, N_kv=2, D=56, S_q=349, S_kv=39, scale=0.249,
+                                           sparse_mode=4, pre_tokens=130, next_tokens=108, keep_prob=0.7),
+    "mqa_6_keys_fp32": dict(layout="BNSD", B=1, N=3, N_kv=1, D=112, S_q=359, S_kv=6, scale=0.0765, sparse_mode=0,
+                            dtype="fp32"),
+}
+
+
+def extreme_geometry(seed: int) -> dict:
+    rng = np.random.default_rng(2_000_033 * seed + 5)
+    kw = random_geometry(10_000 + seed)
+    D = kw["D"]
+    kw["scale"] = float(D ** -0.5 * rng.uniform(1.0, 2.5) * (-1.0 if rng.random() < 0.15 else 1.0))
+    if kw["layout"] == "BNSD":
+        kw["S_kv"] = int(rng.integers(1, 80))
+    kw.pop("dropout_gen", None), kw.pop("dropout_seed", None), kw.pop("dropout_offset", None)
+    kw.pop("keep_prob", None)
+    if rng.random() < 0.5:
+        kw["keep_prob"] = float(rng.uniform(0.5, 0.95))
+        if rng.random() < 0.4:
+            kw.update(dropout_gen=1, dropout_seed=int(rng.integers(0, 2 ** 31)), dropout_offset=int(rng.integers(0, 64)))
+    return kw
+
+
+_EXTREME_RUNS = sorted(EXTREME) + [f"draw{s}" for s in range(16)]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", _EXTREME_RUNS)
+def test_outside_regime_within_rounding_budget(name, built):
+    kw = EXTREME[name] if name in EXTREME else extreme_geometry(int(name[4:]))
+    geom = Geometry(**kw)
+    inp = draw(geom, 95_000 + sum(map(ord, name)))
+    geom = inp.geom
+    pr = to_problem(geom)
+    res = run_gpu(inp)
+    dt = out_dtype(geom)
+    ops = (inp.q, inp.k, inp.v, inp.dy)
+    if dt == "fp32":
+        ops = tuple(t.to(torch.bfloat16).to(torch.float32) for t in ops)
+    mask = inp.drop_mask
+    if geom.dropout_gen:
+        mask = orc.generate_keep_mask(pr, geom.dropout_seed, geom.dropout_offset)
+    out, smax, ssum = orc.forward(pr, *ops[:3], mask)
+    dq, dk, dv = orc.backward(pr, *ops, mask)
+    bounds = orc.rounding_error(pr, *ops, mask, u=2.0 ** -8)
+    label = f"{name}: {kw}"
+    check_stat(label, "softmax_max", res["smax"], smax)
+    check_stat(label, "softmax_sum", res["ssum"], ssum)
+    for tname, ref, bound, tol in (("out", out, bounds[0], TOL_OUT), ("dq", dq, bounds[1], TOL_GRAD),
+                                   ("dk", dk, bounds[2], TOL_GRAD), ("dv", dv, bounds[3], TOL_GRAD)):
+        got = res[tname]
+        assert np.all(np.isfinite(got)), (label, tname)
+        excess = np.abs(got - ref) - (TOL_ABS + half_ulp(ref, dt) + bound)
+        assert float(excess.max()) <= 0.0, (label, tname, "element gate with the rounding bound", float(excess.max()))
+        assert rel_l2(got, ref) <= tol, (label, tname, "relative L2", rel_l2(got, ref))
