@@ -152,3 +152,41 @@ def test_fp32_storage_of_bf16_values_is_the_bf16_path(D):
         assert r32[n].dtype == torch.float32
         assert torch.equal(r32[n].to(torch.bfloat16), r16[n]), n
     same(r16, r32, names=("smax", "ssum"))
+
+
+def test_concurrent_calls_on_two_streams_match_serial_calls():
+    """Two host threads, each with its own stream, call forward + backward
+    at the same time (the binding's calls release the interpreter lock):
+    each gets exactly the results of a serial call.  The library keeps no
+    shared mutable state between calls beyond once-only kernel attributes."""
+    import threading
+
+    geoms = [Geometry(layout="BNSD", B=1, N=3, D=128, S_q=600, S_kv=600, scale=0.09, sparse_mode=4, pre_tokens=200,
+                      next_tokens=10),
+             Geometry(layout="TND", B=3, N=2, D=64, cu_seqlens_q=[300, 300, 750], cu_seqlens_kv=[300, 300, 750],
+                      scale=0.125, sparse_mode=4, pre_tokens=90, next_tokens=10, keep_prob=0.85, dropout_gen=1,
+                      dropout_seed=5, dropout_offset=2)]
+    inputs = [draw(g, 77 + i) for i, g in enumerate(geoms)]
+    serial = [run(inp.geom, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask) for inp in inputs]
+    results = [[None] * 4 for _ in inputs]
+    errors = []
+
+    def worker(t):
+        try:
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                for rep in range(4):
+                    inp = inputs[t]
+                    results[t][rep] = run(inp.geom, inp.q, inp.k, inp.v, inp.dy, inp.drop_mask)
+        except Exception as e:  # surfaced below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(len(inputs))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for t in range(len(inputs)):
+        for rep in range(4):
+            same(results[t][rep], serial[t], label=f"thread {t} call {rep}")
