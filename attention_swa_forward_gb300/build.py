@@ -1,4 +1,10 @@
-"""Build libswa.so in-tree: nvcc for sm_103a, translation units compiled in parallel."""
+"""Build libswa.so in-tree: nvcc for sm_103a, translation units compiled in parallel.
+
+`build(checked=True)` builds libswa_checked.so from the same sources with
+SWA_CHECKS=1: its kernels test every global load and store against the
+extent of its tensor and report an access outside it as SWA_ERR_BOUNDS
+instead of making it (include/swa.h, swa_workspace_status).  It is a
+testing build; nothing loads it unless asked to (swa.checked_lib())."""
 from __future__ import annotations
 
 import concurrent.futures as cf
@@ -12,6 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libswa.so")
+CHECKED_BUILD_DIR = os.path.join(PKG, "_build_checked")
+CHECKED_LIB_PATH = os.path.join(PKG, "libswa_checked.so")
 SOURCES = ["swa_api.cpp", "swa_fwd.cu", "swa_fwd_pair.cu", "swa_bwd_dkv.cu", "swa_bwd_dq.cu", "swa_aux.cu",
            "swa_noalloc.cu", "swa_host.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -31,23 +39,27 @@ def _inputs():
     return [f for f in files if os.path.isfile(f)]
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def is_stale(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every translation unit for sm_103a and link libswa.so; returns its path."""
-    if not force and not is_stale():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Compile every translation unit for sm_103a and link libswa.so (or,
+    with `checked`, the bounds-checked libswa_checked.so); returns its path."""
+    lib_path = CHECKED_LIB_PATH if checked else LIB_PATH
+    build_dir = CHECKED_BUILD_DIR if checked else BUILD_DIR
+    if not force and not is_stale(lib_path):
+        return lib_path
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
+    defines = ["-DSWA_CHECKS=1"] if checked else []
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
+        cmd = [nvcc, *ARCH, *FLAGS, *defines, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -57,13 +69,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -29,6 +29,7 @@ namespace {
 thread_local std::string t_last_error = "no error";
 std::atomic<int32_t> g_stall{0};  // swa_debug_stall: read into Geometry::stall by every call
 std::atomic<int32_t> g_fwd_pairs{0};  // swa_debug_forward_pairs: 0 by size, 1 always, 2 never
+std::atomic<int64_t> g_extent_slack{0};  // swa_debug_extent_slack: taken off every extent of the bounds checks
 thread_local cudaEvent_t t_ev[8] = {};  // start/stop around: forward, dK/dV pass, dQ pass, preprocess
 
 swa_status_t fail(swa_status_t st, const char* fmt, ...) {
@@ -185,6 +186,13 @@ swa_status_t make_plan(const swa_params_t* p, Plan& plan) {
     plan.kv_rows = p->T_kv;
     plan.mask_bits = bits;
   }
+  // tensor extents, for the bounds-checked build's device-side checks
+  g.n_q_elems = plan.q_rows * p->N * p->D;
+  g.n_kv_elems = plan.kv_rows * g.N_kv * p->D;
+  g.n_stats = plan.q_rows * p->N;
+  g.n_mask_bytes = (g.has_mask && !g.drop_gen) ? (plan.mask_bits + 7) / 8 : 0;
+  const int64_t slack = g_extent_slack.load(std::memory_order_relaxed);
+  for (int64_t* x : {&g.n_q_elems, &g.n_kv_elems, &g.n_stats, &g.n_mask_bytes}) *x = std::max<int64_t>(*x - slack, 0);
   // The window cannot reach further than the longest sequence: clamp.
   const int64_t lim = max_len + 1;
   g.pre = static_cast<int32_t>(std::min(std::max(p->pre_tokens, -lim), lim));
@@ -477,7 +485,7 @@ swa_status_t swa_forward(const swa_params_t* p, const void* q, const void* k, co
   a.err = static_cast<int32_t*>(workspace);
 
   std::vector<SeqDesc> descs = build_descs(plan, true);
-  if (descs.empty()) {  // nothing to launch; otherwise the first launch clears the status word itself
+  if (descs.empty() || SWA_CHECKS) {  // otherwise the first launch clears the status word itself
     e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
   }
@@ -501,7 +509,7 @@ swa_status_t swa_forward(const swa_params_t* p, const void* q, const void* k, co
   int launches = 0;
   auto one = [&](const auto& t) {
     FwdArgs at = a;
-    at.clear_err = launches++ == 0 ? 1 : 0;
+    at.clear_err = (launches++ == 0 && !SWA_CHECKS) ? 1 : 0;
     return pair ? launch_forward_pair(at, t, mq, mk, mv, s) : launch_forward(at, t, mq, mk, mv, s);
   };
   e = run_tables(descs, one, one);
@@ -570,8 +578,13 @@ swa_status_t swa_backward(const swa_params_t* p, const void* q, const void* k, c
   pa.ssum = softmax_sum;
   pa.lse2 = lse2;
   pa.dsum = dsum;
+  cudaError_t e = cudaSuccess;
+  if (SWA_CHECKS) {  // the release preprocess clears the status word itself
+    e = cudaMemsetAsync(ws, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
+  }
   if (t_ev[6]) cudaEventRecord(t_ev[6], s);
-  cudaError_t e = launch_prep(pa, s);
+  e = launch_prep(pa, s);
   if (t_ev[7]) cudaEventRecord(t_ev[7], s);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
 
@@ -635,6 +648,8 @@ swa_status_t swa_workspace_status(const void* workspace, swa_stream_t stream) {
   int32_t word = 0;
   e = cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "reading the workspace header");
+  if (word == kErrBounds)
+    return fail(SWA_ERR_BOUNDS, "the bounds-checked build skipped an access outside its tensor (code %d)", word);
   if (word != 0) return fail(SWA_ERR_TIMEOUT, "a kernel gave up a bounded wait (code %d)", word);
   return SWA_OK;
 }
@@ -680,6 +695,7 @@ swa_status_t swa_debug_schedule(const swa_params_t* p, int32_t pass, int32_t* it
 }
 
 void swa_debug_stall(int32_t kernels) { g_stall.store(kernels & 7, std::memory_order_relaxed); }
+void swa_debug_extent_slack(int64_t elems) { g_extent_slack.store(std::max<int64_t>(elems, 0), std::memory_order_relaxed); }
 void swa_debug_forward_pairs(int32_t mode) {
   g_fwd_pairs.store(mode >= 0 && mode <= 2 ? mode : 0, std::memory_order_relaxed);
 }

@@ -31,12 +31,12 @@ __global__ void __launch_bounds__(256) swa_prep_kernel(const PrepArgs a) {
   const int lane = threadIdx.x & 31;
   griddep_wait();  // dY, O and the statistics come from earlier grids
   griddep_launch_dependents();
-  if (blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0;  // fresh error word for this backward call
+  if (!SWA_CHECKS && blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0;  // fresh error word for this backward call
   if (row >= a.rows) return;
   const int D = a.g.D;
   const int64_t base = row * D + lane * kPer;
   float acc = 0.f;
-  if (lane * kPer >= D) {
+  if (lane * kPer >= D || !in_bounds(base, kPer, a.g.n_q_elems, a.err)) {
     // past the row's last element
   } else if (kPer == 4) {
     const uint2 dy = __ldg(reinterpret_cast<const uint2*>(a.dy + base));
@@ -60,9 +60,10 @@ __global__ void __launch_bounds__(256) swa_prep_kernel(const PrepArgs a) {
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, m);
   if (lane == 0) {
-    const float l = a.ssum[row];
     // workspace position: head-major (row = t*N + n in TND, already head-major in BNSD)
     const int64_t ws = a.g.layout == 0 ? row : (row % a.g.N) * a.g.T_q + row / a.g.N;
+    if (!in_bounds(row, 1, a.g.n_stats, a.err) || !in_bounds(ws, 1, a.g.n_stats, a.err)) return;
+    const float l = a.ssum[row];
     a.dsum[ws] = acc;
     a.lse2[ws] = (l > 0.f) ? a.smax[row] * kLog2e + __log2f(l) : INFINITY;
   }
@@ -84,7 +85,7 @@ __global__ void __launch_bounds__(256, 4) swa_prep_wide_kernel(const PrepArgs a)
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   griddep_wait();  // dY, O and the statistics come from earlier grids
   griddep_launch_dependents();
-  if (blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0;  // fresh error word for this backward call
+  if (!SWA_CHECKS && blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0;  // fresh error word for this backward call
   const int64_t row0 = warp * (kRowsPerStep * kSteps) + lane / kLanesPerRow;
   const int col = (lane % kLanesPerRow) * 8;
   // row r of step k is row0 + k * kRowsPerStep: one base pointer per tensor
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(256, 4) swa_prep_wide_kernel(const PrepArgs a)
   uint4 dy[kSteps], o[kSteps];
 #pragma unroll
   for (int k = 0; k < kSteps; ++k) {
-    if (k < nvalid) {
+    if (k < nvalid && in_bounds((row0 + k * kRowsPerStep) * D + col, 8, a.g.n_q_elems, a.err)) {
       dy[k] = __ldg(pdy + k * kStride);
       o[k] = __ldg(po + k * kStride);
     } else {
@@ -118,8 +119,9 @@ __global__ void __launch_bounds__(256, 4) swa_prep_wide_kernel(const PrepArgs a)
     for (int m = kLanesPerRow / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, m);
     const int64_t row = row0 + k * kRowsPerStep;
     if (lane % kLanesPerRow == 0 && k < nvalid) {
-      const float l = a.ssum[row];
       const int64_t ws = a.g.layout == 0 ? row : (row % a.g.N) * a.g.T_q + row / a.g.N;
+      if (!in_bounds(row, 1, a.g.n_stats, a.err) || !in_bounds(ws, 1, a.g.n_stats, a.err)) continue;
+      const float l = a.ssum[row];
       a.dsum[ws] = acc;
       a.lse2[ws] = (l > 0.f) ? a.smax[row] * kLog2e + __log2f(l) : INFINITY;
     }

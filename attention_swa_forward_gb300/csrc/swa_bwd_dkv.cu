@@ -313,10 +313,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q4 = 0; q4 < 4; ++q4) bits[k4][q4] = 0u;
           if (i < sq.q_len) {
             const int64_t si = ws_stat_index(g, sq, w.b, qn, i);
-            l2[k4] = a.lse2[si];
-            dd[k4] = a.dsum[si];
+            if (in_bounds(si, 1, g.n_stats, a.err)) {
+              l2[k4] = a.lse2[si];
+              dd[k4] = a.dsum[si];
+            }
             if constexpr (DROP) dd[k4] *= g.keep;  // the compute warps form P * (z dP - keep D)
-            if constexpr (DM == 1) load_keep_bits(a.mask, sq, qn, i, j0, bits[k4]);
+            if constexpr (DM == 1) load_keep_bits(a.mask, sq, qn, i, j0, bits[k4], g.n_mask_bytes, a.err);
           }
         }
         if (it >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait(&bar[kBarDsFull + region_of<kR>(it - 2)],
@@ -650,7 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kv_valid) {
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4)
-              if (ch * 32 + q4 * 8 < g.D) store8<F16>(dbase, dst + ch * 32 + q4 * 8, &o[q4 * 8], true);
+              if (ch * 32 + q4 * 8 < g.D && in_bounds(dst + ch * 32 + q4 * 8, 8, g.n_kv_elems, a.err))
+                store8<F16>(dbase, dst + ch * 32 + q4 * 8, &o[q4 * 8], true);
           }
         } else {
 #pragma unroll
@@ -667,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c = lane % kChunks;
         for (int rr = wq * kRowsPerStore + lane / kChunks; rr < kTileN; rr += 4 * kRowsPerStore) {
           const int gj = j0 + rr;
-          if (gj < sq.kv_len && c * 8 < g.D)
+          if (gj < sq.kv_len && c * 8 < g.D && in_bounds(kv_elem(g, sq, w.b, w.n, gj) + c * 8, 8, g.n_kv_elems, a.err))
             *reinterpret_cast<uint4*>(static_cast<uint16_t*>(dbase) + kv_elem(g, sq, w.b, w.n, gj) + c * 8) =
                 ld_chunk_sw128(stage, rr, c);
         }

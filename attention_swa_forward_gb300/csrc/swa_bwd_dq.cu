@@ -239,8 +239,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     float lse2 = INFINITY, drow = 0.f;
     if (row_valid) {
       const int64_t si = ws_stat_index(g, sq, w.b, w.n, i);
-      lse2 = a.lse2[si];
-      drow = a.dsum[si];
+      if (in_bounds(si, 1, g.n_stats, a.err)) {
+        lse2 = a.lse2[si];
+        drow = a.dsum[si];
+      }
       if constexpr (DM != 0) drow *= g.keep;  // the loop forms P * (z dP - keep D)
     }
     // keep bits of this thread's 64 key columns of key tile j (two words)
@@ -248,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       kb0 = kb1 = 0xFFFFFFFFu;
       if (DM == 1 && row_valid) {
         uint32_t bits[4];
-        load_keep_bits(a.mask, sq, w.n, i, (kv_t0 + j) * kTileN, bits);
+        load_keep_bits(a.mask, sq, w.n, i, (kv_t0 + j) * kTileN, bits, g.n_mask_bytes, a.err);
         kb0 = h ? bits[2] : bits[0];
         kb1 = h ? bits[3] : bits[1];
       } else if (DM == 2) {
@@ -369,7 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (row_valid) {
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4)
-              if (h * kCols + ch * 32 + q4 * 8 < g.D) store8<F16>(a.dq, dst + ch * 32 + q4 * 8, &o[q4 * 8], true);
+              if (h * kCols + ch * 32 + q4 * 8 < g.D && in_bounds(dst + ch * 32 + q4 * 8, 8, g.n_q_elems, a.err))
+                store8<F16>(a.dq, dst + ch * 32 + q4 * 8, &o[q4 * 8], true);
           }
         } else {
           // staged in the Q buffer (every S is done) for whole-row stores below
@@ -388,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c = lane % kChunks;
         for (int rr = warp * kRowsPerStore + lane / kChunks; rr < kTileM; rr += 8 * kRowsPerStore) {
           const int gi = q0 + rr;
-          if (gi < sq.q_len && c * 8 < g.D)
+          if (gi < sq.q_len && c * 8 < g.D && in_bounds(q_elem(g, sq, w.b, w.n, gi) + c * 8, 8, g.n_q_elems, a.err))
             *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + q_elem(g, sq, w.b, w.n, gi) + c * 8) =
                 ld_chunk_sw128(s.q, rr, c);
         }

@@ -102,17 +102,41 @@ __device__ __forceinline__ void tma_rows(uint8_t* dst, const CUtensorMap* map, u
   }
 }
 
+// --------------------------------------------------- bounds-checked build --
+// Built with SWA_CHECKS = 1, the kernels test every global load and store
+// against the extent of its tensor first (Geometry::n_*): an access outside
+// it is skipped and kErrBounds recorded in the status word, so an indexing
+// or scheduling error shows up as a status instead of as a memory fault.
+// The release build compiles the tests away.  (TMA copies need no test: the
+// tensor maps bound them.)  SWA_CHECKS itself is set in swa_internal.h.
+__device__ __forceinline__ bool in_bounds(int64_t first, int64_t count, int64_t extent, int32_t* err) {
+  if constexpr (SWA_CHECKS == 0) {
+    return true;
+  } else {
+    if (first >= 0 && count >= 0 && first + count <= extent) return true;
+    atomicCAS(err, 0, static_cast<int32_t>(kErrBounds));
+    return false;
+  }
+}
+
 // 128 dropout keep bits of row i for keys [j0, j0+128): bit t of the result
 // (word t >> 5) is key j0 + t.  Bits past the sequence's last key are 0.
 // Element order: mask_base + (n*Sq + i)*Skv + j, least significant bit first.
+// `extent` (mask bytes) and `err` serve the bounds-checked build.
 __device__ __forceinline__ void load_keep_bits(const uint8_t* __restrict__ mask, const SeqInfo& s, int n, int i,
-                                               int j0, uint32_t (&bits)[4]) {
+                                               int j0, uint32_t (&bits)[4], int64_t extent, int32_t* err) {
   const int cnt = min(128, s.kv_len - j0);
   const int64_t e0 = s.mask_base + (static_cast<int64_t>(n) * s.q_len + i) * s.kv_len + j0;
   uint32_t w[5] = {0u, 0u, 0u, 0u, 0u};
   const int sh = static_cast<int>(e0 & 7);
   const uint8_t* p = mask + (e0 >> 3);
-  if ((e0 & 127) == 0 && cnt == 128) {
+  const bool whole = (e0 & 127) == 0 && cnt == 128;
+  if (!in_bounds(e0 >> 3, whole ? 16 : (sh + cnt + 7) >> 3, extent, err)) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) bits[k] = 0u;
+    return;
+  }
+  if (whole) {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
     w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
   } else {

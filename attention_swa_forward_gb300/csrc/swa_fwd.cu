@@ -204,14 +204,14 @@ __global__ void __launch_bounds__(224, 1)
     // Keep bits read from the mask are fetched one tile ahead, so their
     // global-load latency is not on the softmax's path.
     uint32_t next_bits[4] = {0u, 0u, 0u, 0u};
-    if (DM == 1 && n_kv > 0 && row_valid) load_keep_bits(a.mask, sq, w.n, i, kv_t0 * kTileN, next_bits);
+    if (DM == 1 && n_kv > 0 && row_valid) load_keep_bits(a.mask, sq, w.n, i, kv_t0 * kTileN, next_bits, g.n_mask_bytes, a.err);
     for (int it = 0; ok && it < n_kv; ++it) {
       const int sb = it & 1;
       uint32_t bits[4] = {~0u, ~0u, ~0u, ~0u};
       if (DM == 1) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) bits[u] = next_bits[u];
-        if (it + 1 < n_kv && row_valid) load_keep_bits(a.mask, sq, w.n, i, (kv_t0 + it + 1) * kTileN, next_bits);
+        if (it + 1 < n_kv && row_valid) load_keep_bits(a.mask, sq, w.n, i, (kv_t0 + it + 1) * kTileN, next_bits, g.n_mask_bytes, a.err);
       }
       // warp-uniform outcome: the tcgen05.ld below is warp-collective
       if (!s_ready && !__all_sync(0xFFFFFFFFu, mbar_wait(&s.s_full[sb], (it >> 1) & 1, a.err, kErrFwdSoftmax))) {
@@ -374,14 +374,17 @@ __global__ void __launch_bounds__(224, 1)
         if (row_valid) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
-            if (ch * 32 + q4 * 8 < g.D) store8<F16>(a.out, orow + ch * 32 + q4 * 8, &o[q4 * 8], g.out_f32);
+            if (ch * 32 + q4 * 8 < g.D && in_bounds(orow + ch * 32 + q4 * 8, 8, g.n_q_elems, a.err))
+              store8<F16>(a.out, orow + ch * 32 + q4 * 8, &o[q4 * 8], g.out_f32);
         }
       }
       if (row_valid) {
         const int64_t si = stat_index(g, sq, w.b, w.n, i);
         const bool empty = (m_true == -INFINITY);
-        a.smax[si] = empty ? -INFINITY : m_true * kLn2;
-        a.ssum[si] = empty ? 0.f : l * ex2_approx(m_use - m_true);
+        if (in_bounds(si, 1, g.n_stats, a.err)) {
+          a.smax[si] = empty ? -INFINITY : m_true * kLn2;
+          a.ssum[si] = empty ? 0.f : l * ex2_approx(m_use - m_true);
+        }
       }
     }
   }

@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       uint32_t bits[4] = {~0u, ~0u, ~0u, ~0u};
       if (DM == 1) {
         bits[0] = bits[1] = bits[2] = bits[3] = 0u;
-        if (row_valid) load_keep_bits(a.mask, sq, w.n, i, (kv_t0 + it) * kTileN, bits);
+        if (row_valid) load_keep_bits(a.mask, sq, w.n, i, (kv_t0 + it) * kTileN, bits, g.n_mask_bytes, a.err);
       }
       // warp-uniform outcome: the tcgen05.ld below is warp-collective
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(&s.s_full[h], it & 1, a.err, kErrFwdSoftmax))) {
@@ -406,14 +406,17 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         if (row_valid) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
-            if (ch * 32 + q4 * 8 < g.D) store8<F16>(a.out, orow + ch * 32 + q4 * 8, &o[q4 * 8], g.out_f32);
+            if (ch * 32 + q4 * 8 < g.D && in_bounds(orow + ch * 32 + q4 * 8, 8, g.n_q_elems, a.err))
+              store8<F16>(a.out, orow + ch * 32 + q4 * 8, &o[q4 * 8], g.out_f32);
         }
       }
       if (row_valid) {
         const int64_t si = stat_index(g, sq, w.b, w.n, i);
         const bool empty = (m_true == -INFINITY);
-        a.smax[si] = empty ? -INFINITY : m_true * kPairLn2;
-        a.ssum[si] = empty ? 0.f : l * ex2_approx(m_use - m_true);
+        if (in_bounds(si, 1, g.n_stats, a.err)) {
+          a.smax[si] = empty ? -INFINITY : m_true * kPairLn2;
+          a.ssum[si] = empty ? 0.f : l * ex2_approx(m_use - m_true);
+        }
       }
     }
   }

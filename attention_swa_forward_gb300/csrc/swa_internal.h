@@ -76,6 +76,15 @@ cudaError_t set_smem_limit(Kernel kernel, size_t smem, std::atomic<uint64_t>& do
 }
 
 // Error codes a kernel stores into WsHeader::error.
+// 1: the bounds-checked build (libswa_checked.so), whose kernels test every
+// global load and store against its tensor's extent and record kErrBounds
+// instead of making it.  Its host code clears the status word with a memset
+// before a call's first launch, so that no grid's clear can race with a
+// bounds record of another grid's block.
+#ifndef SWA_CHECKS
+#define SWA_CHECKS 0
+#endif
+
 enum : int32_t {
   kErrFwdLoad = 1,
   kErrFwdMma = 2,
@@ -83,6 +92,7 @@ enum : int32_t {
   kErrBwdLoad = 11,
   kErrBwdMma = 12,
   kErrBwdCompute = 13,
+  kErrBounds = 21,  // bounds-checked build: an access outside its tensor was skipped
 };
 
 struct Geometry {
@@ -106,6 +116,12 @@ struct Geometry {
   int32_t out_f32;    // outputs (out, dq, dk, dv) are fp32; the kernels then read bf16 copies of the inputs
   int32_t stall;      // test hook (swa_debug_stall): kStall* bits of kernels whose compute warps first wait
                       // on a barrier that nothing completes, so that the bounded wait runs out
+  // Extents of the caller's tensors, which the bounds-checked build
+  // (SWA_CHECKS = 1) tests every global access of the kernels against.
+  int64_t n_q_elems;     // elements of q, dy, out and dq
+  int64_t n_kv_elems;    // elements of k, v, dk and dv
+  int64_t n_stats;       // query rows x heads: softmax_max, softmax_sum, lse2 and D entries
+  int64_t n_mask_bytes;  // bytes of the packed keep mask (0 without one)
 };
 
 // Geometry::stall bits.

@@ -12,8 +12,9 @@
 // The scratch is one file-scope device array of kNoAllocScratchBytes.  Every
 // GPU that loads this library holds it until the process exits, and every
 // call on that GPU shares it: two calls whose kernels overlap on the GPU race
-// on it.  Whatever must start at zero (the status word) is cleared by the
-// backward's own first kernel on every call.
+// on it.  Whatever must start at zero (the status word) is cleared on every
+// call: by the backward's own first kernel, or by a memset in the
+// bounds-checked build.
 #include "swa.h"
 
 #include <cuda_runtime.h>

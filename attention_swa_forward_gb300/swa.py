@@ -6,6 +6,7 @@ compiled library is missing, every call raises -- there is no fallback path.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -14,6 +15,7 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libswa.so")
+CHECKED_LIB_PATH = os.path.join(_PKG, "libswa_checked.so")
 
 SWA_OK = 0
 SWA_ERR_PARAM_NULLPTR = 161001
@@ -22,6 +24,7 @@ SWA_ERR_UNSUPPORTED = 161100
 SWA_ERR_WORKSPACE = 161101
 SWA_ERR_CUDA = 161102
 SWA_ERR_TIMEOUT = 161103
+SWA_ERR_BOUNDS = 161104
 LAYOUTS = {"BNSD": 0, "TND": 1}
 DTYPES = {"bf16": 0, "fp16": 1, "fp32": 2}
 
@@ -60,62 +63,98 @@ class SwaParams(ctypes.Structure):
 
 
 _lib = None
+_checked_lib = None
 _lock = threading.Lock()
+_local = threading.local()  # .lib: the library this thread's calls go to, when set by using()
 
 
 def lib() -> ctypes.CDLL:
-    """Load libswa.so (built in-tree by ``build.build()``); raise if it is absent."""
+    """The library this thread's calls go to: libswa.so (built in-tree by
+    ``build.build()``), unless ``using()`` chose another; raise if it is absent."""
+    override = getattr(_local, "lib", None)
+    if override is not None:
+        return override
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIB_PATH):
-                raise ImportError(f"{LIB_PATH} is missing: build it with attention_swa_forward_gb300.build.build()")
-            L = ctypes.CDLL(LIB_PATH)
-            P = ctypes.POINTER(SwaParams)
-            vp, sz = ctypes.c_void_p, ctypes.c_size_t
-            st = ctypes.c_int
-            L.swa_params_default.argtypes = [P]
-            L.swa_params_default.restype = None
-            L.swa_forward_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
-            L.swa_forward_workspace_size.restype = st
-            L.swa_backward_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
-            L.swa_backward_workspace_size.restype = st
-            L.swa_forward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
-            L.swa_forward.restype = st
-            L.swa_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
-            L.swa_backward.restype = st
-            L.swa_backward_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
-            L.swa_backward_noalloc.restype = st
-            L.swa_workspace_status.argtypes = [vp, vp]
-            L.swa_workspace_status.restype = st
-            L.swa_dropout_mask.argtypes = [P, vp, sz, vp]
-            L.swa_dropout_mask.restype = st
-            ci = ctypes.c_int
-            L.swa_step_host_buffer_size.argtypes = [P, ci, ctypes.POINTER(sz)]
-            L.swa_step_host_buffer_size.restype = st
-            L.swa_step_host.argtypes = [P, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
-            L.swa_step_host.restype = st
-            L.swa_step_host_status.argtypes = [P, ci, vp, vp]
-            L.swa_step_host_status.restype = st
-            L.swa_set_timing_events.argtypes = [vp]
-            L.swa_set_timing_events.restype = None
-            L.swa_debug_schedule.argtypes = [P, ctypes.c_int32, vp, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]
-            L.swa_debug_schedule.restype = st
-            L.swa_debug_stall.argtypes = [ctypes.c_int32]
-            L.swa_debug_stall.restype = None
-            L.swa_debug_forward_pairs.argtypes = [ctypes.c_int32]
-            L.swa_debug_forward_pairs.restype = None
-            L.swa_last_error.argtypes = []
-            L.swa_last_error.restype = ctypes.c_char_p
-            _lib = L
+            _lib = _open(LIB_PATH, "attention_swa_forward_gb300.build.build()")
     return _lib
+
+
+def checked_lib() -> ctypes.CDLL:
+    """The bounds-checked build, libswa_checked.so (``build.build(checked=True)``):
+    the same kernels with every global load and store tested against its
+    tensor's extent; an access outside it is skipped and reported as
+    SWA_ERR_BOUNDS by swa_workspace_status."""
+    global _checked_lib
+    with _lock:
+        if _checked_lib is None:
+            _checked_lib = _open(CHECKED_LIB_PATH, "attention_swa_forward_gb300.build.build(checked=True)")
+    return _checked_lib
+
+
+@contextlib.contextmanager
+def using(library: ctypes.CDLL):
+    """Route this thread's calls of this module to `library` (e.g. checked_lib())."""
+    before = getattr(_local, "lib", None)
+    _local.lib = library
+    try:
+        yield library
+    finally:
+        _local.lib = before
+
+
+def _open(path: str, how: str) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with {how}")
+    L = ctypes.CDLL(path)
+    P = ctypes.POINTER(SwaParams)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    st = ctypes.c_int
+    L.swa_params_default.argtypes = [P]
+    L.swa_params_default.restype = None
+    L.swa_forward_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
+    L.swa_forward_workspace_size.restype = st
+    L.swa_backward_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
+    L.swa_backward_workspace_size.restype = st
+    L.swa_forward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.swa_forward.restype = st
+    L.swa_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.swa_backward.restype = st
+    L.swa_backward_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.swa_backward_noalloc.restype = st
+    L.swa_workspace_status.argtypes = [vp, vp]
+    L.swa_workspace_status.restype = st
+    L.swa_dropout_mask.argtypes = [P, vp, sz, vp]
+    L.swa_dropout_mask.restype = st
+    ci = ctypes.c_int
+    L.swa_step_host_buffer_size.argtypes = [P, ci, ctypes.POINTER(sz)]
+    L.swa_step_host_buffer_size.restype = st
+    L.swa_step_host.argtypes = [P, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.swa_step_host.restype = st
+    L.swa_step_host_status.argtypes = [P, ci, vp, vp]
+    L.swa_step_host_status.restype = st
+    L.swa_set_timing_events.argtypes = [vp]
+    L.swa_set_timing_events.restype = None
+    L.swa_debug_schedule.argtypes = [P, ctypes.c_int32, vp, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]
+    L.swa_debug_schedule.restype = st
+    L.swa_debug_stall.argtypes = [ctypes.c_int32]
+    L.swa_debug_stall.restype = None
+    L.swa_debug_forward_pairs.argtypes = [ctypes.c_int32]
+    L.swa_debug_forward_pairs.restype = None
+    L.swa_debug_extent_slack.argtypes = [ctypes.c_int64]
+    L.swa_debug_extent_slack.restype = None
+    L.swa_last_error.argtypes = []
+    L.swa_last_error.restype = ctypes.c_char_p
+    return L
 
 
 def exported_symbols():
     return ["swa_params_default", "swa_forward_workspace_size", "swa_forward", "swa_backward_workspace_size",
             "swa_backward", "swa_backward_noalloc", "swa_workspace_status", "swa_set_timing_events",
             "swa_last_error", "swa_dropout_mask", "swa_step_host_buffer_size", "swa_step_host",
-            "swa_step_host_status", "swa_debug_schedule", "swa_debug_stall", "swa_debug_forward_pairs"]
+            "swa_step_host_status", "swa_debug_schedule", "swa_debug_stall", "swa_debug_forward_pairs",
+            "swa_debug_extent_slack"]
 
 
 def _check(status: int):
@@ -255,6 +294,13 @@ def swa_debug_forward_pairs(mode: int):
     """Test hook: forward kernel choice at D <= 64 (0 by size, 1 always one
     CTA per pair of query tiles, 2 never)."""
     lib().swa_debug_forward_pairs(int(mode))
+
+
+def swa_debug_extent_slack(elems: int):
+    """Test hook: elements taken off every extent the bounds-checked build
+    tests the kernels' accesses against (the release build ignores it); 0
+    turns it off."""
+    lib().swa_debug_extent_slack(int(elems))
 
 
 # ------------------------------------------------------- torch convenience --

@@ -95,7 +95,9 @@ typedef enum {
   SWA_ERR_UNSUPPORTED = 161100,   /* valid per the API but not built (e.g. D past 128 or not a multiple of 8) */
   SWA_ERR_WORKSPACE = 161101,     /* workspace NULL or smaller than the size query says */
   SWA_ERR_CUDA = 161102,          /* a CUDA runtime call failed (text in swa_last_error) */
-  SWA_ERR_TIMEOUT = 161103        /* a kernel gave up a bounded wait (swa_workspace_status) */
+  SWA_ERR_TIMEOUT = 161103,       /* a kernel gave up a bounded wait (swa_workspace_status) */
+  SWA_ERR_BOUNDS = 161104         /* bounds-checked build only: a kernel skipped an access outside its
+                                     tensor (swa_workspace_status) */
 } swa_status_t;
 
 typedef struct {
@@ -257,7 +259,10 @@ SWA_API swa_status_t swa_dropout_mask(const swa_params_t *p, uint8_t *mask, size
 
 /* Wait for `stream`, then report whether any kernel of the last call that
  * used `workspace` gave up a bounded wait: SWA_OK or SWA_ERR_TIMEOUT
- * (SWA_ERR_CUDA if the stream itself failed). */
+ * (SWA_ERR_CUDA if the stream itself failed).  In the bounds-checked build
+ * (compiled with SWA_CHECKS = 1; its kernels test every global load and
+ * store against the extent of its tensor and skip it when outside) a
+ * skipped access reports SWA_ERR_BOUNDS. */
 SWA_API swa_status_t swa_workspace_status(const void *workspace, swa_stream_t stream);
 
 /* Measurement support.  `events` is NULL (stop recording) or an array of
@@ -309,11 +314,22 @@ SWA_API void swa_set_timing_events(void *const *events);
  * kernel.  0 (the default): one CTA per pair of query tiles when the pairs
  * fill every SM at least once, else one CTA per query tile; 1: always pairs;
  * 2: never.  Both kernels compute the same results; the switch lets tests
- * reach each on small problems.  Process-wide. */
+ * reach each on small problems.  Process-wide.
+ *
+ * swa_debug_extent_slack: every later call takes `elems` (>= 0; negative
+ * values count as 0) off each tensor extent that the bounds-checked build
+ * (libswa_checked.so, see swa_workspace_status) tests the kernels' global
+ * loads and stores against, so that accesses at the end of q / out / dQ,
+ * k / dK / dV, the statistics and a stored keep mask count as outside their
+ * tensor: they are skipped and the call's status word reports
+ * SWA_ERR_BOUNDS.  It exercises that path with accesses that are all in
+ * range.  The release build has no such checks and ignores it; the
+ * outputs of a call it affects are undefined.  Process-wide; 0 turns it off. */
 SWA_API swa_status_t swa_debug_schedule(const swa_params_t *p, int32_t pass, int32_t *items, int64_t capacity,
                                         int64_t *count);
 SWA_API void swa_debug_stall(int32_t kernels);
 SWA_API void swa_debug_forward_pairs(int32_t mode);
+SWA_API void swa_debug_extent_slack(int64_t elems);
 
 /* Text describing the last non-OK status returned on this thread. */
 SWA_API const char *swa_last_error(void);
