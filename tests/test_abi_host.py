@@ -38,6 +38,22 @@ def test_exports_every_declared_symbol(lib):
     assert sorted(swa.exported_symbols()) == declared
 
 
+def test_checked_build_exports_the_same_symbols():
+    """The bounds-checked build (SWA_CHECKS=1) compiles from the same sources
+    and loads with the same C ABI; only its kernels differ."""
+    path = B.build(checked=True)
+    assert path == swa.CHECKED_LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    assert sorted(set(re.findall(r" T (swa_\w+)", out))) == _declared_symbols()
+    checked = swa.checked_lib()
+    assert checked is not swa.lib()
+    with swa.using(checked):
+        assert swa.lib() is checked
+        p = swa.Params(Geometry("BNSD", 1, 2, 64, S_q=300, S_kv=300, sparse_mode=0))
+        assert swa.swa_backward_workspace_size(p) > 0
+    assert swa.lib() is not checked
+
+
 def test_ctypes_struct_matches_c_layout(tmp_path):
     src = tmp_path / "layout.c"
     src.write_text(
