@@ -171,6 +171,18 @@ def draw_workload(name: str) -> Inputs:
     return draw(w.geom, w.seed, w.lengths)
 
 
+def workload_geometry(name: str) -> Geometry:
+    """The geometry draw_workload(name) uses (sequence lengths drawn from the
+    workload's seed the same way), without drawing its tensors."""
+    w = WORKLOADS[name]
+    if w.lengths is None:
+        return w.geom
+    g = torch.Generator("cpu").manual_seed(int(w.seed))
+    count, lo, hi = w.lengths
+    cu = np.cumsum(torch.randint(lo, hi + 1, (count,), generator=g).tolist()).tolist()
+    return Geometry(**{**w.geom.as_dict(), "B": count, "cu_seqlens_q": cu, "cu_seqlens_kv": list(cu)})
+
+
 def _local_positions(geom: Geometry, q_side: bool) -> torch.Tensor:
     """Index of every row inside its own sequence, shaped to broadcast over
     the q-side ([B,N,S_q,1] / [T_q,1,1]) or k-side layout."""

@@ -38,6 +38,21 @@ def test_exports_every_declared_symbol(lib):
     assert sorted(swa.exported_symbols()) == declared
 
 
+def test_workload_geometry_is_the_drawn_geometry():
+    """workload_geometry() gives the sequence lengths draw_workload() draws
+    (checked on a head dim of 8, which leaves the length draw unchanged)."""
+    from attention_swa_forward_gb300.workloads import WORKLOADS, draw, workload_geometry
+    for name, w in WORKLOADS.items():
+        g = workload_geometry(name)
+        if w.lengths is None:
+            assert g is w.geom
+            continue
+        small = Geometry(**{**w.geom.as_dict(), "D": 8})
+        drawn = draw(small, w.seed, w.lengths, with_dy=False).geom
+        assert g.cu_seqlens_q == drawn.cu_seqlens_q and g.cu_seqlens_kv == drawn.cu_seqlens_kv
+        assert g.D == w.geom.D and g.B == w.lengths[0]
+
+
 def test_checked_build_exports_the_same_symbols():
     """The bounds-checked build (SWA_CHECKS=1) compiles from the same sources
     and loads with the same C ABI; only its kernels differ."""

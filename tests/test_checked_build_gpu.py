@@ -13,14 +13,16 @@ things are checked here:
 - with swa_debug_extent_slack taking 8 elements off every extent, in-range
   accesses at the tensors' ends count as outside and the status is
   SWA_ERR_BOUNDS, for the forward and for the backward, while the release
-  build, which has no checks, ignores the hook.
+  build, which has no checks, ignores the hook;
+- at the full size of each of the five workloads the checked build records
+  nothing and matches the release build bit for bit.
 """
 import pytest
 import torch
 
 from attention_swa_forward_gb300 import build as B
 from attention_swa_forward_gb300 import swa
-from attention_swa_forward_gb300.workloads import Geometry, draw
+from attention_swa_forward_gb300.workloads import WORKLOAD_ORDER, Geometry, draw, workload_geometry
 
 pytestmark = pytest.mark.gpu
 
@@ -166,3 +168,42 @@ def test_extent_slack_reports_bounds_errors_in_the_checked_build_only(libs):
             swa.swa_debug_extent_slack(0)
     for n in NAMES:
         assert torch.equal(got[n], clean[id(release)][n]), n
+
+
+# ------------------------------------------------- full-size workloads -----
+def _device_inputs(geom, seed, dev):
+    """Seeded device tensors of geom's shapes (values do not matter here:
+    every access the kernels make depends on the shapes alone)."""
+    g = torch.Generator(dev).manual_seed(seed)
+    q = torch.randn(geom.q_shape(), generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn(geom.kv_shape(), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn(geom.kv_shape(), generator=g, device=dev).to(torch.bfloat16)
+    dy = torch.randn(geom.q_shape(), generator=g, device=dev).to(torch.bfloat16)
+    mask = None
+    if geom.keep_prob < 1.0 and not geom.dropout_gen:
+        nbytes = (geom.mask_bits() + 7) // 8
+        mask = torch.randint(0, 256, (nbytes,), generator=g, device=dev, dtype=torch.uint8)
+    return q, k, v, dy, mask
+
+
+@pytest.mark.parametrize("name", WORKLOAD_ORDER)
+def test_full_size_workloads_stay_in_bounds(name, libs):
+    """At each workload's full size (the largest offsets the kernels form),
+    the checked build records no access outside its tensor and matches the
+    release build bit for bit."""
+    geom = workload_geometry(name)
+    dev = torch.device("cuda:0")
+    q, k, v, dy, mask = _device_inputs(geom, 91, dev)
+    res = []
+    for library in libs:
+        with swa.using(library):
+            fws = torch.empty(swa.swa_forward_workspace_size(swa.Params(geom)), dtype=torch.uint8, device=dev)
+            out, smax, ssum = swa.forward(geom, q, k, v, mask, workspace=fws)
+            swa.check_workspace(fws)
+            bws = torch.empty(swa.swa_backward_workspace_size(swa.Params(geom)), dtype=torch.uint8, device=dev)
+            dq, dk, dv = swa.backward(geom, q, k, v, dy, out, smax, ssum, mask, workspace=bws)
+            swa.check_workspace(bws)
+            res.append((out, smax, ssum, dq, dk, dv))
+            del fws, bws
+    for n, a, b in zip(NAMES, *res):
+        assert torch.equal(a, b), (name, n)
