@@ -14,8 +14,9 @@ things are checked here:
   accesses at the tensors' ends count as outside and the status is
   SWA_ERR_BOUNDS, for the forward and for the backward, while the release
   build, which has no checks, ignores the hook;
-- at the full size of each of the five workloads the checked build records
-  nothing and matches the release build bit for bit.
+- at the full size of each of the five workloads, and on the seeded random
+  geometries of the parity sweep (tests/test_parity_random_gpu.py), the
+  checked build records nothing and matches the release build bit for bit.
 """
 import pytest
 import torch
@@ -207,3 +208,31 @@ def test_full_size_workloads_stay_in_bounds(name, libs):
             del fws, bws
     for n, a, b in zip(NAMES, *res):
         assert torch.equal(a, b), (name, n)
+
+
+# ------------------------------------------ the random geometries ------
+def _random_kws():
+    from tests.test_parity_random_gpu import EXTREME, N_CASES, extreme_geometry, random_geometry
+    kws = [(f"random{s}", random_geometry(s)) for s in range(N_CASES)]
+    kws += [(f"extreme{s}", extreme_geometry(s)) for s in range(16)]
+    kws += sorted(EXTREME.items())
+    return kws
+
+
+_RANDOM = dict(_random_kws())
+
+
+@pytest.mark.parametrize("name", list(_RANDOM))
+def test_random_geometries_stay_in_bounds(name, libs):
+    """The seeded random geometries of the parity sweep (empty and ragged
+    TND sequences, GQA / MQA, every head dim, both masks and dropout forms,
+    every element type, scales and key counts outside the workloads'
+    regime): no bounds error in the checked build, the release build's bits."""
+    geom = Geometry(**_RANDOM[name])
+    inp = draw(geom, 97_000 + sum(map(ord, name)))
+    res = []
+    for library in libs:
+        with swa.using(library):
+            res.append(run(inp.geom, inp))
+    for n in NAMES:
+        assert torch.equal(res[0][n], res[1][n]), (name, n)
