@@ -69,61 +69,119 @@ __global__ void __launch_bounds__(256) swa_prep_kernel(const PrepArgs a) {
   }
 }
 
-// The same for D = 64 or 128 exactly, with more bytes in flight: a row is
-// split over D/8 lanes (16 bytes of dY and of O each), a warp covers 32/(D/8)
-// rows per load step and kSteps steps, all loads issued before any use.  The
-// kernel is memory-latency bound (its loads in flight per SM set the rate),
-// so it is held to 64 registers a thread, which fits four blocks of 256
-// threads per SM instead of three: 0.70 -> 0.79 of the measured copy
-// bandwidth on 32 x 32768 rows of D = 128 (0.117 -> 0.103 ms).
+// The same for D = 64 and 128, by bulk copies.  One CTA of 4 warps per chunk of
+// prep_chunk_rows(D) rows: 16 KB of dY, 16 KB of O and the chunk's
+// softmax_max / softmax_sum, fetched by one thread with cp.async.bulk into
+// shared memory.  Six CTAs fit an SM (shared memory), so up to six chunks
+// are in flight per SM without holding them in registers, and the CTAs stay
+// short, so that the grid fills SMs freed by kernels of other streams as
+// they come.  Warp w reduces rows [w*R/4, (w+1)*R/4) of the chunk (4
+// elements per lane, then a butterfly over the row's lanes), lane t ends up
+// holding row t's D and writes D and lse2.
+constexpr int kPrepThreads = 128;
+__host__ __device__ constexpr int prep_chunk_rows(int D) { return 8192 / D; }
+__host__ __device__ constexpr size_t prep_bulk_smem(int D) {
+  return 2 * static_cast<size_t>(prep_chunk_rows(D)) * D * 2 + 2 * static_cast<size_t>(prep_chunk_rows(D)) * 4 + 16;
+}
+static_assert(prep_bulk_smem(64) <= 48 * 1024 && prep_bulk_smem(128) <= 48 * 1024, "default launch limit");
+
+// Bounded wait of the preprocess.  It does not consult the error word, which
+// block 0 of this grid clears at its start, possibly after this block began.
+__device__ __forceinline__ bool prep_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(err, 0, static_cast<int32_t>(kErrPrepLoad));
+      return false;
+    }
+  return true;
+}
+
 template <int D, bool F16>
-__global__ void __launch_bounds__(256, 4) swa_prep_wide_kernel(const PrepArgs a) {
-  constexpr int kLanesPerRow = D / 8;
-  constexpr int kRowsPerStep = 32 / kLanesPerRow;
-  constexpr int kSteps = 4;
-  const int lane = threadIdx.x & 31;
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+__global__ void __launch_bounds__(kPrepThreads) swa_prep_bulk_kernel(const PrepArgs a) {
+  constexpr int kRows = prep_chunk_rows(D);          // 64 or 128
+  constexpr uint32_t kTileBytes = kRows * D * 2;     // 16 KB
+  constexpr int kLanesPerRow = D / 4;                // 8 bytes of each tensor per lane
+  constexpr int kRowsPerIter = 32 / kLanesPerRow;    // 1 or 2 rows per warp step
+  constexpr int kRowsPerWarp = kRows / (kPrepThreads / 32);  // 16 or 32
+  static_assert(kRowsPerWarp <= 32 && kRowsPerWarp % kRowsPerIter == 0, "chunk split");
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint8_t* sdy = smem;
+  const uint8_t* so = smem + kTileBytes;
+  const float* s_max = reinterpret_cast<const float*>(smem + 2 * kTileBytes);
+  const float* s_sum = s_max + kRows;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + 2 * kTileBytes + 2 * kRows * 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kRows;
+  const int nrows = static_cast<int>(a.rows - row0 < kRows ? a.rows - row0 : kRows);
+  const int nstat = nrows & ~3;  // statistics of whole 4-row groups come by bulk copy (16-byte sizes)
+  if (threadIdx.x == 0) {
+    mbar_init(full, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
   griddep_wait();  // dY, O and the statistics come from earlier grids
   griddep_launch_dependents();
   if (!SWA_CHECKS && blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0;  // fresh error word for this backward call
-  const int64_t row0 = warp * (kRowsPerStep * kSteps) + lane / kLanesPerRow;
-  const int col = (lane % kLanesPerRow) * 8;
-  // row r of step k is row0 + k * kRowsPerStep: one base pointer per tensor
-  // and a fixed stride, so the addresses cost one add per load
-  const uint4* pdy = reinterpret_cast<const uint4*>(a.dy + row0 * D + col);
-  const uint4* po = reinterpret_cast<const uint4*>(a.out + row0 * D + col);
-  constexpr int kStride = kRowsPerStep * D / 8;  // uint4 per step
-  const int64_t left = a.rows > row0 ? (a.rows - row0 + kRowsPerStep - 1) / kRowsPerStep : 0;
-  const int nvalid = left < kSteps ? static_cast<int>(left) : kSteps;  // steps whose row exists
-  uint4 dy[kSteps], o[kSteps];
-#pragma unroll
-  for (int k = 0; k < kSteps; ++k) {
-    if (k < nvalid && in_bounds((row0 + k * kRowsPerStep) * D + col, 8, a.g.n_q_elems, a.err)) {
-      dy[k] = __ldg(pdy + k * kStride);
-      o[k] = __ldg(po + k * kStride);
-    } else {
-      dy[k] = o[k] = make_uint4(0u, 0u, 0u, 0u);
+  if (threadIdx.x == 0) {
+    const uint32_t tile = static_cast<uint32_t>(nrows) * D * 2;
+    const bool ok = in_bounds(row0 * D, static_cast<int64_t>(nrows) * D, a.g.n_q_elems, a.err) &&
+                    in_bounds(row0, nstat, a.g.n_stats, a.err);
+    mbar_arrive_expect_tx(full, ok ? 2 * tile + 2 * nstat * 4 : 0);
+    if (ok) {  // (the bounds-checked build skips the chunk; its status reports it)
+      bulk_load(smem, a.dy + row0 * D, tile, full);
+      bulk_load(smem + kTileBytes, a.out + row0 * D, tile, full);
+      if (nstat > 0) {
+        bulk_load(smem + 2 * kTileBytes, a.smax + row0, nstat * 4, full);
+        bulk_load(smem + 2 * kTileBytes + kRows * 4, a.ssum + row0, nstat * 4, full);
+      }
     }
   }
+  if (!prep_wait(full, 0, a.err)) {
+    if (threadIdx.x == 0) mbar_wait_drain(full, 0);  // copies in flight land before the CTA exits
+    return;
+  }
+  float d_mine = 0.f;  // lane t < kRowsPerWarp: D of the warp's row t
 #pragma unroll
-  for (int k = 0; k < kSteps; ++k) {
-    const uint32_t d4[4] = {dy[k].x, dy[k].y, dy[k].z, dy[k].w}, o4[4] = {o[k].x, o[k].y, o[k].z, o[k].w};
-    float acc = 0.f;
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const float2 df = unpack2<F16>(d4[t]), of = unpack2<F16>(o4[t]);
-      acc = fmaf(df.x, of.x, acc);
-      acc = fmaf(df.y, of.y, acc);
-    }
+  for (int it = 0; it < kRowsPerWarp / kRowsPerIter; ++it) {
+    const int r = warp * kRowsPerWarp + it * kRowsPerIter + lane / kLanesPerRow;
+    const int off = (r * D + (lane % kLanesPerRow) * 4) * 2;
+    const uint2 dv = *reinterpret_cast<const uint2*>(sdy + off);
+    const uint2 ov = *reinterpret_cast<const uint2*>(so + off);
+    const float2 d0 = unpack2<F16>(dv.x), d1 = unpack2<F16>(dv.y);
+    const float2 o0 = unpack2<F16>(ov.x), o1 = unpack2<F16>(ov.y);
+    float acc = d0.x * o0.x;
+    acc = fmaf(d0.y, o0.y, acc);
+    acc = fmaf(d1.x, o1.x, acc);
+    acc = fmaf(d1.y, o1.y, acc);
 #pragma unroll
     for (int m = kLanesPerRow / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, m);
-    const int64_t row = row0 + k * kRowsPerStep;
-    if (lane % kLanesPerRow == 0 && k < nvalid) {
-      const int64_t ws = a.g.layout == 0 ? row : (row % a.g.N) * a.g.T_q + row / a.g.N;
-      if (!in_bounds(row, 1, a.g.n_stats, a.err) || !in_bounds(ws, 1, a.g.n_stats, a.err)) continue;
-      const float l = a.ssum[row];
-      a.dsum[ws] = acc;
-      a.lse2[ws] = (l > 0.f) ? a.smax[row] * kLog2e + __log2f(l) : INFINITY;
+    if constexpr (kRowsPerIter == 1) {
+      if (lane == it) d_mine = acc;
+    } else {  // lanes 0-15 hold row 2*it, lanes 16-31 row 2*it + 1; lanes 2*it and 2*it + 1 take them
+      const float other = __shfl_xor_sync(0xFFFFFFFFu, acc, 16);
+      const float even = lane < 16 ? acc : other, odd = lane < 16 ? other : acc;
+      if (lane == 2 * it) d_mine = even;
+      if (lane == 2 * it + 1) d_mine = odd;
+    }
+  }
+  const int rloc = warp * kRowsPerWarp + lane;
+  if (lane < kRowsPerWarp && rloc < nrows) {
+    const int64_t row = row0 + rloc;
+    const int64_t ws = a.g.layout == 0 ? row : (row % a.g.N) * a.g.T_q + row / a.g.N;
+    float m, l;
+    if (rloc < nstat) {
+      m = s_max[rloc];
+      l = s_sum[rloc];
+    } else {  // past the tensor's last whole 4-row group: plain loads
+      const bool in = in_bounds(row, 1, a.g.n_stats, a.err);
+      m = in ? a.smax[row] : 0.f;
+      l = in ? a.ssum[row] : 0.f;
+    }
+    if (in_bounds(ws, 1, a.g.n_stats, a.err)) {
+      a.dsum[ws] = d_mine;
+      a.lse2[ws] = (l > 0.f) ? m * kLog2e + __log2f(l) : INFINITY;
     }
   }
 }
@@ -190,15 +248,12 @@ cudaError_t launch_to_bf16(const float* in, __nv_bfloat16* out, int64_t n, cudaS
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream) {
   if (a.rows == 0) return cudaSuccess;
   if (a.g.D == 64 || a.g.D == 128) {
-    const int64_t rows_per_block = 8 * (32 / (a.g.D / 8)) * 4;  // 8 warps x rows per step x 4 steps
-    const unsigned gr = static_cast<unsigned>((a.rows + rows_per_block - 1) / rows_per_block);
-    if (a.g.D == 64) {
-      if (a.g.f16) return launch_pdl(swa_prep_wide_kernel<64, true>, dim3(gr), dim3(256), 0, stream, a);
-      return launch_pdl(swa_prep_wide_kernel<64, false>, dim3(gr), dim3(256), 0, stream, a);
-    } else {
-      if (a.g.f16) return launch_pdl(swa_prep_wide_kernel<128, true>, dim3(gr), dim3(256), 0, stream, a);
-      return launch_pdl(swa_prep_wide_kernel<128, false>, dim3(gr), dim3(256), 0, stream, a);
-    }
+    const int64_t chunks = (a.rows + prep_chunk_rows(a.g.D) - 1) / prep_chunk_rows(a.g.D);
+    const dim3 grid(static_cast<unsigned>(chunks));
+    const size_t smem = prep_bulk_smem(a.g.D);  // under the 48 KB a launch may use without opting in
+    auto go = [&](auto kernel) { return launch_pdl(kernel, grid, dim3(kPrepThreads), smem, stream, a); };
+    if (a.g.D == 64) return a.g.f16 ? go(swa_prep_bulk_kernel<64, true>) : go(swa_prep_bulk_kernel<64, false>);
+    return a.g.f16 ? go(swa_prep_bulk_kernel<128, true>) : go(swa_prep_bulk_kernel<128, false>);
   }
   const int64_t threads = a.rows * 32;
   const int block = 256;

@@ -20,9 +20,11 @@
 // every copy is a single 2-D copy (rows = batches or tokens, pitch = the full
 // row).
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "swa.h"
@@ -31,6 +33,81 @@
 namespace {
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ------------------------------------------------ streams and events --
+// The internal streams and events of swa_step_host are created once per CUDA
+// context and kept for the life of the process.  Creating and destroying five
+// streams and some seventy events on every call took 0.5 ms of host time, and
+// now and then a call stalled ~9 ms inside those driver calls (measured on the
+// headline workload: one step in a dozen took 16 ms instead of 7.6), delaying
+// the whole step.  A context is told apart by its unique id (cuCtxGetId), so
+// that a context created after cudaDeviceReset gets a set of its own and
+// never touches handles of the destroyed one.  A call holds g_step_mu while
+// it enqueues: another call cannot re-record one of its events before the
+// waits on it are queued.  (Re-recording an event whose earlier record is
+// still pending on the GPU is fine: a wait is bound to the record that
+// preceded it.)
+struct StepStreams {
+  unsigned long long ctx = 0;
+  cudaStream_t s_in = nullptr, s_outs[2] = {nullptr, nullptr}, s_comp[2] = {nullptr, nullptr};
+  std::vector<cudaEvent_t> events;
+};
+std::mutex g_step_mu;
+std::vector<StepStreams*> g_step_sets;  // guarded by g_step_mu; kept until the process exits
+
+// Unique id of the context current on this thread (the runtime's primary
+// context of the current device, made current here if it was not).
+cudaError_t current_context_id(unsigned long long* id) {
+  static std::once_flag once;
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  });
+  if (!get_current || !get_id) return cudaErrorNotSupported;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaSetDevice(dev);  // initialises the primary context and makes it current
+  if (e != cudaSuccess) return e;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
+  if (get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  return cudaSuccess;
+}
+
+// The set of the current context, created on first use.  Call with g_step_mu held.
+cudaError_t step_streams(StepStreams** out) {
+  unsigned long long id = 0;
+  cudaError_t e = current_context_id(&id);
+  if (e != cudaSuccess) return e;
+  for (StepStreams* x : g_step_sets)
+    if (x->ctx == id) {
+      *out = x;
+      return cudaSuccess;
+    }
+  StepStreams* x = new StepStreams;
+  x->ctx = id;
+  e = cudaStreamCreateWithFlags(&x->s_in, cudaStreamNonBlocking);
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&x->s_outs[i], cudaStreamNonBlocking);
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&x->s_comp[i], cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    for (cudaStream_t st : {x->s_in, x->s_outs[0], x->s_outs[1], x->s_comp[0], x->s_comp[1]})
+      if (st) cudaStreamDestroy(st);
+    delete x;
+    return e;
+  }
+  g_step_sets.push_back(x);
+  *out = x;
+  return cudaSuccess;
+}
 
 // Copy geometry of one tensor for one head group: `rows` rows of `width`
 // bytes at `pitch` on the host, packed back to back on the device.
@@ -192,26 +269,24 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
                           P.total, device_bytes);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   // One host -> device stream, two compute streams with a device -> host
-  // stream each, and their events, released by the driver once their work has
-  // run (cudaStreamDestroy / cudaEventDestroy on pending work).
-  cudaStream_t s_in = nullptr, s_outs[2] = {nullptr, nullptr}, s_comp[2] = {nullptr, nullptr};
-  std::vector<cudaEvent_t> ev;
-  auto release = [&]() {
-    for (cudaEvent_t e : ev) cudaEventDestroy(e);
-    if (s_in) cudaStreamDestroy(s_in);
-    for (cudaStream_t x : s_outs)
-      if (x) cudaStreamDestroy(x);
-    for (cudaStream_t x : s_comp)
-      if (x) cudaStreamDestroy(x);
+  // stream each, and events from the context's pool (StepStreams).
+  std::lock_guard<std::mutex> lock(g_step_mu);
+  StepStreams* set = nullptr;
+  cudaError_t e = step_streams(&set);
+  if (e != cudaSuccess) return cuda_fail(e, "setting up the copy streams");
+  cudaStream_t s_in = set->s_in, s_outs[2] = {set->s_outs[0], set->s_outs[1]},
+               s_comp[2] = {set->s_comp[0], set->s_comp[1]};
+  size_t n_ev = 0;  // events of the pool taken by this call
+  auto event = [&](cudaEvent_t* ev) {
+    if (n_ev == set->events.size()) {
+      cudaEvent_t fresh = nullptr;
+      const cudaError_t r = cudaEventCreateWithFlags(&fresh, cudaEventDisableTiming);
+      if (r != cudaSuccess) return r;
+      set->events.push_back(fresh);
+    }
+    *ev = set->events[n_ev++];
+    return cudaSuccess;
   };
-  auto event = [&](cudaEvent_t* e) {
-    const cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
-    if (r == cudaSuccess) ev.push_back(*e);
-    return r;
-  };
-  cudaError_t e = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking);
-  for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&s_outs[i], cudaStreamNonBlocking);
-  for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&s_comp[i], cudaStreamNonBlocking);
   cudaEvent_t start = nullptr, done = nullptr;
   if (e == cudaSuccess) e = event(&start);
   if (e == cudaSuccess) e = event(&done);
@@ -219,10 +294,7 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
   if (e == cudaSuccess) e = cudaEventRecord(start, cs);
   for (cudaStream_t x : {s_in, s_outs[0], s_outs[1], s_comp[0], s_comp[1]})
     if (e == cudaSuccess) e = cudaStreamWaitEvent(x, start, 0);
-  if (e != cudaSuccess) {
-    release();
-    return cuda_fail(e, "setting up the copy streams");
-  }
+  if (e != cudaSuccess) return cuda_fail(e, "setting up the copy streams");
   uint8_t* base = static_cast<uint8_t*>(device_buffer);
   for (size_t u = 0; u < P.units.size(); ++u) {
     const Layout& L = *P.units[u].L;
@@ -285,7 +357,6 @@ swa_status_t swa_step_host(const swa_params_t* p, int chunks, const void* q, con
   if (e_end == cudaSuccess) e_end = cudaEventRecord(done2, s_outs[1]);
   if (e_end == cudaSuccess) e_end = cudaStreamWaitEvent(cs, done2, 0);
   if (e == cudaSuccess) e = e_end;
-  release();
   if (st != SWA_OK) return st;
   if (e != cudaSuccess) return cuda_fail(e, "host step copies");
   return SWA_OK;

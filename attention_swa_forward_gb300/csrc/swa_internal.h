@@ -75,8 +75,7 @@ cudaError_t set_smem_limit(Kernel kernel, size_t smem, std::atomic<uint64_t>& do
   return e;
 }
 
-// Error codes a kernel stores into WsHeader::error.
-// 1: the bounds-checked build (libswa_checked.so), whose kernels test every
+// SWA_CHECKS = 1: the bounds-checked build (libswa_checked.so), whose kernels test every
 // global load and store against its tensor's extent and record kErrBounds
 // instead of making it.  Its host code clears the status word with a memset
 // before a call's first launch, so that no grid's clear can race with a
@@ -85,6 +84,7 @@ cudaError_t set_smem_limit(Kernel kernel, size_t smem, std::atomic<uint64_t>& do
 #define SWA_CHECKS 0
 #endif
 
+// Error codes a kernel stores into WsHeader::error.
 enum : int32_t {
   kErrFwdLoad = 1,
   kErrFwdMma = 2,
@@ -92,6 +92,7 @@ enum : int32_t {
   kErrBwdLoad = 11,
   kErrBwdMma = 12,
   kErrBwdCompute = 13,
+  kErrPrepLoad = 14,  // the preprocess's wait for a chunk of dY / O
   kErrBounds = 21,  // bounds-checked build: an access outside its tensor was skipped
 };
 

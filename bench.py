@@ -391,7 +391,7 @@ def run_swa(args, name: str):
         for _ in range(max(3, args.warmup)):
             e2e_step()
         torch.cuda.synchronize(dev)
-        n_e2e = max(3, min(args.steps, 10))
+        n_e2e = max(3, args.steps)
         barrier(ws)
         t0 = time.perf_counter()
         for _ in range(n_e2e):
@@ -400,7 +400,7 @@ def run_swa(args, name: str):
         t_e2e = (time.perf_counter() - t0) / n_e2e
         t_e2e = max_over_ranks(t_e2e, ws, dev)
         e2e = {"value": whole_job_value(fl["total"], ws, t_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
+               "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3, "steps": n_e2e,
                "api": f"swa_step_host, {chunks} head groups" if chunks else "copies + swa_forward / swa_backward"}
         if chunks:
             swa.check_step_host(g, chunks, step_buf, stream)
@@ -445,7 +445,7 @@ def run_swa(args, name: str):
     prep_bytes = rows * (2 * g.D * 2 + 4 * 4)
     hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     prep_gbs = prep_bytes / (prep_ms / 1e3) / 1e9
-    memory_bound = {"kernel": "swa_prep_wide_kernel" if g.D in (64, 128) else "swa_prep_kernel", "bound": "hbm",
+    memory_bound = {"kernel": "swa_prep_bulk_kernel" if g.D in (64, 128) else "swa_prep_kernel", "bound": "hbm",
                     "ms": prep_ms, "bytes": prep_bytes, "achieved": prep_gbs, "peak": hbm_peak, "unit": "GB/s",
                     "frac": prep_gbs / hbm_peak, "peak_source": f"{source} hbm_gbs"}
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

@@ -219,7 +219,10 @@ SWA_API swa_status_t swa_backward_noalloc(const swa_params_t *p, const void *q, 
  * out and statistics go back while its backward runs.  Consecutive groups
  * compute on two further internal streams in turn, so one group's kernels
  * may start while the previous group's last CTAs still run; each of those
- * has its own device -> host stream.
+ * has its own device -> host stream.  The five internal streams and their
+ * events are created by the first call in a CUDA context and kept until the
+ * process exits; calls in one context share them (their enqueueing is
+ * serialised by a lock, and their GPU work runs one call after the other).
  * Heads are independent, so the results equal those of one swa_forward +
  * swa_backward on device copies of the same tensors, bit for bit.
  *   q, k, v, dy   host, p->dtype, shapes and layout as for swa_forward /
