@@ -107,8 +107,9 @@ __device__ __forceinline__ void tma_rows(uint8_t* dst, const CUtensorMap* map, u
 // against the extent of its tensor first (Geometry::n_*): an access outside
 // it is skipped and kErrBounds recorded in the status word, so an indexing
 // or scheduling error shows up as a status instead of as a memory fault.
-// The release build compiles the tests away.  (TMA copies need no test: the
-// tensor maps bound them.)  SWA_CHECKS itself is set in swa_internal.h.
+// The release build compiles the tests away.  (Tiled TMA copies need no
+// test: the tensor maps bound them.  The preprocess's untiled bulk copies
+// are tested.)  SWA_CHECKS itself is set in swa_internal.h.
 __device__ __forceinline__ bool in_bounds(int64_t first, int64_t count, int64_t extent, int32_t* err) {
   if constexpr (SWA_CHECKS == 0) {
     return true;
