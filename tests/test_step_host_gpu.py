@@ -64,3 +64,63 @@ def test_step_host_rejects_bad_chunks():
     with pytest.raises(swa.SwaError):
         swa.swa_step_host_buffer_size(swa.Params(drop), 2)
     assert swa.swa_step_host_buffer_size(swa.Params(drop), 1) > 0
+
+
+def test_concurrent_host_steps_share_the_internal_streams():
+    """Two host threads call swa_step_host at once, each on its own stream,
+    host tensors and device buffer, three times in a row.  The calls share
+    the context's internal streams and events (their enqueueing is
+    serialised, their GPU work runs one after the other): every result is
+    the serial call's, bit for bit, and repeated calls reuse the events."""
+    import threading
+
+    kws = [dict(layout="BNSD", B=1, N=8, D=128, S_q=300, S_kv=300, scale=0.09, sparse_mode=4, pre_tokens=100,
+                next_tokens=20),
+           dict(layout="TND", B=3, N=4, D=64, cu_seqlens_q=[130, 130, 400], cu_seqlens_kv=[130, 130, 400],
+                scale=0.125, sparse_mode=0)]
+    chunks = [4, 2]
+    geoms = [Geometry(**kw) for kw in kws]
+    inputs = [draw(g, 78 + i) for i, g in enumerate(geoms)]
+    hosts = [tuple(t.pin_memory() for t in (inp.q, inp.k, inp.v, inp.dy)) for inp in inputs]
+
+    def outputs(g, inp):
+        st = tuple(g.stat_shape())
+        return [torch.full(inp.q.shape, float("nan"), dtype=inp.q.dtype).pin_memory(),
+                torch.full(st, float("nan")).pin_memory(), torch.full(st, float("nan")).pin_memory(),
+                torch.full(inp.q.shape, float("nan"), dtype=inp.q.dtype).pin_memory(),
+                torch.full(inp.k.shape, float("nan"), dtype=inp.k.dtype).pin_memory(),
+                torch.full(inp.v.shape, float("nan"), dtype=inp.v.dtype).pin_memory()]
+
+    serial = []
+    for g, inp, h, c in zip(geoms, inputs, hosts, chunks):
+        got = outputs(g, inp)
+        buf = swa.step_host(g, *h, *got, chunks=c)
+        torch.cuda.synchronize()
+        swa.check_step_host(g, c, buf)
+        serial.append(got)
+    results = [[None] * 3 for _ in geoms]
+    errors = []
+
+    def worker(t):
+        try:
+            stream = torch.cuda.Stream()
+            buf = None
+            for rep in range(3):
+                got = outputs(geoms[t], inputs[t])
+                buf = swa.step_host(geoms[t], *hosts[t], *got, chunks=chunks[t], device_buffer=buf, stream=stream)
+                stream.synchronize()
+                swa.check_step_host(geoms[t], chunks[t], buf, stream)
+                results[t][rep] = got
+        except Exception as e:  # surfaced below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(len(geoms))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for t in range(len(geoms)):
+        for rep in range(3):
+            for a, b, n in zip(results[t][rep], serial[t], ("out", "softmax_max", "softmax_sum", "dq", "dk", "dv")):
+                assert torch.equal(a, b), (t, rep, n)
