@@ -55,8 +55,9 @@ struct StepStreams {
 std::mutex g_step_mu;
 std::vector<StepStreams*> g_step_sets;  // guarded by g_step_mu; kept until the process exits
 
-// Unique id of the context current on this thread (the runtime's primary
-// context of the current device, made current here if it was not).
+// Unique id of the context current on this thread: the caller's own context
+// if it made one current, else the runtime's primary context of the current
+// device, which the runtime makes current on its first use in the thread.
 cudaError_t current_context_id(unsigned long long* id) {
   static std::once_flag once;
   static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
@@ -73,12 +74,13 @@ cudaError_t current_context_id(unsigned long long* id) {
       get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
   });
   if (!get_current || !get_id) return cudaErrorNotSupported;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaSetDevice(dev);  // initialises the primary context and makes it current
-  if (e != cudaSuccess) return e;
   CUcontext ctx = nullptr;
-  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
+  if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (!ctx) {  // no context current yet: a no-op runtime call binds the primary one
+    const cudaError_t e = cudaFree(nullptr);
+    if (e != cudaSuccess) return e;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
+  }
   if (get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
   return cudaSuccess;
 }
