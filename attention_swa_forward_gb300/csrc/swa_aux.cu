@@ -21,63 +21,17 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
   else return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
 }
 
-// One warp per row; each lane handles DP/32 consecutive elements of a row of
-// D <= DP elements (D a multiple of 8: a lane's elements lie all below D or
-// all past it).
-template <int DP, bool F16>
-__global__ void __launch_bounds__(256) swa_prep_kernel(const PrepArgs a) {
-  constexpr int kPer = DP / 32;  // 2 or 4 elements per lane
-  const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  griddep_wait();  // dY, O and the statistics come from earlier grids
-  griddep_launch_dependents();
-  if (!SWA_CHECKS && blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0;  // fresh error word for this backward call
-  if (row >= a.rows) return;
-  const int D = a.g.D;
-  const int64_t base = row * D + lane * kPer;
-  float acc = 0.f;
-  if (lane * kPer >= D || !in_bounds(base, kPer, a.g.n_q_elems, a.err)) {
-    // past the row's last element
-  } else if (kPer == 4) {
-    const uint2 dy = __ldg(reinterpret_cast<const uint2*>(a.dy + base));
-    const uint2 o = __ldg(reinterpret_cast<const uint2*>(a.out + base));
-    const uint32_t d2[2] = {dy.x, dy.y}, o2[2] = {o.x, o.y};
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      const float2 df = unpack2<F16>(d2[t]);
-      const float2 of = unpack2<F16>(o2[t]);
-      acc = fmaf(df.x, of.x, acc);
-      acc = fmaf(df.y, of.y, acc);
-    }
-  } else {
-    const uint32_t dy = __ldg(reinterpret_cast<const uint32_t*>(a.dy + base));
-    const uint32_t o = __ldg(reinterpret_cast<const uint32_t*>(a.out + base));
-    const float2 df = unpack2<F16>(dy);
-    const float2 of = unpack2<F16>(o);
-    acc = fmaf(df.x, of.x, acc);
-    acc = fmaf(df.y, of.y, acc);
-  }
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, m);
-  if (lane == 0) {
-    // workspace position: head-major (row = t*N + n in TND, already head-major in BNSD)
-    const int64_t ws = a.g.layout == 0 ? row : (row % a.g.N) * a.g.T_q + row / a.g.N;
-    if (!in_bounds(row, 1, a.g.n_stats, a.err) || !in_bounds(ws, 1, a.g.n_stats, a.err)) return;
-    const float l = a.ssum[row];
-    a.dsum[ws] = acc;
-    a.lse2[ws] = (l > 0.f) ? a.smax[row] * kLog2e + __log2f(l) : INFINITY;
-  }
-}
-
-// The same for D = 64 and 128, by bulk copies.  One CTA of 4 warps per chunk of
-// prep_chunk_rows(D) rows: 16 KB of dY, 16 KB of O and the chunk's
+// D = rowsum(dY * O) and lse2 per query row, by bulk copies.  One CTA of 4
+// warps per chunk of prep_chunk_rows(DP) rows (DP = 64 or 128, the head dim
+// rounded up to one of them): up to 16 KB of dY, 16 KB of O and the chunk's
 // softmax_max / softmax_sum, fetched by one thread with cp.async.bulk into
 // shared memory.  Six CTAs fit an SM (shared memory), so up to six chunks
 // are in flight per SM without holding them in registers, and the CTAs stay
 // short, so that the grid fills SMs freed by kernels of other streams as
 // they come.  Warp w reduces rows [w*R/4, (w+1)*R/4) of the chunk (4
-// elements per lane, then a butterfly over the row's lanes), lane t ends up
-// holding row t's D and writes D and lse2.
+// elements per lane over DP/4 lanes, those past D idle, then a butterfly
+// over the row's lanes), lane t ends up holding row t's D and writes D and
+// lse2.  kExact: D == DP, known at compile time.
 constexpr int kPrepThreads = 128;
 __host__ __device__ constexpr int prep_chunk_rows(int D) { return 8192 / D; }
 __host__ __device__ constexpr size_t prep_bulk_smem(int D) {
@@ -98,14 +52,15 @@ __device__ __forceinline__ bool prep_wait(uint64_t* bar, uint32_t parity, int32_
   return true;
 }
 
-template <int D, bool F16>
+template <int DP, bool F16, bool kExact>
 __global__ void __launch_bounds__(kPrepThreads) swa_prep_bulk_kernel(const PrepArgs a) {
-  constexpr int kRows = prep_chunk_rows(D);          // 64 or 128
-  constexpr uint32_t kTileBytes = kRows * D * 2;     // 16 KB
-  constexpr int kLanesPerRow = D / 4;                // 8 bytes of each tensor per lane
+  constexpr int kRows = prep_chunk_rows(DP);         // 64 or 128
+  constexpr uint32_t kTileBytes = kRows * DP * 2;    // 16 KB: the stage of each tensor
+  constexpr int kLanesPerRow = DP / 4;               // 8 bytes of each tensor per lane
   constexpr int kRowsPerIter = 32 / kLanesPerRow;    // 1 or 2 rows per warp step
   constexpr int kRowsPerWarp = kRows / (kPrepThreads / 32);  // 16 or 32
   static_assert(kRowsPerWarp <= 32 && kRowsPerWarp % kRowsPerIter == 0, "chunk split");
+  const int D = kExact ? DP : a.g.D;  // a multiple of 8, at most DP
   extern __shared__ __align__(128) uint8_t smem[];
   const uint8_t* sdy = smem;
   const uint8_t* so = smem + kTileBytes;
@@ -146,9 +101,13 @@ __global__ void __launch_bounds__(kPrepThreads) swa_prep_bulk_kernel(const PrepA
 #pragma unroll
   for (int it = 0; it < kRowsPerWarp / kRowsPerIter; ++it) {
     const int r = warp * kRowsPerWarp + it * kRowsPerIter + lane / kLanesPerRow;
-    const int off = (r * D + (lane % kLanesPerRow) * 4) * 2;
-    const uint2 dv = *reinterpret_cast<const uint2*>(sdy + off);
-    const uint2 ov = *reinterpret_cast<const uint2*>(so + off);
+    const int c = (lane % kLanesPerRow) * 4;  // first of the lane's 4 elements
+    const int off = (r * D + c) * 2;
+    uint2 dv = make_uint2(0u, 0u), ov = make_uint2(0u, 0u);
+    if (kExact || c < D) {
+      dv = *reinterpret_cast<const uint2*>(sdy + off);
+      ov = *reinterpret_cast<const uint2*>(so + off);
+    }
     const float2 d0 = unpack2<F16>(dv.x), d1 = unpack2<F16>(dv.y);
     const float2 o0 = unpack2<F16>(ov.x), o1 = unpack2<F16>(ov.y);
     float acc = d0.x * o0.x;
@@ -247,26 +206,18 @@ cudaError_t launch_to_bf16(const float* in, __nv_bfloat16* out, int64_t n, cudaS
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream) {
   if (a.rows == 0) return cudaSuccess;
-  if (a.g.D == 64 || a.g.D == 128) {
-    const int64_t chunks = (a.rows + prep_chunk_rows(a.g.D) - 1) / prep_chunk_rows(a.g.D);
-    const dim3 grid(static_cast<unsigned>(chunks));
-    const size_t smem = prep_bulk_smem(a.g.D);  // under the 48 KB a launch may use without opting in
-    auto go = [&](auto kernel) { return launch_pdl(kernel, grid, dim3(kPrepThreads), smem, stream, a); };
-    if (a.g.D == 64) return a.g.f16 ? go(swa_prep_bulk_kernel<64, true>) : go(swa_prep_bulk_kernel<64, false>);
-    return a.g.f16 ? go(swa_prep_bulk_kernel<128, true>) : go(swa_prep_bulk_kernel<128, false>);
+  const int DP = a.g.D <= 64 ? 64 : 128;
+  const int64_t chunks = (a.rows + prep_chunk_rows(DP) - 1) / prep_chunk_rows(DP);
+  const dim3 grid(static_cast<unsigned>(chunks));
+  const size_t smem = prep_bulk_smem(DP);  // under the 48 KB a launch may use without opting in
+  auto go = [&](auto kernel) { return launch_pdl(kernel, grid, dim3(kPrepThreads), smem, stream, a); };
+  const bool exact = a.g.D == DP;
+  if (DP == 64) {
+    if (exact) return a.g.f16 ? go(swa_prep_bulk_kernel<64, true, true>) : go(swa_prep_bulk_kernel<64, false, true>);
+    return a.g.f16 ? go(swa_prep_bulk_kernel<64, true, false>) : go(swa_prep_bulk_kernel<64, false, false>);
   }
-  const int64_t threads = a.rows * 32;
-  const int block = 256;
-  const int64_t grid = (threads + block - 1) / block;
-  const unsigned gr = static_cast<unsigned>(grid);
-  if (a.g.D <= 64) {
-    if (a.g.f16) return launch_pdl(swa_prep_kernel<64, true>, dim3(gr), dim3(block), 0, stream, a);
-    return launch_pdl(swa_prep_kernel<64, false>, dim3(gr), dim3(block), 0, stream, a);
-  } else {
-    if (a.g.f16) return launch_pdl(swa_prep_kernel<128, true>, dim3(gr), dim3(block), 0, stream, a);
-    return launch_pdl(swa_prep_kernel<128, false>, dim3(gr), dim3(block), 0, stream, a);
-  }
-  return cudaGetLastError();
+  if (exact) return a.g.f16 ? go(swa_prep_bulk_kernel<128, true, true>) : go(swa_prep_bulk_kernel<128, false, true>);
+  return a.g.f16 ? go(swa_prep_bulk_kernel<128, true, false>) : go(swa_prep_bulk_kernel<128, false, false>);
 }
 
 }  // namespace swa

@@ -445,7 +445,7 @@ def run_swa(args, name: str):
     prep_bytes = rows * (2 * g.D * 2 + 4 * 4)
     hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     prep_gbs = prep_bytes / (prep_ms / 1e3) / 1e9
-    memory_bound = {"kernel": "swa_prep_bulk_kernel" if g.D in (64, 128) else "swa_prep_kernel", "bound": "hbm",
+    memory_bound = {"kernel": "swa_prep_bulk_kernel", "bound": "hbm",
                     "ms": prep_ms, "bytes": prep_bytes, "achieved": prep_gbs, "peak": hbm_peak, "unit": "GB/s",
                     "frac": prep_gbs / hbm_peak, "peak_source": f"{source} hbm_gbs"}
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

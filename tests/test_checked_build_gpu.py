@@ -5,7 +5,7 @@ caller's tensor before making it; an access outside it is skipped and the
 call's status word reports SWA_ERR_BOUNDS instead of a memory fault.  Two
 things are checked here:
 - on cases that reach every kernel variant (both layouts, one-tile and pair
-  forward, both preprocess kernels, stored and generated dropout, each
+  forward, the preprocess at exact and padded head dims, stored and generated dropout, each
   element type, GQA, the head-group host step and the no-alloc backward)
   the checked build finds no access outside its tensor and computes the
   release build's results bit for bit: the checks only skip, they change no
@@ -59,7 +59,7 @@ CASES = {
     "tnd_d64_gqa_mask": dict(layout="TND", B=4, N=4, N_kv=2, D=64, cu_seqlens_q=[200, 200, 531, 700],
                              cu_seqlens_kv=[150, 150, 600, 777], scale=0.125, sparse_mode=4, pre_tokens=96,
                              next_tokens=40, keep_prob=0.9),
-    # D = 40: narrow preprocess, fp32 storage, generated dropout
+    # D = 40: the preprocess with lanes past D idle, fp32 storage, generated dropout
     "bnsd_d40_fp32_gendrop": dict(layout="BNSD", B=1, N=3, D=40, S_q=333, S_kv=270, scale=40 ** -0.5,
                                   sparse_mode=0, keep_prob=0.85, dropout_gen=1, dropout_seed=3, dropout_offset=7,
                                   dtype="fp32"),
