@@ -69,6 +69,29 @@ def test_checked_build_exports_the_same_symbols():
     assert swa.lib() is not checked
 
 
+def test_library_choice_is_per_thread_and_restored():
+    """using() routes only the calling thread, nests, and restores the
+    previous choice on exit, also when the body raises."""
+    import threading
+
+    release = swa.lib()
+    B.build(checked=True)
+    checked = swa.checked_lib()
+    seen = []
+    with swa.using(checked):
+        t = threading.Thread(target=lambda: seen.append(swa.lib()))
+        t.start()
+        t.join()
+        with swa.using(release):
+            assert swa.lib() is release
+        assert swa.lib() is checked
+    assert seen == [release]
+    with pytest.raises(RuntimeError):
+        with swa.using(checked):
+            raise RuntimeError("inside")
+    assert swa.lib() is release
+
+
 def test_ctypes_struct_matches_c_layout(tmp_path):
     src = tmp_path / "layout.c"
     src.write_text(
