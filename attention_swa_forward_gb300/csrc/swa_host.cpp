@@ -38,9 +38,9 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 // The internal streams and events of swa_step_host are created once per CUDA
 // context and kept for the life of the process.  Creating and destroying five
 // streams and some seventy events on every call took 0.5 ms of host time, and
-// now and then a call stalled ~9 ms inside those driver calls (measured on the
-// headline workload: one step in a dozen took 16 ms instead of 7.6), delaying
-// the whole step.  A context is told apart by its unique id (cuCtxGetId), so
+// now and then a call stalled ~9 ms inside those driver calls (measured on
+// BNSD 1x32x32768x128 in 16 head groups: one step in a dozen took 16 ms
+// instead of 7.6), delaying the whole step.  A context is told apart by its unique id (cuCtxGetId), so
 // that a context created after cudaDeviceReset gets a set of its own and
 // never touches handles of the destroyed one.  A call holds g_step_mu while
 // it enqueues: another call cannot re-record one of its events before the
