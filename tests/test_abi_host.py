@@ -249,6 +249,25 @@ def test_fp32_workspace_holds_bf16_copies(lib):
     assert _size(g16)[1] == 256 and _size(g16, backward=True)[1] == 256 + stats
 
 
+def test_step_host_rejects_bad_arguments_before_any_device_work(lib):
+    """swa_step_host checks its arguments on the host and returns before it
+    touches a stream (no GPU is needed to see these statuses)."""
+    g = Geometry("BNSD", 1, 4, 64, S_q=128, S_kv=128, scale=0.125, sparse_mode=0)
+    p = swa.Params(g)
+    need = swa.swa_step_host_buffer_size(p, 2)
+    fake, buf = 1 << 20, 1 << 24  # never dereferenced: every case fails its checks first
+    L = swa.lib()
+    args = lambda **kw: [kw.get(n, fake) for n in ("q", "k", "v", "dy", "out", "smax", "ssum", "dq", "dk", "dv")]
+    call = lambda chunks, a, b, n: L.swa_step_host(p.ref(), chunks, *a, b, n, None)
+    assert call(2, args(dq=None), buf, need) == swa.SWA_ERR_PARAM_NULLPTR
+    assert call(2, args(q=None), buf, need) == swa.SWA_ERR_PARAM_NULLPTR
+    assert call(2, args(), None, need) == swa.SWA_ERR_WORKSPACE
+    assert call(2, args(), buf, need - 1) == swa.SWA_ERR_WORKSPACE
+    assert call(2, args(), buf + 16, need) == swa.SWA_ERR_WORKSPACE  # not 256-byte aligned
+    assert call(3, args(), buf, need) == swa.SWA_ERR_PARAM_INVALID  # 3 does not divide N = 4
+    assert call(0, args(), buf, need) == swa.SWA_ERR_PARAM_INVALID
+
+
 def test_step_host_buffer_sizes(lib):
     """swa_step_host's device buffer: per pipeline unit, compact copies of q,
     k, v, dy, out, dq, dk, dv and the statistics plus that unit's workspaces.
