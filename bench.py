@@ -392,15 +392,25 @@ def run_swa(args, name: str):
             e2e_step()
         torch.cuda.synchronize(dev)
         n_e2e = max(3, args.steps)
+        # events around each step on the caller's stream give its duration
+        # (steps run one after the other: each starts behind the last one's
+        # results); the figure is the wall-clock mean, the median and the
+        # slowest step show whether a rare stalled step is in it
+        step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n_e2e)]
         barrier(ws)
         t0 = time.perf_counter()
-        for _ in range(n_e2e):
+        for e_begin, e_end in step_ev:
+            e_begin.record(stream)
             e2e_step()
+            e_end.record(stream)
         torch.cuda.synchronize(dev)
         t_e2e = (time.perf_counter() - t0) / n_e2e
         t_e2e = max_over_ranks(t_e2e, ws, dev)
+        per_step = sorted(a.elapsed_time(b) for a, b in step_ev)
         e2e = {"value": whole_job_value(fl["total"], ws, t_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3, "steps": n_e2e,
+               "step_ms_median": per_step[len(per_step) // 2], "step_ms_max": per_step[-1],
                "api": f"swa_step_host, {chunks} head groups" if chunks else "copies + swa_forward / swa_backward"}
         if chunks:
             swa.check_step_host(g, chunks, step_buf, stream)
